@@ -1,0 +1,180 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts decode-layer forward.
+ *
+ * One library, libmoe_gb300.so, computes the MoE layer of a decoder for a
+ * decode-sized batch of N tokens (N = 1..256 and beyond), on one GPU:
+ *
+ *   router   logits[t,e] = sum_h x[t,h] * Wr[e,h]                 (fp32)
+ *   top-k    softmax: rank logits, p = softmax over all E logits;
+ *            sigmoid+bias: rank sigmoid(l)+bias, p = sigmoid(l);
+ *            w = p / sum_topk p if norm_topk_prob; w *= routed_scaling_factor
+ *   experts  per (token t, slot j), e = idx[t,j]:
+ *            d = Wd[e] (SiLU(Wg[e] x_t) * (Wu[e] x_t)),  SiLU(g) = g/(1+exp(-g))
+ *   shared   ds = the same SwiGLU with the shared expert's three matrices
+ *   blend    out[t] = sum_j w[t,j] d[t,j] + g_s ds,
+ *            g_s = sigmoid(x_t . shared_gate_w), or 1 without a gate weight
+ *
+ * The operation is the one the pages "metrale_model_layers/layers/moe/forward.rs"
+ * (MoeLayer::forward: gate, topk, exp_gate_up, exp_silu_down and wsum_blend
+ * steps), "spark_model/layers/moe/forward_token_major.rs"
+ * (forward_token_major_decode: gate GEMM, batched top-k, gate+up, silu+down,
+ * weighted sum and blend for N tokens) and
+ * "metrale_model_layers/layers/moe/forward_fp8_grouped_router.rs"
+ * (grouped_route: router logits and top-k written as [m*top_k] indices and
+ * fp32 weights) describe.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer marked "device" is a CUDA device (or managed) address on the
+ *    current device; the caller owns every buffer (weights, input, outputs,
+ *    workspace).  The library never allocates, frees or synchronises: each call
+ *    only enqueues kernels on `stream` and returns.
+ *  - Device pointers must be 16-byte aligned (MOE_ERR_ALIGNMENT otherwise).
+ *  - All arguments are validated on the host before anything is enqueued; an
+ *    error status means nothing was launched.  There is no fallback path: a
+ *    configuration the kernels do not cover is refused by name
+ *    (MOE_ERR_UNSUPPORTED), never computed some other way.
+ *  - Asynchronous device faults are not reported by the call that enqueued
+ *    the work; they surface from the next CUDA call as usual.
+ *  - n == 0 is a valid no-op (MOE_OK, nothing launched).
+ *  - The workspace is scratch the layer reuses across its steps; its content
+ *    is not meaningful between calls.  Two calls that run at the same time on
+ *    the GPU must not share a workspace.
+ *
+ * Tensor layouts (row-major, C order)
+ * -----------------------------------
+ *  x            BF16  [N, H]
+ *  router_w     BF16  [E, H]  (each expert's router row contiguous)
+ *  routed gate, up:   [E, I, H];  routed down: [E, H, I]
+ *  shared gate, up:   [1, S, H];  shared down: [1, H, S]
+ *  For a stacked [E, out, in] matrix the formats are
+ *   MOE_W_BF16      w: BF16 [E, out, in]; scale, scale2 unused (NULL)
+ *   MOE_W_FP8_B128  w: FP8 E4M3 bytes [E, out, in];
+ *                   scale: fp32 [E, ceil(out/128), ceil(in/128)];
+ *                   value = e4m3(w) * scale[o/128][i/128]
+ *   MOE_W_NVFP4     w: bytes [E, out, in/2], two E2M1 codes per byte, the
+ *                   element with even `in` index in the low nibble;
+ *                   scale: FP8 E4M3 bytes [E, out, in/16] (one per 16 elements);
+ *                   scale2: fp32 [E];
+ *                   value = e2m1(code) * e4m3(scale[o][i/16]) * scale2[e]
+ *  idx          int32 [N, k], slots in descending selection score
+ *  w            fp32  [N, k]
+ *  logits       fp32  [N, E]
+ *  out          BF16  [N, H] (round to nearest even from fp32)
+ */
+#ifndef MOE_GB300_MOE_H
+#define MOE_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+/* A CUDA stream handle (the same object as cudaStream_t; NULL = legacy default stream). */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_NULL = 1,            /* a required pointer is NULL                              */
+    MOE_ERR_INVALID_CONFIG = 2,  /* a size, enum or flag is out of range or inconsistent    */
+    MOE_ERR_UNSUPPORTED = 3,     /* valid, but outside what the kernels cover (named refusal)*/
+    MOE_ERR_WORKSPACE = 4,       /* workspace missing or smaller than moe_workspace_bytes()  */
+    MOE_ERR_CUDA = 5,            /* a CUDA call failed while enqueueing (cudaGetLastError)   */
+    MOE_ERR_ALIGNMENT = 6,       /* a device pointer is not 16-byte aligned                  */
+    MOE_ERR_ALIAS = 7            /* `out` overlaps `x`                                       */
+} moe_status_t;
+
+typedef enum { MOE_ROUTE_SOFTMAX = 0, MOE_ROUTE_SIGMOID_BIAS = 1 } moe_routing_t;
+typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_B128 = 1, MOE_W_NVFP4 = 2 } moe_wfmt_t;
+/* Expert-stage algorithm.  AUTO: token-major for N <= 16, expert-grouped
+ * tensor-core GEMM above.  The two explicit values force one (tests). */
+typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_TOKEN_MAJOR = 1, MOE_PATH_GROUPED = 2 } moe_path_t;
+
+/* Layer configuration (the config fields hidden_size, num_experts,
+ * num_experts_per_tok, moe_intermediate_size, shared_expert_intermediate_size,
+ * norm_topk_prob and routed_scaling_factor of the pages' layer).
+ * Limits: 1 <= num_experts <= 1024; 1 <= top_k <= min(num_experts, 32);
+ * hidden, inter > 0 and multiples of 32; shared_inter >= 0 and a multiple of 32
+ * (0 = no shared expert); routed_scaling_factor finite. */
+typedef struct {
+    int32_t hidden;                 /* H */
+    int32_t num_experts;            /* E */
+    int32_t top_k;                  /* k */
+    int32_t inter;                  /* I  (routed expert intermediate size) */
+    int32_t shared_inter;           /* S  (shared expert intermediate size; 0 = none) */
+    int32_t routing;                /* moe_routing_t */
+    int32_t norm_topk_prob;         /* 0 or 1 */
+    float   routed_scaling_factor;
+    int32_t expert_fmt;             /* moe_wfmt_t: routed and shared experts alike */
+    int32_t path;                   /* moe_path_t */
+} moe_config_t;
+
+/* One stacked expert matrix (device pointers; see the layouts above). */
+typedef struct {
+    const void*  w;
+    const void*  scale;    /* FP8: fp32 block scales; NVFP4: E4M3 bytes; BF16: NULL */
+    const float* scale2;   /* NVFP4 only: fp32 [E]; else NULL */
+} moe_qmat_t;
+
+/* All weights of one layer (device pointers).  The shared-expert matrices are
+ * ignored (may be NULL) when shared_inter == 0. */
+typedef struct {
+    const void*  router_w;          /* BF16 [E, H] */
+    const float* correction_bias;   /* fp32 [E]; required for SIGMOID_BIAS, must be NULL for SOFTMAX */
+    moe_qmat_t   gate, up, down;    /* routed experts */
+    moe_qmat_t   sh_gate, sh_up, sh_down;   /* shared expert (E = 1) */
+    const void*  shared_gate_w;     /* BF16 [H] or NULL (then the shared gate is 1) */
+} moe_weights_t;
+
+/* Bytes of workspace a call with up to `max_tokens` tokens needs (a multiple
+ * of 256).  Returns 0 if `cfg` is NULL or invalid, or max_tokens < 0. */
+size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t max_tokens);
+
+/* Router and top-k for n tokens (the pages' gate and topk steps, grouped_route).
+ *   x       device BF16 [n, H]
+ *   idx     device int32 [n, k]   (out) selected experts, descending score
+ *   w       device fp32  [n, k]   (out) routing weights
+ *   logits  device fp32  [n, E]   (out, optional: NULL = not returned)
+ *   ws      device workspace of at least moe_workspace_bytes(cfg, n) bytes
+ * Errors: MOE_ERR_NULL, MOE_ERR_INVALID_CONFIG, MOE_ERR_UNSUPPORTED,
+ * MOE_ERR_WORKSPACE, MOE_ERR_ALIGNMENT, MOE_ERR_CUDA. */
+moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* wts,
+                       const void* x, int32_t n,
+                       int32_t* idx, float* w, float* logits,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Routed experts, shared expert and blend for n tokens given their routing
+ * (the pages' exp_gate_up, exp_silu_down and wsum_blend steps).
+ *   x     device BF16 [n, H]
+ *   idx   device int32 [n, k]; every entry must lie in [0, E) (not checked on
+ *         the device; an out-of-range index reads outside the weights)
+ *   w     device fp32  [n, k]
+ *   out   device BF16 [n, H] (out); must not overlap x
+ * Errors: as moe_route, plus MOE_ERR_ALIAS. */
+moe_status_t moe_experts(const moe_config_t* cfg, const moe_weights_t* wts,
+                         const void* x, int32_t n,
+                         const int32_t* idx, const float* w,
+                         void* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The whole layer: moe_route then moe_experts on one stream.
+ *   idx, w  optional device outputs ([n, k] int32 / fp32); NULL = kept in the
+ *           workspace only. */
+moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* wts,
+                         const void* x, int32_t n, void* out,
+                         int32_t* idx, float* w,
+                         void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char* moe_status_string(moe_status_t status);
+
+/* MOE_ABI_VERSION of the built library. */
+int32_t moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_MOE_H */
