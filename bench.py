@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE decode-layer forward on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode_n1]
+    python bench.py --impl reference ...      # the fp64 CPU oracle, timed on host cores
+
+A step is one ``moe_forward`` call (router, top-k, expert grouping, gate+up,
+down+blend) over one batch of synthetic input of the workload (default: the
+single-token decode, hidden 2048, 256 experts, top-8).  The L2 is flushed
+(a write of 2.5x its size) between steps, outside the timed events, because
+the weights one call touches fit in L2.  Prints one JSON line.
+
+Multi-GPU: the layer has no exchange step in this build, so N GPUs run N
+independent replicas ("scaling": "weak"); value = tokens of all ranks / the
+slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer µs/call, tokens/s and HBM GB/s (frac of ~8 TB/s) at N=1–256"
+STAGES = ["router", "topk", "group", "gate_up", "down_blend"]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="decode_n1")
+    p.add_argument("--path", default="auto", choices=["auto", "token_major", "grouped"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--oracle-budget", type=float, default=15.0,
+                   help="seconds of oracle work for the CPU baseline sample")
+    p.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--oracle-tokens", type=int, default=0, help=argparse.SUPPRESS)
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ helpers
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _src_hash(files) -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "mixture_experts_decode_router_gb300", "csrc")
+    for f in files:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel: str, workload: str):
+    """dram bytes per launch of `kernel` from the committed ncu summary, or None
+    when the kernel's source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    ent = d.get(workload, {}).get(kernel)
+    if not ent:
+        return None
+    try:
+        if _src_hash(ent["sources"]) != ent["sha"]:
+            return None
+    except OSError:
+        return None
+    return float(ent["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed loop runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sms:
+            return None
+        sms.sort()
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------------ oracle (CPU) leg
+
+def _oracle_child(args):
+    """Runs in a fresh process with one BLAS thread: the oracle as it stands on a
+    bounded sample of the workload's tokens.  Prints one JSON object."""
+    import numpy as np
+    import torch
+
+    from mixture_experts_decode_router_gb300 import synth
+    from oracle import moe_oracle as O
+
+    torch.set_num_threads(1)
+    cfg = synth.WORKLOADS[args.workload]
+    n_pool = max(cfg.n_tokens, 8)
+    x = synth.make_input(cfg, n_pool, "cpu", dup_frac=0.0, stream=7)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    router = synth.make_router(cfg).view(torch.int16).numpy().view(np.uint16)
+    bias = synth.make_bias(cfg)
+    bias = bias.numpy() if bias is not None else None
+    sgw = synth.make_shared_gate_w(cfg)
+    sgw = sgw.view(torch.int16).numpy().view(np.uint16) if sgw is not None else None
+
+    # Route the pool first (cheap), then generate only the experts it touches
+    # (generation is input preparation, outside the timed region).
+    lg = O.router_logits(O.bf16_decode(xb), router)
+    idx, _ = O.route(lg, cfg.routing, cfg.top_k, cfg.norm_topk_prob, cfg.routed_scaling_factor,
+                     bias)
+    need = sorted(set(int(e) for e in np.unique(idx)))
+
+    class Lazy(dict):
+        def __init__(self, tensor, field):
+            super().__init__()
+            self.tensor, self.field = tensor, field
+
+        def __missing__(self, e):
+            q, s, s2 = synth.expert_matrix(cfg, self.tensor, int(e))
+            v = {"w": q, "scale": s, "scale2": s2}[self.field]
+            if self.field == "w" and v.dtype == torch.bfloat16:
+                v = v.view(torch.int16).numpy().view(np.uint16)
+            elif self.field == "scale2":
+                v = np.float32(v)
+            else:
+                v = v.numpy()
+            self[e] = v
+            return v
+
+    def qm(tensor):
+        return O.QMat(cfg.expert_fmt, Lazy(tensor, "w"), Lazy(tensor, "scale"),
+                      Lazy(tensor, "scale2"))
+
+    layer = O.OracleLayer(hidden=cfg.hidden, num_experts=cfg.num_experts, top_k=cfg.top_k,
+                          inter=cfg.inter, shared_inter=cfg.shared_inter, routing=cfg.routing,
+                          norm_topk_prob=cfg.norm_topk_prob,
+                          routed_scaling_factor=cfg.routed_scaling_factor, router_w=router,
+                          gate=qm("gate"), up=qm("up"), down=qm("down"), sh_gate=qm("sh_gate"),
+                          sh_up=qm("sh_up"), sh_down=qm("sh_down"), correction_bias=bias,
+                          shared_gate_w=sgw)
+    for q in (layer.gate, layer.up, layer.down):
+        for e in need:
+            q.w[e], q.scale[e] if cfg.expert_fmt != "bf16" else None
+            if cfg.expert_fmt == "nvfp4":
+                q.scale2[e]
+    for q in (layer.sh_gate, layer.sh_up, layer.sh_down):
+        q.w[0], q.scale[0] if cfg.expert_fmt != "bf16" else None
+        if cfg.expert_fmt == "nvfp4":
+            q.scale2[0]
+
+    budget = args.oracle_budget
+    limit = args.oracle_tokens if args.oracle_tokens > 0 else 10**9
+    done = 0
+    t0 = time.perf_counter()
+    while done < limit:
+        O.moe_forward(layer, xb, rows=[done % n_pool])
+        done += 1
+        if time.perf_counter() - t0 >= budget:
+            break
+    el = time.perf_counter() - t0
+    print(json.dumps({"tokens": done, "seconds": el, "tokens_per_s": done / el}))
+
+
+def cpu_baseline(args, budget: float, tokens: int = 0):
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", args.workload,
+           "--oracle-budget", str(budget), "--oracle-tokens", str(tokens)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=budget * 4 + 600)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle child failed:\n{r.stderr[-2000:]}")
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{d['tokens']} token(s) of {args.workload}, one at a time, fp64 numpy "
+                      f"with 1 BLAS thread, {d['seconds']:.1f} s (expert generation excluded)"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from mixture_experts_decode_router_gb300 import binding as B
+    from mixture_experts_decode_router_gb300 import synth
+    from mixture_experts_decode_router_gb300.layer import MoeLayer
+
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.load()
+
+    cfg = synth.WORKLOADS[args.workload]
+    n = cfg.n_tokens
+    lw = synth.make_weights(cfg, dev)
+    x = synth.make_input(cfg, device=dev)
+    layer = MoeLayer(lw, n, args.path)
+    out = torch.empty(n, cfg.hidden, dtype=torch.bfloat16, device=dev)
+    idx = torch.empty(n, cfg.top_k, dtype=torch.int32, device=dev)
+    wts = torch.empty(n, cfg.top_k, dtype=torch.float32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(int(2.5 * l2) // 4 * 4, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    def step():
+        s = B.moe_forward(layer.c_cfg, layer.c_w, x, n, out, idx, wts, layer.ws, layer.ws_bytes,
+                          sptr)
+        if s != B.MOE_OK:
+            raise B.MoeError(B.moe_status_string(s))
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)       # let the sampler start before the timed loop
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        ev_s[i].record(stream)
+        step()
+        ev_e[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    per = np.array([a.elapsed_time(b) for a, b in zip(ev_s, ev_e)])   # ms
+    dev_ms = float(per.sum())
+    if world > 1:
+        tt = torch.tensor([dev_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        dev_ms = float(tt.item())
+
+    # Touched bytes from this input's routing (constant over the steps).
+    idx_h = idx.cpu().numpy()
+    touched = synth.touched_bytes(cfg, idx_h)
+    distinct = len(np.unique(idx_h))
+
+    # Per-stage durations (moe_forward_timed: events between the kernels).
+    Kp = min(K, 500)
+    nst = len(STAGES) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(Kp)]
+    for row in evs:          # torch creates the CUDA event on its first record
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(Kp):
+        flush.zero_()
+        s, nm = B.moe_forward_timed(layer.c_cfg, layer.c_w, x, n, out, idx, wts, layer.ws,
+                                    layer.ws_bytes, sptr, [e.cuda_event for e in evs[i]])
+        if s != B.MOE_OK or nm != nst:
+            raise B.MoeError(f"timed forward: status {s}, markers {nm}")
+    torch.cuda.synchronize()
+    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(nst - 1)]
+                         for i in range(Kp)]).mean(axis=0)
+
+    # Algorithmic bytes per launch of each stage.
+    H, I, S, E, k = cfg.hidden, cfg.inter, cfg.shared_inter, cfg.num_experts, cfg.top_k
+    mb = synth.matrix_bytes
+    fmt = cfg.expert_fmt
+    alg = {
+        "router": E * H * 2 + n * H * 2 + n * E * 4,
+        "topk": n * E * 4 + n * k * 8 + (4 * E if lw.correction_bias is not None else 0),
+        "group": n * k * 4 + 4 * (3 * E + 1) + n * k * 4,
+        "gate_up": distinct * 2 * mb(fmt, I, H) + (2 * mb(fmt, S, H) if S else 0) + n * H * 2
+        + 4 * (n * k * I + n * S),
+        "down_blend": distinct * mb(fmt, H, I) + (mb(fmt, H, S) if S else 0)
+        + 4 * (n * k * I + n * S) + n * H * 2 + n * k * 8,
+    }
+    peak, peak_kind = _peaks()
+    dom = STAGES[int(np.argmax(stage_ms))]
+    dom_ms = float(stage_ms[STAGES.index(dom)])
+    achieved = alg[dom] / (dom_ms * 1e-3) / 1e9
+    stages = {s: {"us": round(float(stage_ms[j]) * 1e3, 3), "alg_bytes": int(alg[s]),
+                  "gbs": round(alg[s] / (stage_ms[j] * 1e-3) / 1e9, 1)}
+              for j, s in enumerate(STAGES)}
+
+    # End to end through the public API: pinned host input, H2D, call, D2H.
+    x_h = x.cpu().pin_memory()
+    out_h = torch.empty(n, cfg.hidden, dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+    Ke = min(K, 1000)
+    e2s = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    e2e_ = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    for i in range(Ke):
+        flush.zero_()
+        e2s[i].record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        s = B.moe_forward(layer.c_cfg, layer.c_w, x_d, n, out, idx, wts, layer.ws, layer.ws_bytes,
+                          sptr)
+        if s != B.MOE_OK:
+            raise B.MoeError(B.moe_status_string(s))
+        out_h.copy_(out, non_blocking=True)
+        e2e_[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(np.sum([a.elapsed_time(b) for a, b in zip(e2s, e2e_)]))
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args, args.oracle_budget)
+
+    if rank == 0:
+        ms_step = dev_ms / K
+        tok_s = world * n * K / (dev_ms * 1e-3)
+        line = {
+            "metric": METRIC,
+            "value": round(tok_s, 2),
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 6),
+            "us_per_call": round(ms_step * 1e3, 3),
+            "us_per_call_p10_p50_p90": [round(float(np.percentile(per, q)) * 1e3, 3)
+                                        for q in (10, 50, 90)],
+            "hbm_gbs": round(touched / (ms_step * 1e-3) / 1e9, 1),
+            "hbm_frac_of_measured": round(touched / (ms_step * 1e-3) / 1e9 / peak, 4),
+            "touched_bytes": touched,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16" if fmt == "bf16" else ("fp8e4m3-w/bf16-a" if fmt == "fp8_b128"
+                                                   else "nvfp4-w/bf16-a"),
+            "data": "synthetic (seeded; weights N(0,0.02), input N(0,1))",
+            "config": {"workload": cfg.name, "n_tokens": n, "hidden": H, "num_experts": E,
+                       "top_k": k, "inter": I, "shared_inter": S, "routing": cfg.routing,
+                       "expert_fmt": fmt, "path": args.path,
+                       "l2": "flushed between steps (2.5x L2 write), flush outside the events",
+                       "parallelism": f"replicas{world}" if world > 1 else "single"},
+            "wall_s_timed_loop": round(t1 - t0, 3),
+            "gpu_launches": K * len(STAGES),
+            "stages": stages,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": _traffic(dom, cfg.name),
+                         "alg_bytes_per_launch": int(alg[dom]),
+                         "avg_launch_us": round(dom_ms * 1e3, 3)},
+            "e2e": {"value": round(world * n * Ke / (e2e_ms * 1e-3), 2), "unit": "tokens/s",
+                    "h2d_bytes_per_step": n * H * 2, "d2h_bytes_per_step": n * H * 2,
+                    "us_per_call": round(e2e_ms / Ke * 1e3, 3)},
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    from mixture_experts_decode_router_gb300 import synth
+    cfg = synth.WORKLOADS[args.workload]
+    # One step = one token through the oracle; the run is bounded to ~2 minutes.
+    budget = 120.0
+    cpu = cpu_baseline(args, budget, tokens=max(1, args.steps))
+    tok_s = cpu["value"]
+    line = {
+        "metric": METRIC, "impl": "reference", "value": round(tok_s, 4), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * cfg.n_tokens / tok_s, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "n_tokens": cfg.n_tokens},
+        "cpu_baseline": {"kind": "oracle", "cores": cpu["cores"], "sample": cpu["sample"],
+                         "value": round(tok_s, 4), "unit": "tokens/s"},
+        "e2e": {"value": round(tok_s, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.oracle_child:
+        _oracle_child(args)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -150,8 +150,8 @@ moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* wts,
 /* Routed experts, shared expert and blend for n tokens given their routing
  * (the pages' exp_gate_up, exp_silu_down and wsum_blend steps).
  *   x     device BF16 [n, H]
- *   idx   device int32 [n, k]; every entry must lie in [0, E) (not checked on
- *         the device; an out-of-range index reads outside the weights)
+ *   idx   device int32 [n, k]; an entry outside [0, E) is dropped (that slot
+ *         contributes nothing), so a bad index never reads outside the weights
  *   w     device fp32  [n, k]
  *   out   device BF16 [n, H] (out); must not overlap x
  * Errors: as moe_route, plus MOE_ERR_ALIAS. */
@@ -167,6 +167,22 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* wts,
                          const void* x, int32_t n, void* out,
                          int32_t* idx, float* w,
                          void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* moe_forward with stage markers, for profiling (the per-stage timing the
+ * pages' `prof!` macro in MoeLayer::forward takes with a stream sync, done here
+ * with device events and no sync).
+ *   events    array of n_events cudaEvent_t handles (cast to void*) created by
+ *             the caller on the current device; marker i is recorded with
+ *             cudaEventRecord(events[i], stream) for i < n_events
+ *   n_marks   (out, optional) markers the call reached
+ * Markers: 0 before the first kernel, then one after each kernel, in launch
+ * order: router, top-k, expert grouping, gate+up, down+blend.
+ * Errors: as moe_forward, plus MOE_ERR_NULL for events == NULL with n_events > 0. */
+moe_status_t moe_forward_timed(const moe_config_t* cfg, const moe_weights_t* wts,
+                               const void* x, int32_t n, void* out,
+                               int32_t* idx, float* w,
+                               void* ws, size_t ws_bytes, moe_stream_t stream,
+                               void* const* events, int32_t n_events, int32_t* n_marks);
 
 /* Static description of a status code (never NULL). */
 const char* moe_status_string(moe_status_t status);

@@ -1,0 +1,390 @@
+// moe_capi.cu -- the C ABI of libmoe_gb300 (declared in include/moe.h):
+// host-side validation, workspace carving and the launch sequence.
+//
+// Validation refuses by name before anything is enqueued, in the manner of the
+// pages' named refusals ("spark_model/layers/moe/forward_token_major.rs":
+// forward_token_major_decode refuses zero-expert routing rather than compute
+// it wrongly; "metrale_model_layers/layers/moe/forward.rs": reject_decode_lora,
+// refuse_lean_layout).
+#include <mutex>
+
+#include "moe_launch.cuh"
+
+namespace moe {
+
+static int device_sm_count() {
+    static std::mutex mu;
+    static int cache[128] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+    std::lock_guard<std::mutex> g(mu);
+    if (cache[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 148;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
+// Optional stage markers: records events[i] on the stream at stage boundaries
+// (the pages' per-stage `prof!` timing, done with device events, no sync).
+struct Marks {
+    cudaEvent_t* ev = nullptr;
+    int n = 0, next = 0;
+    void mark(cudaStream_t st) {
+        if (next < n) cudaEventRecord(ev[next], st);
+        ++next;
+    }
+};
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static moe_status_t check_config(const moe_config_t* c) {
+    if (!c) return MOE_ERR_NULL;
+    if (c->num_experts < 1 || c->num_experts > kMaxExperts) return MOE_ERR_INVALID_CONFIG;
+    if (c->top_k < 1 || c->top_k > c->num_experts || c->top_k > kMaxTopK) return MOE_ERR_INVALID_CONFIG;
+    if (c->hidden <= 0 || c->hidden % 32) return MOE_ERR_INVALID_CONFIG;
+    if (c->inter <= 0 || c->inter % 32) return MOE_ERR_INVALID_CONFIG;
+    if (c->shared_inter < 0 || c->shared_inter % 32) return MOE_ERR_INVALID_CONFIG;
+    if (c->routing != MOE_ROUTE_SOFTMAX && c->routing != MOE_ROUTE_SIGMOID_BIAS)
+        return MOE_ERR_INVALID_CONFIG;
+    if (c->norm_topk_prob != 0 && c->norm_topk_prob != 1) return MOE_ERR_INVALID_CONFIG;
+    if (!(c->routed_scaling_factor == c->routed_scaling_factor) ||
+        c->routed_scaling_factor > 3.0e38f || c->routed_scaling_factor < -3.0e38f)
+        return MOE_ERR_INVALID_CONFIG;
+    if (c->expert_fmt != MOE_W_BF16 && c->expert_fmt != MOE_W_FP8_B128 && c->expert_fmt != MOE_W_NVFP4)
+        return MOE_ERR_INVALID_CONFIG;
+    if (c->path != MOE_PATH_AUTO && c->path != MOE_PATH_TOKEN_MAJOR && c->path != MOE_PATH_GROUPED)
+        return MOE_ERR_INVALID_CONFIG;
+    // Sizes that keep every index below 2^31.
+    const int64_t big = (int64_t)c->num_experts * c->inter * c->hidden;
+    if (big > (int64_t)1 << 40) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+static moe_status_t check_qmat(int fmt, const moe_qmat_t& q) {
+    if (!q.w) return MOE_ERR_NULL;
+    if (!aligned16(q.w)) return MOE_ERR_ALIGNMENT;
+    if (fmt == MOE_W_FP8_B128 || fmt == MOE_W_NVFP4) {
+        if (!q.scale) return MOE_ERR_NULL;
+        if (!aligned16(q.scale)) return MOE_ERR_ALIGNMENT;
+    }
+    if (fmt == MOE_W_NVFP4) {
+        if (!q.scale2) return MOE_ERR_NULL;
+        if (!aligned16(q.scale2)) return MOE_ERR_ALIGNMENT;
+    }
+    return MOE_OK;
+}
+
+static moe_status_t check_router_weights(const moe_config_t* c, const moe_weights_t* w) {
+    if (!w || !w->router_w) return MOE_ERR_NULL;
+    if (!aligned16(w->router_w)) return MOE_ERR_ALIGNMENT;
+    if (c->routing == MOE_ROUTE_SIGMOID_BIAS) {
+        if (!w->correction_bias) return MOE_ERR_NULL;
+        if (!aligned16(w->correction_bias)) return MOE_ERR_ALIGNMENT;
+    } else if (w->correction_bias) {
+        return MOE_ERR_INVALID_CONFIG;   // a bias has no meaning under softmax routing
+    }
+    return MOE_OK;
+}
+
+static moe_status_t check_expert_weights(const moe_config_t* c, const moe_weights_t* w) {
+    if (!w) return MOE_ERR_NULL;
+    moe_status_t s;
+    if ((s = check_qmat(c->expert_fmt, w->gate)) != MOE_OK) return s;
+    if ((s = check_qmat(c->expert_fmt, w->up)) != MOE_OK) return s;
+    if ((s = check_qmat(c->expert_fmt, w->down)) != MOE_OK) return s;
+    if (c->shared_inter > 0) {
+        if ((s = check_qmat(c->expert_fmt, w->sh_gate)) != MOE_OK) return s;
+        if ((s = check_qmat(c->expert_fmt, w->sh_up)) != MOE_OK) return s;
+        if ((s = check_qmat(c->expert_fmt, w->sh_down)) != MOE_OK) return s;
+    }
+    if (w->shared_gate_w && !aligned16(w->shared_gate_w)) return MOE_ERR_ALIGNMENT;
+    return MOE_OK;
+}
+
+static moe_status_t check_ws(const moe_config_t* c, int32_t n, const void* ws, size_t ws_bytes,
+                             WsLayout* L) {
+    *L = ws_layout(*c, n);
+    if (!ws) return MOE_ERR_WORKSPACE;
+    if (!aligned16(ws)) return MOE_ERR_ALIGNMENT;
+    if (ws_bytes < L->total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+template <typename T> static T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+static QMatDev qdev(const moe_qmat_t& q, int out_dim, int in_dim) {
+    QMatDev d;
+    d.w = static_cast<const uint8_t*>(q.w);
+    d.scale = q.scale;
+    d.scale2 = q.scale2;
+    d.out_dim = out_dim;
+    d.in_dim = in_dim;
+    return d;
+}
+
+// Enqueue router + top-k.  Arguments already validated.
+static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w, const void* x,
+                                  int32_t n, int32_t* idx, float* wt, float* logits, void* ws,
+                                  const WsLayout& L, cudaStream_t st, Marks& mk) {
+    const int sms = device_sm_count();
+    float* lg = logits ? logits : at<float>(ws, L.logits);
+    cudaError_t e = launch_router(static_cast<const uint16_t*>(x), n, c->hidden,
+                                  static_cast<const uint16_t*>(w->router_w), c->num_experts,
+                                  static_cast<const uint16_t*>(w->shared_gate_w), lg,
+                                  at<float>(ws, L.sg_logit), sms, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    mk.mark(st);
+    e = launch_topk(lg, n, c->num_experts, c->top_k, c->routing, w->correction_bias,
+                    c->norm_topk_prob, c->routed_scaling_factor, idx, wt, st);
+    mk.mark(st);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Token counts up to this use the token-major CUDA-core kernels under AUTO.
+constexpr int kTokenMajorMaxN = 1 << 30;   // grouped path: forced only, until verified on the GPU
+
+// The grouped tensor-core expert stage (after the grouping kernel).
+static moe_status_t enqueue_grouped(const moe_config_t* c, const moe_weights_t* w, const void* x,
+                                    int32_t n, const float* wt, void* out, void* ws, const WsLayout& L,
+                                    float* sg_logit, cudaStream_t st, Marks& mk) {
+    const int sms = device_sm_count();
+    const int fmt = c->expert_fmt;
+    const int H = c->hidden, I = c->inter, S = c->shared_inter, k = c->top_k, E = c->num_experts;
+    const bool nv = fmt == MOE_W_NVFP4;
+    uint16_t* xs = at<uint16_t>(ws, L.xs);
+    uint16_t* xh = at<uint16_t>(ws, L.xh);
+    cudaError_t e = launch_gather(fmt, static_cast<const uint16_t*>(x), n, H, k, at<int32_t>(ws, L.perm),
+                                  at<int32_t>(ws, L.offsets), E, xs, xh, sms, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    mk.mark(st);
+
+    TcParams p{};
+    p.n = n;
+    p.k = k;
+    p.segs = at<int32_t>(ws, L.segs);
+    p.ctrl = at<Ctrl>(ws, L.ctrl);
+    p.err = &at<Ctrl>(ws, L.ctrl)->err;
+    p.perm = at<int32_t>(ws, L.perm);
+    p.route_w = wt;
+    p.sg_logit = w->shared_gate_w ? sg_logit : nullptr;
+    p.act_out = at<uint16_t>(ws, L.as);
+    p.act_sh_out = at<uint16_t>(ws, L.ash);
+    p.y = at<float>(ws, L.y);
+    p.y_sh = at<float>(ws, L.ysh);
+
+    // gate + up
+    TcMaps maps;
+    if (!build_tc_maps(fmt, true, w, E, H, I, S, n, n * k, xs, nv ? (const void*)xh : x, &maps))
+        return MOE_ERR_CUDA;
+    p.out_dim = I; p.in_dim = H; p.sh_out = S; p.sh_in = H;
+    p.scale[0] = w->gate.scale; p.scale[1] = w->up.scale;
+    p.sh_scale[0] = w->sh_gate.scale; p.sh_scale[1] = w->sh_up.scale;
+    p.scale2[0] = w->gate.scale2; p.scale2[1] = w->up.scale2;
+    p.sh_scale2[0] = w->sh_gate.scale2; p.sh_scale2[1] = w->sh_up.scale2;
+    if ((e = launch_grouped_tc(fmt, true, maps, p, sms, st)) != cudaSuccess) return MOE_ERR_CUDA;
+    mk.mark(st);
+
+    // down (+ routing weight / shared gate)
+    if (!build_tc_maps(fmt, false, w, E, H, I, S, n, n * k, p.act_out, p.act_sh_out, &maps))
+        return MOE_ERR_CUDA;
+    p.out_dim = H; p.in_dim = I; p.sh_out = S > 0 ? H : 0; p.sh_in = S;
+    p.scale[0] = p.scale[1] = w->down.scale;
+    p.sh_scale[0] = p.sh_scale[1] = w->sh_down.scale;
+    p.scale2[0] = p.scale2[1] = w->down.scale2;
+    p.sh_scale2[0] = p.sh_scale2[1] = w->sh_down.scale2;
+    if ((e = launch_grouped_tc(fmt, false, maps, p, sms, st)) != cudaSuccess) return MOE_ERR_CUDA;
+    mk.mark(st);
+
+    e = launch_combine(p.y, p.y_sh, at<int32_t>(ws, L.inv), n, H, k, S > 0 ? 1 : 0,
+                       static_cast<uint16_t*>(out), sms, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    mk.mark(st);
+    return MOE_OK;
+}
+
+// Enqueue grouping + experts + blend.  `sg_from_ws`: the shared-gate logit was
+// written to the workspace by enqueue_route of the same call.
+static moe_status_t enqueue_experts(const moe_config_t* c, const moe_weights_t* w, const void* x,
+                                    int32_t n, const int32_t* idx, const float* wt, void* out,
+                                    void* ws, const WsLayout& L, bool sg_from_ws, cudaStream_t st,
+                                    Marks& mk) {
+    const int sms = device_sm_count();
+    const int H = c->hidden, I = c->inter, S = c->shared_inter, k = c->top_k, E = c->num_experts;
+    float* sg_logit = at<float>(ws, L.sg_logit);
+    cudaError_t e;
+    if (w->shared_gate_w && !sg_from_ws) {
+        // moe_experts called on its own: the shared gate logit x . gw is the
+        // router kernel's extra row, run with no expert rows.
+        e = launch_router(static_cast<const uint16_t*>(x), n, H,
+                          static_cast<const uint16_t*>(w->router_w), 0,
+                          static_cast<const uint16_t*>(w->shared_gate_w), nullptr, sg_logit, sms, st);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    e = launch_group(idx, n * k, E, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+                     at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv), at<int32_t>(ws, L.active),
+                     at<int32_t>(ws, L.segs), at<Ctrl>(ws, L.ctrl), st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    mk.mark(st);
+
+    const int path = (c->path == MOE_PATH_AUTO) ? (n <= kTokenMajorMaxN ? MOE_PATH_TOKEN_MAJOR
+                                                                        : MOE_PATH_GROUPED)
+                                                : c->path;
+    if (path == MOE_PATH_GROUPED)
+        return enqueue_grouped(c, w, x, n, wt, out, ws, L, sg_logit, st, mk);
+
+    GateUpParams gu{};
+    gu.x = static_cast<const uint16_t*>(x);
+    gu.n = n; gu.H = H; gu.I = I; gu.S = S; gu.k = k;
+    gu.gate = qdev(w->gate, I, H);
+    gu.up = qdev(w->up, I, H);
+    if (S > 0) {
+        gu.sh_gate = qdev(w->sh_gate, S, H);
+        gu.sh_up = qdev(w->sh_up, S, H);
+    }
+    gu.counts = at<int32_t>(ws, L.counts);
+    gu.offsets = at<int32_t>(ws, L.offsets);
+    gu.perm = at<int32_t>(ws, L.perm);
+    gu.active = at<int32_t>(ws, L.active);
+    gu.ctrl = at<Ctrl>(ws, L.ctrl);
+    gu.act = at<float>(ws, L.act);
+    gu.act_sh = at<float>(ws, L.act_sh);
+
+    DownParams dn{};
+    dn.n = n; dn.H = H; dn.I = I; dn.S = S; dn.k = k; dn.E = E;
+    dn.down = qdev(w->down, H, I);
+    if (S > 0) dn.sh_down = qdev(w->sh_down, H, S);
+    dn.idx = idx;
+    dn.w = wt;
+    dn.act = gu.act;
+    dn.act_sh = gu.act_sh;
+    dn.sg_logit = w->shared_gate_w ? sg_logit : nullptr;
+    dn.out = static_cast<uint16_t*>(out);
+
+    e = launch_gate_up_tm(c->expert_fmt, gu, sms, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    mk.mark(st);
+    e = launch_down_blend_tm(c->expert_fmt, dn, sms, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    mk.mark(st);
+    return MOE_OK;
+}
+
+static bool overlaps(const void* a, const void* b, size_t bytes) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + bytes && pb < pa + bytes;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t max_tokens) {
+    if (check_config(cfg) != MOE_OK || max_tokens < 0) return 0;
+    return ws_layout(*cfg, max_tokens).total;
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* wts, const void* x, int32_t n,
+                       int32_t* idx, float* w, float* logits, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+    moe_status_t s = check_config(cfg);
+    if (s != MOE_OK) return s;
+    if (n < 0) return MOE_ERR_INVALID_CONFIG;
+    if ((s = check_router_weights(cfg, wts)) != MOE_OK) return s;
+    if (n == 0) return MOE_OK;
+    if (!x || !idx || !w) return MOE_ERR_NULL;
+    if (!aligned16(x) || !aligned16(idx) || !aligned16(w) || (logits && !aligned16(logits)))
+        return MOE_ERR_ALIGNMENT;
+    if (wts->shared_gate_w && !aligned16(wts->shared_gate_w)) return MOE_ERR_ALIGNMENT;
+    WsLayout L;
+    if ((s = check_ws(cfg, n, ws, ws_bytes, &L)) != MOE_OK) return s;
+    Marks mk;
+    return enqueue_route(cfg, wts, x, n, idx, w, logits, ws, L, reinterpret_cast<cudaStream_t>(stream),
+                         mk);
+}
+
+moe_status_t moe_experts(const moe_config_t* cfg, const moe_weights_t* wts, const void* x, int32_t n,
+                         const int32_t* idx, const float* w, void* out, void* ws, size_t ws_bytes,
+                         moe_stream_t stream) {
+    moe_status_t s = check_config(cfg);
+    if (s != MOE_OK) return s;
+    if (n < 0) return MOE_ERR_INVALID_CONFIG;
+    if ((s = check_expert_weights(cfg, wts)) != MOE_OK) return s;
+    if (wts->shared_gate_w && !wts->router_w) return MOE_ERR_NULL;
+    if (n == 0) return MOE_OK;
+    if (!x || !idx || !w || !out) return MOE_ERR_NULL;
+    if (!aligned16(x) || !aligned16(idx) || !aligned16(w) || !aligned16(out)) return MOE_ERR_ALIGNMENT;
+    if (overlaps(x, out, (size_t)n * cfg->hidden * 2)) return MOE_ERR_ALIAS;
+    WsLayout L;
+    if ((s = check_ws(cfg, n, ws, ws_bytes, &L)) != MOE_OK) return s;
+    Marks mk;
+    return enqueue_experts(cfg, wts, x, n, idx, w, out, ws, L, false,
+                           reinterpret_cast<cudaStream_t>(stream), mk);
+}
+
+static moe_status_t forward_impl(const moe_config_t* cfg, const moe_weights_t* wts, const void* x,
+                                 int32_t n, void* out, int32_t* idx, float* w, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream, Marks& mk) {
+    moe_status_t s = check_config(cfg);
+    if (s != MOE_OK) return s;
+    if (n < 0) return MOE_ERR_INVALID_CONFIG;
+    if ((s = check_router_weights(cfg, wts)) != MOE_OK) return s;
+    if ((s = check_expert_weights(cfg, wts)) != MOE_OK) return s;
+    if (n == 0) return MOE_OK;
+    if (!x || !out) return MOE_ERR_NULL;
+    if (!aligned16(x) || !aligned16(out) || (idx && !aligned16(idx)) || (w && !aligned16(w)))
+        return MOE_ERR_ALIGNMENT;
+    if (overlaps(x, out, (size_t)n * cfg->hidden * 2)) return MOE_ERR_ALIAS;
+    WsLayout L;
+    if ((s = check_ws(cfg, n, ws, ws_bytes, &L)) != MOE_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int32_t* idx_p = idx ? idx : at<int32_t>(ws, L.idx);
+    float* w_p = w ? w : at<float>(ws, L.w);
+    mk.mark(st);
+    if ((s = enqueue_route(cfg, wts, x, n, idx_p, w_p, nullptr, ws, L, st, mk)) != MOE_OK) return s;
+    return enqueue_experts(cfg, wts, x, n, idx_p, w_p, out, ws, L, true, st, mk);
+}
+
+moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* wts, const void* x, int32_t n,
+                         void* out, int32_t* idx, float* w, void* ws, size_t ws_bytes,
+                         moe_stream_t stream) {
+    Marks mk;
+    return forward_impl(cfg, wts, x, n, out, idx, w, ws, ws_bytes, stream, mk);
+}
+
+moe_status_t moe_forward_timed(const moe_config_t* cfg, const moe_weights_t* wts, const void* x,
+                               int32_t n, void* out, int32_t* idx, float* w, void* ws,
+                               size_t ws_bytes, moe_stream_t stream, void* const* events,
+                               int32_t n_events, int32_t* n_marks) {
+    if (n_events < 0 || (n_events > 0 && !events)) return MOE_ERR_NULL;
+    Marks mk;
+    mk.ev = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events));
+    mk.n = n_events;
+    const moe_status_t s = forward_impl(cfg, wts, x, n, out, idx, w, ws, ws_bytes, stream, mk);
+    if (n_marks) *n_marks = mk.next;
+    return s;
+}
+
+const char* moe_status_string(moe_status_t status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK: success";
+        case MOE_ERR_NULL: return "MOE_ERR_NULL: a required pointer is NULL";
+        case MOE_ERR_INVALID_CONFIG: return "MOE_ERR_INVALID_CONFIG: a size, enum or flag is out of range";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: configuration outside what the kernels cover";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing or too small";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA launch failed";
+        case MOE_ERR_ALIGNMENT: return "MOE_ERR_ALIGNMENT: a device pointer is not 16-byte aligned";
+        case MOE_ERR_ALIAS: return "MOE_ERR_ALIAS: out overlaps x";
+        default: return "unknown moe_status_t";
+    }
+}
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+}  // extern "C"

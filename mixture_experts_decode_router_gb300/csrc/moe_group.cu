@@ -1,0 +1,151 @@
+// moe_group.cu -- group the routes of a call by expert (sm_103a).
+//
+// The pages' grouped decode ("metrale_model_layers/layers/moe/forward.rs",
+// forward_nvfp4_grouped_decode; "metrale_model_layers/layers/moe/
+// forward_fp8_grouped_router.rs", module header) runs the experts sorted by
+// expert, so that every expert's weights are streamed once for all the tokens
+// that chose it.  This kernel builds that order on the device (no host
+// read-back, so the call can be captured in a CUDA graph):
+//   counts[e]   routes of expert e
+//   offsets[e]  exclusive prefix sum of counts (offsets[E] = routes kept)
+//   perm[p]     route ids r = t*k + j, grouped by expert, ascending r within an
+//               expert (a stable order, independent of thread timing); a route
+//               whose index lies outside [0, E) is dropped
+//   inv[r]      sorted position of route r (-1 for a dropped route)
+//   active[u]   experts with counts > 0, ascending; ctrl->n_active of them
+//   segs[s]     (expert, first sorted position, routes) for runs of at most
+//               kTcTokensPerTile routes of one expert, ascending expert;
+//               ctrl->n_rsegs of them (the tiles of the grouped path)
+#include "moe_launch.cuh"
+
+namespace moe {
+
+constexpr int kGroupThreads = 1024;
+constexpr int kSegWarps = 8;   // warps that own contiguous route segments
+
+__global__ void __launch_bounds__(kGroupThreads)
+group_kernel(const int32_t* __restrict__ idx, int nk, int E,
+             int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+             int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ active,
+             int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl) {
+    extern __shared__ int32_t sm[];
+    int32_t* cnt = sm;                           // [kSegWarps][E]
+    int32_t* tot = sm + kSegWarps * E;           // [E]
+    __shared__ int32_t warp_sums[3][32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    for (int i = tid; i < kSegWarps * E; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+
+    const int seg = (nk + kSegWarps - 1) / kSegWarps;
+    if (warp < kSegWarps) {
+        const int b = warp * seg, e_ = min(nk, b + seg);
+        for (int r = b + lane; r < e_; r += 32) {
+            const int e = idx[r];
+            if (e >= 0 && e < E) atomicAdd(&cnt[warp * E + e], 1);   // out-of-range: dropped
+        }
+    }
+    __syncthreads();
+
+    // Per expert: exclusive scan over the segment warps, and the total.
+    for (int e = tid; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < kSegWarps; ++w) {
+            const int c = cnt[w * E + e];
+            cnt[w * E + e] = run;
+            run += c;
+        }
+        tot[e] = run;
+    }
+    __syncthreads();
+
+    // Exclusive scans over experts (E <= 1024 = one element per thread):
+    // offsets (of counts), active positions (of counts > 0) and segment starts
+    // (of ceil(counts / kTcTokensPerTile)).
+    const int c = (tid < E) ? tot[tid] : 0;
+    const int a = (tid < E && c > 0) ? 1 : 0;
+    const int g = (c + kTcTokensPerTile - 1) / kTcTokensPerTile;
+    int sc = c, sa = a, sg = g;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int yc = __shfl_up_sync(0xffffffffu, sc, o);
+        const int ya = __shfl_up_sync(0xffffffffu, sa, o);
+        const int yg = __shfl_up_sync(0xffffffffu, sg, o);
+        if (lane >= o) { sc += yc; sa += ya; sg += yg; }
+    }
+    if (lane == 31) { warp_sums[0][warp] = sc; warp_sums[1][warp] = sa; warp_sums[2][warp] = sg; }
+    __syncthreads();
+    if (warp == 0) {
+        int vc = warp_sums[0][lane], va = warp_sums[1][lane], vg = warp_sums[2][lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int yc = __shfl_up_sync(0xffffffffu, vc, o);
+            const int ya = __shfl_up_sync(0xffffffffu, va, o);
+            const int yg = __shfl_up_sync(0xffffffffu, vg, o);
+            if (lane >= o) { vc += yc; va += ya; vg += yg; }
+        }
+        warp_sums[0][lane] = vc;   // inclusive over warps
+        warp_sums[1][lane] = va;
+        warp_sums[2][lane] = vg;
+    }
+    __syncthreads();
+    const int base_c = (warp > 0 ? warp_sums[0][warp - 1] : 0);
+    const int base_a = (warp > 0 ? warp_sums[1][warp - 1] : 0);
+    const int base_g = (warp > 0 ? warp_sums[2][warp - 1] : 0);
+    const int excl_c = base_c + sc - c;
+    const int excl_a = base_a + sa - a;
+    const int excl_g = base_g + sg - g;
+    if (tid < E) {
+        counts[tid] = c;
+        offsets[tid] = excl_c;
+        tot[tid] = excl_c;                 // reuse: start of expert tid
+        if (a) active[excl_a] = tid;
+        for (int b = 0; b < g; ++b) {
+            int32_t* sgp = segs + 3 * (excl_g + b);
+            sgp[0] = tid;
+            sgp[1] = excl_c + b * kTcTokensPerTile;
+            sgp[2] = min(kTcTokensPerTile, c - b * kTcTokensPerTile);
+        }
+    }
+    if (tid == 0) {
+        offsets[E] = warp_sums[0][31];     // routes kept (n*k minus dropped ones)
+        ctrl->n_active = warp_sums[1][31];
+        ctrl->n_rsegs = warp_sums[2][31];
+    }
+    __syncthreads();
+
+    // Stable scatter: each segment warp walks its routes in order.
+    if (warp < kSegWarps) {
+        const int b = warp * seg, e_ = min(nk, b + seg);
+        for (int r0 = b; r0 < e_; r0 += 32) {
+            const int r = r0 + lane;
+            const bool valid = r < e_;
+            const int e = valid ? idx[r] : -1;
+            const bool in_range = valid && e >= 0 && e < E;
+            if (valid && !in_range) inv[r] = -1;
+            const unsigned vmask = __ballot_sync(0xffffffffu, in_range);
+            if (in_range) {
+                const unsigned peers = __match_any_sync(vmask, e);
+                const int rank = __popc(peers & ((1u << lane) - 1u));
+                const int pos = tot[e] + cnt[warp * E + e] + rank;
+                perm[pos] = r;
+                inv[r] = pos;
+                __syncwarp(vmask);
+                if (rank == 0) cnt[warp * E + e] += __popc(peers);
+            }
+            __syncwarp();
+        }
+    }
+}
+
+cudaError_t launch_group(const int32_t* idx, int nk, int E, int32_t* counts, int32_t* offsets,
+                         int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs, Ctrl* ctrl,
+                         cudaStream_t st) {
+    const size_t smem = sizeof(int32_t) * (size_t)(kSegWarps + 1) * E;
+    // (kSegWarps + 1) * E ints <= 36 KB for E <= 1024: under the 48 KB default.
+    group_kernel<<<1, kGroupThreads, smem, st>>>(idx, nk, E, counts, offsets, perm, inv, active, segs,
+                                                  ctrl);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,644 @@
+// moe_grouped_tc.cu -- expert-grouped tensor-core path for batched decode (sm_103a).
+//
+// The grouped decode of the pages ("metrale_model_layers/layers/moe/forward.rs":
+// forward_nvfp4_grouped_decode, "rows do not depend on how many share the
+// call"; "metrale_model_layers/layers/moe/forward_fp8_grouped_router.rs":
+// grouped FP8 expert kernels fed by grouped_route): routes are grouped by
+// expert, and each expert's matrices are streamed once for all of its tokens
+// as a dense GEMM on the 5th-generation tensor cores.
+//
+//   gather     xs[p, :] = x[token(perm[p]), :]   (expert-sorted activations)
+//   gate_up    per (expert, 128 rows of I, <=128 tokens) tile:
+//              G = Wg x^T, U = Wu x^T on tcgen05 (TMEM accumulators),
+//              a = SiLU(G) * U  -> as[p, i]
+//   down       per (expert, 128 rows of H, <=128 tokens) tile:
+//              D = Wd a^T;  y[p, h] = w(route p) * D      (fp32)
+//   combine    out[t, h] = sum over t's slots, in slot order, of y[., h]
+//              + the gated shared expert; BF16.  No atomics, so every row's
+//              bits are independent of the rest of the batch.
+//
+// The tile's M dimension is 128 weight rows and its N dimension the expert's
+// tokens (padded to a multiple of 16), so a thin token set still fills the
+// MMA.  Weights: BF16 arrive by TMA straight in the 128-byte swizzled K-major
+// layout the MMA reads; FP8 and NVFP4 arrive raw by TMA and eight dequant warps
+// rewrite them as BF16 (FP8: RNE(e4m3 * block scale)) or f16 (NVFP4:
+// e2m1 * e4m3 scale, exact in f16; the fp32 scale2 is applied to the
+// accumulator) in that layout.  NVFP4 tiles therefore run the f16 MMA with f16
+// activations.  Warp roles: 0 TMA producer, 1 MMA issuer (one thread) and TMEM
+// owner, 2-5 epilogue (TMEM -> registers -> global), 6-13 dequant.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "moe_launch.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;   // weight rows per tile (MMA M)
+constexpr int BK = 64;    // K elements per pipeline stage
+constexpr int NT = kTcTokensPerTile;   // tokens per tile (max MMA N)
+
+template <int FMT, bool GU>
+struct TcCfg {
+    static constexpr bool kDeq = FMT != MOE_W_BF16;
+    static constexpr bool kF16 = FMT == MOE_W_NVFP4;
+    static constexpr int kMats = GU ? 2 : 1;
+    static constexpr int kAMat = BM * BK * 2;
+    static constexpr int kAStage = kMats * kAMat;
+    static constexpr int kBStage = NT * BK * 2;
+    static constexpr int kRawRow = FMT == MOE_W_FP8_B128 ? BK : (FMT == MOE_W_NVFP4 ? BK / 2 : 0);
+    static constexpr int kRawMat = BM * kRawRow;
+    static constexpr int kRawStage = kMats * kRawMat;
+    static constexpr int kAStages = kDeq ? (GU ? 3 : 4) : (GU ? 4 : 6);
+    static constexpr int kRawStages = !kDeq ? 0 : ((FMT == MOE_W_FP8_B128 && GU) ? 4 : 8);
+    static constexpr int kAccCols = kMats * NT;
+    static constexpr int kTmemCols = 2 * kAccCols;
+    static constexpr int kDeqWarps = kDeq ? 8 : 0;
+    static constexpr int kThreads = (6 + kDeqWarps) * 32;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kAStages * kAStage;
+    static constexpr int kOffRaw = kOffB + kAStages * kBStage;
+    static constexpr int kOffBar = kOffRaw + kRawStages * kRawStage;
+    // a_full, a_empty, b_full per A stage; raw_full, raw_empty per raw stage;
+    // acc_full[2], acc_empty[2], drain.
+    static constexpr int kNumBars = 3 * kAStages + 2 * kRawStages + 5;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmem = kOffMisc + 16 + 1024;   // + alignment slack
+    static_assert(kSmem <= 232448, "shared memory budget");
+    static_assert(kTmemCols <= 512, "TMEM budget");
+};
+
+struct Tile {
+    int e;        // expert (routed) or -1 (shared)
+    int pos0;     // first row of this tile's tokens in the activation matrix
+    int ntok;     // tokens in the tile (1..NT)
+    int m0;       // first weight row
+    int out;      // weight rows of this matrix
+    int K;        // reduction length
+};
+
+__device__ __forceinline__ Tile decode_tile(int tau, const TcParams& p, int n_ssegs, int n_rsegs) {
+    Tile t;
+    const int mbs = (p.sh_out + BM - 1) / BM;
+    const int mbr = (p.out_dim + BM - 1) / BM;
+    if (tau < n_ssegs * mbs) {
+        const int s = tau / mbs, mb = tau - s * mbs;
+        t.e = -1;
+        t.pos0 = s * NT;
+        t.ntok = min(NT, p.n - t.pos0);
+        t.m0 = mb * BM;
+        t.out = p.sh_out;
+        t.K = p.sh_in;
+    } else {
+        const int t2 = tau - n_ssegs * mbs;
+        const int s = t2 / mbr, mb = t2 - s * mbr;
+        const int32_t* sg = p.segs + 3 * s;
+        t.e = sg[0];
+        t.pos0 = sg[1];
+        t.ntok = sg[2];
+        t.m0 = mb * BM;
+        t.out = p.out_dim;
+        t.K = p.in_dim;
+    }
+    (void)n_rsegs;
+    return t;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t h2;
+    asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h2) : "r"(byte));
+    return h2;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    uint32_t h2;
+    asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(two));
+    return h2;
+}
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t h2) {
+    __half2_raw raw;
+    raw.x = (unsigned short)(h2 & 0xffffu);
+    raw.y = (unsigned short)(h2 >> 16);
+    return __half22float2(__half2(raw));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+template <int FMT, bool GU>
+__global__ void __launch_bounds__(TcCfg<FMT, GU>::kThreads, 1)
+grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+    using C = TcCfg<FMT, GU>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem + C::kOffA;
+    uint8_t* sB = smem + C::kOffB;
+    uint8_t* sRaw = smem + C::kOffRaw;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint64_t* a_full = bars;
+    uint64_t* a_empty = bars + C::kAStages;
+    uint64_t* b_full = bars + 2 * C::kAStages;
+    uint64_t* raw_full = bars + 3 * C::kAStages;
+    uint64_t* raw_empty = raw_full + C::kRawStages;
+    uint64_t* acc_full = raw_empty + C::kRawStages;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kAStages; ++s) {
+            ptx::mbar_init(&a_full[s], C::kDeq ? C::kDeqWarps : 1);
+            ptx::mbar_init(&a_empty[s], 1);
+            ptx::mbar_init(&b_full[s], 1);
+        }
+        for (int s = 0; s < C::kRawStages; ++s) {
+            ptx::mbar_init(&raw_full[s], 1);
+            ptx::mbar_init(&raw_empty[s], C::kDeqWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&acc_full[b], 1);
+            ptx::mbar_init(&acc_empty[b], 4);
+        }
+        ptx::mbar_init(drain, 1);
+        *s_abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) ptx::tmem_alloc(s_tmem, C::kTmemCols);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    const int n_rsegs = p.ctrl->n_rsegs;
+    const int n_ssegs = (p.sh_out > 0) ? (p.n + NT - 1) / NT : 0;
+    const int n_tiles = n_ssegs * ((p.sh_out + BM - 1) / BM) + n_rsegs * ((p.out_dim + BM - 1) / BM);
+    int32_t* err = p.err;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int tau = blockIdx.x; tau < n_tiles && !*s_abort; tau += gridDim.x) {
+                const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
+                const bool sh = t.e < 0;
+                const int wrow = sh ? t.m0 : t.e * t.out + t.m0;
+                const int nbox = (t.ntok + 15) >> 4;
+                const CUtensorMap* bmap = sh ? &maps.bs : &maps.b;
+                const int KB = (t.K + BK - 1) / BK;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int k0 = kb * BK;
+                    if constexpr (C::kDeq) {
+                        const int rs = it % C::kRawStages;
+                        if (!ptx::mbar_wait(&raw_empty[rs], ((it / C::kRawStages) & 1) ^ 1, s_abort, err, 1))
+                            break;
+                        ptx::mbar_arrive_expect_tx(&raw_full[rs], C::kRawStage);
+                        const int xr = (FMT == MOE_W_FP8_B128) ? k0 : k0 / 2;
+                        for (int m = 0; m < C::kMats; ++m)
+                            ptx::tma_load_2d(sRaw + rs * C::kRawStage + m * C::kRawMat,
+                                             sh ? &maps.ws[m] : &maps.w[m], xr, wrow, &raw_full[rs]);
+                    }
+                    const int as = it % C::kAStages;
+                    if (!ptx::mbar_wait(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 1))
+                        break;
+                    if constexpr (!C::kDeq) {
+                        ptx::mbar_arrive_expect_tx(&a_full[as], C::kAStage + nbox * 2048);
+                        for (int m = 0; m < C::kMats; ++m)
+                            ptx::tma_load_2d(sA + as * C::kAStage + m * C::kAMat,
+                                             sh ? &maps.ws[m] : &maps.w[m], k0, wrow, &a_full[as]);
+                        for (int j = 0; j < nbox; ++j)
+                            ptx::tma_load_2d(sB + as * C::kBStage + j * 2048, bmap, k0, t.pos0 + 16 * j,
+                                             &a_full[as]);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(&b_full[as], nbox * 2048);
+                        for (int j = 0; j < nbox; ++j)
+                            ptx::tma_load_2d(sB + as * C::kBStage + j * 2048, bmap, k0, t.pos0 + 16 * j,
+                                             &b_full[as]);
+                    }
+                }
+            }
+            if (*s_abort) {
+                // Let every copy this thread issued land before the CTA exits:
+                // wait (bounded) on the last phase of each ring stage it used.
+                const uint32_t na = it < (uint32_t)C::kAStages ? it : C::kAStages;
+                for (uint32_t q = 0; q < na; ++q) {
+                    const uint32_t i2 = it - 1 - q, s2 = i2 % C::kAStages;
+                    ptx::mbar_wait_quiet(C::kDeq ? &b_full[s2] : &a_full[s2], (i2 / C::kAStages) & 1,
+                                         100000000ull);
+                }
+                if constexpr (C::kDeq) {
+                    const uint32_t nr = it < (uint32_t)C::kRawStages ? it : C::kRawStages;
+                    for (uint32_t q = 0; q < nr; ++q) {
+                        const uint32_t i2 = it - 1 - q, s2 = i2 % C::kRawStages;
+                        ptx::mbar_wait_quiet(&raw_full[s2], (i2 / C::kRawStages) & 1, 100000000ull);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, acc_it = 0;
+            for (int tau = blockIdx.x; tau < n_tiles && !*s_abort; tau += gridDim.x, ++acc_it) {
+                const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
+                const int ab = acc_it & 1;
+                if (!ptx::mbar_wait(&acc_empty[ab], ((acc_it >> 1) & 1) ^ 1, s_abort, err, 2)) break;
+                ptx::tc_fence_after();
+                const int nmma = ((t.ntok + 15) >> 4) << 4;
+                const uint32_t idesc = ptx::idesc_f16(BM, nmma, !C::kF16);
+                const uint32_t d0 = tmem + ab * C::kAccCols;
+                const int KB = (t.K + BK - 1) / BK;
+                bool ok = true;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int as = it % C::kAStages;
+                    const uint32_t ph = (it / C::kAStages) & 1;
+                    if (!ptx::mbar_wait(&a_full[as], ph, s_abort, err, 2)) { ok = false; break; }
+                    if constexpr (C::kDeq)
+                        if (!ptx::mbar_wait(&b_full[as], ph, s_abort, err, 2)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t a_base = ptx::smem_u32(sA + as * C::kAStage);
+                    const uint32_t b_base = ptx::smem_u32(sB + as * C::kBStage);
+#pragma unroll
+                    for (int m = 0; m < C::kMats; ++m)
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            ptx::mma_f16(d0 + m * NT, ptx::sw128_desc(a_base + m * C::kAMat + kk * 32),
+                                         ptx::sw128_desc(b_base + kk * 32), idesc,
+                                         (kb > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(&a_empty[as]);
+                }
+                if (!ok) break;
+                ptx::mma_commit(&acc_full[ab]);
+            }
+            // Every MMA issued has completed before TMEM is released.
+            ptx::mma_commit(drain);
+            ptx::mbar_wait_quiet(drain, 0, 100000000ull);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                     // TMEM lane quarter of this warp
+        const int row = 32 * q + lane;
+        uint32_t acc_it = 0;
+        for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x, ++acc_it) {
+            const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
+            const int ab = acc_it & 1;
+            if (!ptx::mbar_wait_warp(&acc_full[ab], (acc_it >> 1) & 1, s_abort, err, 3)) break;
+            ptx::tc_fence_after();
+            const int m = t.m0 + row;
+            const bool valid = m < t.out;
+            const bool sh = t.e < 0;
+            const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + ab * C::kAccCols;
+            if constexpr (GU) {
+                float s2g = 1.f, s2u = 1.f;
+                if constexpr (FMT == MOE_W_NVFP4) {
+                    s2g = sh ? p.sh_scale2[0][0] : p.scale2[0][t.e];
+                    s2u = sh ? p.sh_scale2[1][0] : p.scale2[1][t.e];
+                }
+                uint16_t* dst = reinterpret_cast<uint16_t*>(sh ? p.act_sh_out : p.act_out);
+                for (int j0 = 0; j0 < t.ntok; j0 += 16) {
+                    float g[16], u[16];
+                    ptx::tmem_ld16(tb + j0, g);
+                    ptx::tmem_ld16(tb + NT + j0, u);
+                    if (valid) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int j = j0 + jj;
+                            if (j < t.ntok) {
+                                const float gv = g[jj] * s2g, uv = u[jj] * s2u;
+                                const float a = gv / (1.0f + expf(-gv)) * uv;
+                                uint16_t bits;
+                                if constexpr (C::kF16) {
+                                    const __half h = __float2half_rn(fminf(fmaxf(a, -65504.f), 65504.f));
+                                    bits = *reinterpret_cast<const uint16_t*>(&h);
+                                } else {
+                                    const __nv_bfloat16 b = __float2bfloat16_rn(a);
+                                    bits = *reinterpret_cast<const uint16_t*>(&b);
+                                }
+                                dst[(size_t)(t.pos0 + j) * t.out + m] = bits;
+                            }
+                        }
+                    }
+                }
+            } else {
+                float s2 = 1.f;
+                if constexpr (FMT == MOE_W_NVFP4) s2 = sh ? p.sh_scale2[0][0] : p.scale2[0][t.e];
+                float* dst = sh ? p.y_sh : p.y;
+                for (int j0 = 0; j0 < t.ntok; j0 += 16) {
+                    float d[16];
+                    ptx::tmem_ld16(tb + j0, d);
+                    if (valid) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int j = j0 + jj;
+                            if (j < t.ntok) {
+                                float wgt;
+                                if (sh) {
+                                    wgt = p.sg_logit ? 1.0f / (1.0f + expf(-p.sg_logit[t.pos0 + j])) : 1.0f;
+                                } else {
+                                    wgt = p.route_w[p.perm[t.pos0 + j]];
+                                }
+                                dst[(size_t)(t.pos0 + j) * t.out + m] = d[jj] * (wgt * s2);
+                            }
+                        }
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);
+        }
+    } else if constexpr (C::kDeq) {
+        // ------------------------------------------------------------ dequant
+        const int dt = threadIdx.x - 6 * 32;        // 0 .. 255
+        const int dwarp = dt >> 5;
+        uint32_t it = 0;
+        for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
+            const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
+            const bool sh = t.e < 0;
+            const int KB = (t.K + BK - 1) / BK;
+            bool ok = true;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int rs = it % C::kRawStages, as = it % C::kAStages;
+                if (!ptx::mbar_wait_warp(&raw_full[rs], (it / C::kRawStages) & 1, s_abort, err, 4)) { ok = false; break; }
+                if (!ptx::mbar_wait_warp(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 4)) { ok = false; break; }
+                const int k0 = kb * BK;
+                for (int m = 0; m < C::kMats; ++m) {
+                    const uint8_t* raw = sRaw + rs * C::kRawStage + m * C::kRawMat;
+                    const uint32_t a_mat = ptx::smem_u32(sA + as * C::kAStage + m * C::kAMat);
+                    if constexpr (FMT == MOE_W_FP8_B128) {
+                        // One fp32 scale per 128x128 block: uniform over this stage.
+                        const int ob = (t.out + 127) >> 7, ib = (t.K + 127) >> 7;
+                        const float* sc = reinterpret_cast<const float*>(sh ? p.sh_scale[m] : p.scale[m]);
+                        const float s = __ldg(sc + (size_t)(sh ? 0 : t.e) * ob * ib + (t.m0 >> 7) * ib + (k0 >> 7));
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const int qd = dt + 256 * c;           // 512 chunks of 16 codes
+                            const int r = qd >> 2, ch = qd & 3;
+                            const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 64 + ch * 16);
+                            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                            uint32_t o[8];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 lo = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] & 0xffffu));
+                                const float2 hi = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] >> 16));
+                                o[2 * i] = pack_bf16(lo.x * s, lo.y * s);
+                                o[2 * i + 1] = pack_bf16(hi.x * s, hi.y * s);
+                            }
+                            const uint32_t rowb = a_mat + r * 128;
+                            st_shared_v4(rowb + (((2 * ch) ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
+                            st_shared_v4(rowb + (((2 * ch + 1) ^ (r & 7)) << 4), o[4], o[5], o[6], o[7]);
+                        }
+                    } else {
+                        // NVFP4: 256 chunks of 32 codes (16 bytes), one per thread.
+                        const int r = dt >> 1, ch = dt & 1;
+                        const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 32 + ch * 16);
+                        const int kc = k0 + 32 * ch;
+                        const int mrow = t.m0 + r;
+                        uint32_t s0 = 0, s1 = 0;   // f16x2 of the two block scales (0 outside the matrix)
+                        if (mrow < t.out && kc < t.K) {
+                            const uint8_t* sc = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]) +
+                                                ((size_t)(sh ? 0 : t.e) * t.out + mrow) * (t.K / 16) + kc / 16;
+                            const uint32_t b0 = __ldg(sc), b1 = __ldg(sc + 1);
+                            s0 = e4m3x2_to_f16x2(b0 | (b0 << 8));
+                            s1 = e4m3x2_to_f16x2(b1 | (b1 << 8));
+                        }
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                        uint32_t o[16];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t sc2 = (i < 2) ? s0 : s1;
+#pragma unroll
+                            for (int b = 0; b < 4; ++b)
+                                o[4 * i + b] = f16x2_mul(e2m1x2_to_f16x2((w4[i] >> (8 * b)) & 0xffu), sc2);
+                        }
+                        const uint32_t rowb = a_mat + r * 128;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            st_shared_v4(rowb + (((4 * ch + i) ^ (r & 7)) << 4), o[4 * i], o[4 * i + 1],
+                                         o[4 * i + 2], o[4 * i + 3]);
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::mbar_arrive(&raw_empty[rs]);
+                    ptx::mbar_arrive(&a_full[as]);
+                }
+            }
+            if (!ok) break;
+        }
+        (void)dwarp;
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// 2-D map over a row-major [rows, cols] matrix of `esize`-byte elements.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t cols,
+              uint64_t rows, uint32_t box_cols, uint32_t box_rows, bool swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * esize};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Weight map: raw codes (FP8 / NVFP4, unswizzled) or BF16 (swizzled, MMA layout).
+bool weight_map(CUtensorMap* m, int fmt, const void* w, int rows_total, int in_dim) {
+    if (fmt == MOE_W_BF16)
+        return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, in_dim, rows_total, BK, BM, true);
+    if (fmt == MOE_W_FP8_B128)
+        return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim, rows_total, BK, BM, false);
+    return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim / 2, rows_total, BK / 2, BM, false);
+}
+
+bool act_map(CUtensorMap* m, int fmt, const void* a, int rows, int cols) {
+    return make_map(m, a, fmt == MOE_W_NVFP4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    2, cols, rows > 0 ? rows : 1, BK, 16, true);
+}
+
+template <int FMT, bool GU>
+cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int num_sms, cudaStream_t st) {
+    using C = TcCfg<FMT, GU>;
+    auto kern = grouped_tc_kernel<FMT, GU>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<num_sms, C::kThreads, C::kSmem, st>>>(maps, p);
+    return cudaGetLastError();
+}
+
+// xs[p, :] = x[perm[p] / k, :] for the grouped routes (bf16, or f16 for NVFP4),
+// and for NVFP4 also xh = f16(x) (the shared expert's operand).
+template <bool F16>
+__global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int n, int H, int k,
+                                                     const int32_t* __restrict__ perm,
+                                                     const int32_t* __restrict__ offsets, int E,
+                                                     uint16_t* __restrict__ xs, uint16_t* __restrict__ xh) {
+    const int n_routes = offsets[E];
+    const int rows = n_routes + (F16 ? n : 0);
+    const int C8 = H >> 3;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)rows * C8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int r = (int)(i / C8), c = (int)(i - (int64_t)r * C8);
+        const bool routed = r < n_routes;
+        const int t = routed ? perm[r] / k : r - n_routes;
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c);
+        if constexpr (F16) {
+            uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xffff0000u);
+                const __half2 h = __floats2half2_rn(fminf(fmaxf(lo, -65504.f), 65504.f),
+                                                    fminf(fmaxf(hi, -65504.f), 65504.f));
+                w4[q] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        uint16_t* dst = routed ? xs + (size_t)r * H : xh + (size_t)(r - n_routes) * H;
+        reinterpret_cast<uint4*>(dst)[c] = v;
+    }
+}
+
+// out[t, h] = bf16( sum_j y[inv[t*k + j], h] (slot order) + y_sh[t, h] ).
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ ysh,
+                                                      const int32_t* __restrict__ inv, int n, int H, int k,
+                                                      int has_shared, uint16_t* __restrict__ out) {
+    const int C4 = H >> 2;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)n * C4;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / C4), c = (int)(i - (int64_t)t * C4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const int pos = __ldg(inv + t * k + j);
+            if (pos < 0) continue;
+            const float4 v = __ldg(reinterpret_cast<const float4*>(y + (size_t)pos * H) + c);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        if (has_shared) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(ysh + (size_t)t * H) + c);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        const uint32_t lo = pack_bf16(acc.x, acc.y), hi = pack_bf16(acc.z, acc.w);
+        reinterpret_cast<uint2*>(out + (size_t)t * H)[c] = make_uint2(lo, hi);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const int32_t* perm,
+                          const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, int num_sms,
+                          cudaStream_t st) {
+    const int grid = 2 * num_sms;
+    if (fmt == MOE_W_NVFP4) gather_kernel<true><<<grid, 256, 0, st>>>(x, n, H, k, perm, offsets, E, xs, xh);
+    else gather_kernel<false><<<grid, 256, 0, st>>>(x, n, H, k, perm, offsets, E, xs, xh);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* y, const float* ysh, const int32_t* inv, int n, int H, int k,
+                           int has_shared, uint16_t* out, int num_sms, cudaStream_t st) {
+    combine_kernel<<<2 * num_sms, 256, 0, st>>>(y, ysh, inv, n, H, k, has_shared, out);
+    return cudaGetLastError();
+}
+
+bool build_tc_maps(int fmt, bool gate_up, const moe_weights_t* w, int E, int H, int I, int S, int n,
+                   int n_routes_max, const void* act_routed, const void* act_shared, TcMaps* maps) {
+    // gate_up: routed weights [E*I, H], shared [S, H], B = xs [rows, H] / x(or xh) [n, H]
+    // down:    routed weights [E*H, I], shared [H, S], B = as [rows, I] / ash [n, S]
+    bool ok = true;
+    if (gate_up) {
+        ok &= weight_map(&maps->w[0], fmt, w->gate.w, E * I, H);
+        ok &= weight_map(&maps->w[1], fmt, w->up.w, E * I, H);
+        if (S > 0) {
+            ok &= weight_map(&maps->ws[0], fmt, w->sh_gate.w, S, H);
+            ok &= weight_map(&maps->ws[1], fmt, w->sh_up.w, S, H);
+            ok &= act_map(&maps->bs, fmt, act_shared, n, H);
+        } else {
+            maps->ws[0] = maps->w[0];
+            maps->ws[1] = maps->w[1];
+            maps->bs = maps->w[0];
+        }
+        ok &= act_map(&maps->b, fmt, act_routed, n_routes_max, H);
+    } else {
+        ok &= weight_map(&maps->w[0], fmt, w->down.w, E * H, I);
+        maps->w[1] = maps->w[0];
+        if (S > 0) {
+            ok &= weight_map(&maps->ws[0], fmt, w->sh_down.w, H, S);
+            ok &= act_map(&maps->bs, fmt, act_shared, n, S);
+        } else {
+            maps->ws[0] = maps->w[0];
+            maps->bs = maps->w[0];
+        }
+        maps->ws[1] = maps->ws[0];
+        ok &= act_map(&maps->b, fmt, act_routed, n_routes_max, I);
+    }
+    return ok;
+}
+
+cudaError_t launch_grouped_tc(int fmt, bool gate_up, const TcMaps& maps, const TcParams& p, int num_sms,
+                              cudaStream_t st) {
+    if (gate_up) {
+        switch (fmt) {
+            case MOE_W_BF16: return launch_tc<MOE_W_BF16, true>(maps, p, num_sms, st);
+            case MOE_W_FP8_B128: return launch_tc<MOE_W_FP8_B128, true>(maps, p, num_sms, st);
+            case MOE_W_NVFP4: return launch_tc<MOE_W_NVFP4, true>(maps, p, num_sms, st);
+        }
+    } else {
+        switch (fmt) {
+            case MOE_W_BF16: return launch_tc<MOE_W_BF16, false>(maps, p, num_sms, st);
+            case MOE_W_FP8_B128: return launch_tc<MOE_W_FP8_B128, false>(maps, p, num_sms, st);
+            case MOE_W_NVFP4: return launch_tc<MOE_W_NVFP4, false>(maps, p, num_sms, st);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

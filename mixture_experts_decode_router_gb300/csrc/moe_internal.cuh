@@ -1,0 +1,220 @@
+// moe_internal.cuh -- device helpers and host/device structures shared by the
+// kernels of libmoe_gb300 (sm_103a).  Nothing here is part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kWarp = 32;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+// ----------------------------------------------------------------------------
+// Workspace layout.  The control block sits at offset 0 for every n; the other
+// regions follow, each 256-byte aligned, sized for the call's n.
+// ----------------------------------------------------------------------------
+struct Ctrl {
+    int32_t n_active;      // experts with at least one route (written by the group kernel)
+    int32_t n_rsegs;       // routed token segments of <= kTcTokensPerTile (group kernel)
+    int32_t err;           // sticky device error code (bounded waits that gave up); 0 = none
+    int32_t pad[61];
+};
+
+// Tokens per tile of the grouped tensor-core path (its MMA N is at most this).
+constexpr int kTcTokensPerTile = 128;
+
+struct WsLayout {
+    size_t ctrl, logits, sg_logit, idx, w, counts, offsets, perm, active, act, act_sh,
+        inv, segs, xs, xh, as, ash, y, ysh, total;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Upper bound of the routed segments (<= kTcTokensPerTile routes of one expert):
+// sum_e ceil(c_e / T) <= (n*k)/T + min(E, n*k).
+inline int64_t grouped_segs_bound(int64_t n, int64_t k, int64_t E) {
+    const int64_t nk = n * k;
+    return nk / kTcTokensPerTile + (nk < E ? nk : E) + 1;
+}
+
+inline WsLayout ws_layout(const moe_config_t& c, int64_t n) {
+    WsLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    const int64_t E = c.num_experts, k = c.top_k, H = c.hidden, I = c.inter, S = c.shared_inter;
+    L.ctrl = take(sizeof(Ctrl));
+    L.logits = take(sizeof(float) * n * E);
+    L.sg_logit = take(sizeof(float) * n);
+    L.idx = take(sizeof(int32_t) * n * k);
+    L.w = take(sizeof(float) * n * k);
+    L.counts = take(sizeof(int32_t) * E);
+    L.offsets = take(sizeof(int32_t) * (E + 1));
+    L.perm = take(sizeof(int32_t) * n * k);
+    L.active = take(sizeof(int32_t) * E);
+    L.act = take(sizeof(float) * n * k * I);
+    L.act_sh = take(sizeof(float) * n * (S > 0 ? S : 1));
+    // Grouped tensor-core path.
+    L.inv = take(sizeof(int32_t) * n * k);                       // route -> sorted position
+    L.segs = take(sizeof(int32_t) * 3 * grouped_segs_bound(n, k, E));
+    L.xs = take(sizeof(uint16_t) * n * k * H);                   // expert-sorted activations
+    L.xh = take(sizeof(uint16_t) * n * H);                       // f16 copy of x (NVFP4)
+    L.as = take(sizeof(uint16_t) * n * k * I);                   // SiLU(g)*u, sorted rows
+    L.ash = take(sizeof(uint16_t) * n * (S > 0 ? S : 1));
+    L.y = take(sizeof(float) * n * k * H);                       // weighted down rows
+    L.ysh = take(sizeof(float) * n * H);
+    L.total = off;
+    return L;
+}
+
+// ----------------------------------------------------------------------------
+// Device-side views of the weights.
+// ----------------------------------------------------------------------------
+struct QMatDev {
+    const uint8_t* w;       // base of the stacked matrix (bytes)
+    const void* scale;      // FP8: float blocks; NVFP4: E4M3 bytes
+    const float* scale2;    // NVFP4 per-expert
+    int out_dim, in_dim;
+};
+
+// ----------------------------------------------------------------------------
+// Small device helpers.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// 16-byte streaming load that does not allocate in L1 (each weight byte is used once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+    uint32_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+// Two FP8 E4M3 codes (low byte = first element) -> two floats, exactly.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+    uint32_t h2;
+    asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(two_codes));
+    __half2_raw raw;
+    raw.x = (unsigned short)(h2 & 0xffffu);
+    raw.y = (unsigned short)(h2 >> 16);
+    return __half22float2(__half2(raw));
+}
+
+// Two E2M1 codes in one byte (low nibble = first element) -> two floats, exactly.
+__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
+    uint32_t h2;
+    asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h2) : "r"(byte));
+    __half2_raw raw;
+    raw.x = (unsigned short)(h2 & 0xffffu);
+    raw.y = (unsigned short)(h2 >> 16);
+    return __half22float2(__half2(raw));
+}
+
+// One E4M3 code -> float (exact).
+__device__ __forceinline__ float e4m3_to_float(uint32_t code) {
+    return e4m3x2_to_float2(code & 0xffu).x;
+}
+
+// ----------------------------------------------------------------------------
+// Weight chunks: 8 consecutive elements of one row (along `in`), decoded to
+// fp32, plus the multiplier that applies to the whole chunk.  Every format's
+// chunk lies inside one scale block (FP8: 128 columns; NVFP4: 16 columns),
+// because chunks start at multiples of 8.
+// ----------------------------------------------------------------------------
+template <int FMT> struct WChunk;
+
+template <> struct WChunk<MOE_W_BF16> {
+    uint4 raw;
+    __device__ __forceinline__ void load(const QMatDev& m, int e, int row, int c) {
+        const uint16_t* base = reinterpret_cast<const uint16_t*>(m.w) +
+                               ((size_t)e * m.out_dim + row) * m.in_dim + (size_t)c * 8;
+        raw = ld_stream_v4(base);
+    }
+    __device__ __forceinline__ float scale(const QMatDev&, int, int, int) const { return 1.0f; }
+    __device__ __forceinline__ void decode(float (&v)[8]) const {
+        v[0] = bf16_lo(raw.x); v[1] = bf16_hi(raw.x); v[2] = bf16_lo(raw.y); v[3] = bf16_hi(raw.y);
+        v[4] = bf16_lo(raw.z); v[5] = bf16_hi(raw.z); v[6] = bf16_lo(raw.w); v[7] = bf16_hi(raw.w);
+    }
+};
+
+template <> struct WChunk<MOE_W_FP8_B128> {
+    uint2 raw;
+    __device__ __forceinline__ void load(const QMatDev& m, int e, int row, int c) {
+        const uint8_t* base = m.w + ((size_t)e * m.out_dim + row) * m.in_dim + (size_t)c * 8;
+        raw = ld_stream_v2(base);
+    }
+    __device__ __forceinline__ float scale(const QMatDev& m, int e, int row, int c) const {
+        const int ob = (m.out_dim + 127) >> 7, ib = (m.in_dim + 127) >> 7;
+        const float* s = reinterpret_cast<const float*>(m.scale) + (size_t)e * ob * ib;
+        return __ldg(s + (row >> 7) * ib + ((c * 8) >> 7));
+    }
+    __device__ __forceinline__ void decode(float (&v)[8]) const {
+        float2 a = e4m3x2_to_float2(raw.x & 0xffffu), b = e4m3x2_to_float2(raw.x >> 16);
+        float2 c2 = e4m3x2_to_float2(raw.y & 0xffffu), d = e4m3x2_to_float2(raw.y >> 16);
+        v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y; v[4] = c2.x; v[5] = c2.y; v[6] = d.x; v[7] = d.y;
+    }
+};
+
+template <> struct WChunk<MOE_W_NVFP4> {
+    uint32_t raw;
+    __device__ __forceinline__ void load(const QMatDev& m, int e, int row, int c) {
+        const uint8_t* base = m.w + ((size_t)e * m.out_dim + row) * (m.in_dim / 2) + (size_t)c * 4;
+        raw = ld_stream_u32(base);
+    }
+    __device__ __forceinline__ float scale(const QMatDev& m, int e, int row, int c) const {
+        const uint8_t* s = reinterpret_cast<const uint8_t*>(m.scale) +
+                           ((size_t)e * m.out_dim + row) * (m.in_dim / 16);
+        return e4m3_to_float(__ldg(s + (c >> 1)));
+    }
+    __device__ __forceinline__ void decode(float (&v)[8]) const {
+        float2 a = e2m1x2_to_float2(raw & 0xffu), b = e2m1x2_to_float2((raw >> 8) & 0xffu);
+        float2 c2 = e2m1x2_to_float2((raw >> 16) & 0xffu), d = e2m1x2_to_float2(raw >> 24);
+        v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y; v[4] = c2.x; v[5] = c2.y; v[6] = d.x; v[7] = d.y;
+    }
+};
+
+// Per-matrix multiplier applied after the row's dot product (NVFP4 scale2).
+template <int FMT>
+__device__ __forceinline__ float matrix_scale(const QMatDev& m, int e) {
+    if constexpr (FMT == MOE_W_NVFP4) return __ldg(m.scale2 + e);
+    else return 1.0f;
+}
+
+// 8 BF16 activations (16 bytes) -> floats.
+__device__ __forceinline__ void bf16x8_to_float(uint4 r, float (&v)[8]) {
+    v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x); v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
+    v[4] = bf16_lo(r.z); v[5] = bf16_hi(r.z); v[6] = bf16_lo(r.w); v[7] = bf16_hi(r.w);
+}
+
+__device__ __forceinline__ float dot8(const float (&a)[8], const float (&b)[8]) {
+    float s = a[0] * b[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) s = fmaf(a[i], b[i], s);
+    return s;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+}  // namespace moe

@@ -1,0 +1,84 @@
+// moe_launch.cuh -- kernel parameter blocks and launch entry points used by
+// the C ABI layer (moe_capi.cu).  Internal to libmoe_gb300.
+#pragma once
+
+#include <cuda.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+struct GateUpParams {
+    const uint16_t* x;
+    int n, H, I, S, k;
+    QMatDev gate, up, sh_gate, sh_up;
+    const int32_t* counts;
+    const int32_t* offsets;
+    const int32_t* perm;
+    const int32_t* active;
+    const Ctrl* ctrl;
+    float* act;      // [n*k, I], row = route id t*k + j
+    float* act_sh;   // [n, S]
+};
+
+struct DownParams {
+    int n, H, I, S, k, E;
+    QMatDev down, sh_down;
+    const int32_t* idx;
+    const float* w;
+    const float* act;
+    const float* act_sh;
+    const float* sg_logit;   // NULL = shared gate 1
+    uint16_t* out;
+};
+
+// Grouped tensor-core path (moe_grouped_tc.cu).
+struct TcMaps {
+    CUtensorMap w[2];    // routed weights: (gate, up) or (down)
+    CUtensorMap ws[2];   // shared-expert weights
+    CUtensorMap b;       // routed activations (expert-sorted rows)
+    CUtensorMap bs;      // shared-expert activations (token rows)
+};
+
+struct TcParams {
+    int out_dim, in_dim;     // routed matrix [out, in] per expert
+    int sh_out, sh_in;       // shared matrix (sh_out == 0: no shared expert)
+    int n, k;
+    const int32_t* segs;     // [n_rsegs][3] = (expert, first sorted row, tokens)
+    const Ctrl* ctrl;
+    const void* scale[2];    // routed scales (FP8 fp32 blocks / NVFP4 E4M3 bytes)
+    const void* sh_scale[2];
+    const float* scale2[2];  // NVFP4 per-expert fp32
+    const float* sh_scale2[2];
+    void* act_out;           // gate_up: sorted SiLU(g)*u rows [n*k, I] (bf16 / f16)
+    void* act_sh_out;        // gate_up: shared [n, S]
+    float* y;                // down: weighted rows [n*k, H]
+    float* y_sh;             // down: gated shared rows [n, H]
+    const float* route_w;    // [n*k] routing weights (by route id)
+    const int32_t* perm;     // sorted position -> route id
+    const float* sg_logit;   // shared gate logits or NULL
+    int32_t* err;            // Ctrl::err
+};
+
+bool build_tc_maps(int fmt, bool gate_up, const moe_weights_t* w, int E, int H, int I, int S, int n,
+                   int n_routes_max, const void* act_routed, const void* act_shared, TcMaps* maps);
+cudaError_t launch_grouped_tc(int fmt, bool gate_up, const TcMaps& maps, const TcParams& p, int num_sms,
+                              cudaStream_t st);
+cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const int32_t* perm,
+                          const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, int num_sms,
+                          cudaStream_t st);
+cudaError_t launch_combine(const float* y, const float* ysh, const int32_t* inv, int n, int H, int k,
+                           int has_shared, uint16_t* out, int num_sms, cudaStream_t st);
+
+cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, int E,
+                          const uint16_t* gw, float* logits, float* sg_logit, int num_sms,
+                          cudaStream_t st);
+cudaError_t launch_topk(const float* logits, int n, int E, int k, int routing, const float* bias,
+                        int norm, float scale, int32_t* idx, float* w, cudaStream_t st);
+cudaError_t launch_group(const int32_t* idx, int nk, int E, int32_t* counts, int32_t* offsets,
+                         int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs, Ctrl* ctrl,
+                         cudaStream_t st);
+cudaError_t launch_gate_up_tm(int fmt, const GateUpParams& gu, int num_sms, cudaStream_t st);
+cudaError_t launch_down_blend_tm(int fmt, const DownParams& dn, int num_sms, cudaStream_t st);
+
+}  // namespace moe

@@ -152,6 +152,28 @@ class QMatT:
     scale2: Optional[torch.Tensor] = None
 
 
+def matrix_dims(cfg: LayerConfig, tensor: str):
+    """(out, in) of one expert matrix of `tensor`."""
+    H, I, S = cfg.hidden, cfg.inter, cfg.shared_inter
+    return {"gate": (I, H), "up": (I, H), "down": (H, I), "sh_gate": (S, H), "sh_up": (S, H),
+            "sh_down": (H, S)}[tensor]
+
+
+def expert_matrix(cfg: LayerConfig, tensor: str, e: int, device="cpu"):
+    """The stored form of expert e's `tensor` matrix alone: (w, scale, scale2)
+    -- identical to slice e of the stacked tensor make_weights builds."""
+    out_d, in_d = matrix_dims(cfg, tensor)
+    m = torch.randn(out_d, in_d, generator=_gen(device, cfg.seed, tensor, e), device=device,
+                    dtype=torch.float32) * cfg.weight_std
+    if cfg.expert_fmt == FMT_BF16:
+        return m.to(torch.bfloat16), None, None
+    if cfg.expert_fmt == FMT_FP8_B128:
+        q, s = _quant_fp8_b128(m)
+        return q, s, None
+    q, s, s2 = _quant_nvfp4(m)
+    return q, s, s2
+
+
 def _stacked(cfg: LayerConfig, tensor: str, n_exp: int, out_d: int, in_d: int,
              device) -> QMatT:
     fmt = cfg.expert_fmt
@@ -168,16 +190,12 @@ def _stacked(cfg: LayerConfig, tensor: str, n_exp: int, out_d: int, in_d: int,
     else:
         raise ValueError(fmt)
     for e in range(n_exp):
-        m = torch.randn(out_d, in_d, generator=_gen(device, cfg.seed, tensor, e),
-                        device=device, dtype=torch.float32) * cfg.weight_std
-        if fmt == FMT_BF16:
-            w[e] = m.to(torch.bfloat16)
-        elif fmt == FMT_FP8_B128:
-            q, s = _quant_fp8_b128(m)
-            w[e], sc[e] = q, s
-        else:
-            q, s, s2v = _quant_nvfp4(m)
-            w[e], sc[e], s2[e] = q, s, s2v
+        q, s, s2v = expert_matrix(cfg, tensor, e, device)
+        w[e] = q
+        if fmt != FMT_BF16:
+            sc[e] = s
+        if fmt == FMT_NVFP4:
+            s2[e] = s2v
     if fmt == FMT_BF16:
         return QMatT(fmt, w)
     if fmt == FMT_FP8_B128:
@@ -199,11 +217,28 @@ class LayerWeights:
     shared_gate_w: Optional[torch.Tensor]    # bf16 [H]
 
 
+def make_router(cfg: LayerConfig, device="cpu") -> torch.Tensor:
+    return (torch.randn(cfg.num_experts, cfg.hidden, generator=_gen(device, cfg.seed, "router"),
+                        device=device) * cfg.weight_std).to(torch.bfloat16)
+
+
+def make_bias(cfg: LayerConfig, device="cpu") -> Optional[torch.Tensor]:
+    if cfg.routing != ROUTE_SIGMOID_BIAS:
+        return None
+    u = torch.rand(cfg.num_experts, generator=_gen(device, cfg.seed, "bias"), device=device)
+    return ((u * 2.0 - 1.0) * cfg.bias_range).to(torch.float32)
+
+
+def make_shared_gate_w(cfg: LayerConfig, device="cpu") -> Optional[torch.Tensor]:
+    if not cfg.shared_gate:
+        return None
+    return (torch.randn(cfg.hidden, generator=_gen(device, cfg.seed, "shared_gate_w"),
+                        device=device) * cfg.weight_std).to(torch.bfloat16)
+
+
 def make_weights(cfg: LayerConfig, device="cpu") -> LayerWeights:
     E, H, I, S = cfg.num_experts, cfg.hidden, cfg.inter, cfg.shared_inter
-    std = cfg.weight_std
-    router = (torch.randn(E, H, generator=_gen(device, cfg.seed, "router"), device=device)
-              * std).to(torch.bfloat16)
+    router = make_router(cfg, device)
     gate = _stacked(cfg, "gate", E, I, H, device)
     up = _stacked(cfg, "up", E, I, H, device)
     down = _stacked(cfg, "down", E, H, I, device)
@@ -213,15 +248,8 @@ def make_weights(cfg: LayerConfig, device="cpu") -> LayerWeights:
         sh_down = _stacked(cfg, "sh_down", 1, H, S, device)
     else:
         sh_gate = sh_up = sh_down = None
-    bias = None
-    if cfg.routing == ROUTE_SIGMOID_BIAS:
-        u = torch.rand(E, generator=_gen(device, cfg.seed, "bias"), device=device)
-        bias = ((u * 2.0 - 1.0) * cfg.bias_range).to(torch.float32)
-    sgw = None
-    if cfg.shared_gate:
-        sgw = (torch.randn(H, generator=_gen(device, cfg.seed, "shared_gate_w"),
-                           device=device) * std).to(torch.bfloat16)
-    return LayerWeights(cfg, router, gate, up, down, sh_gate, sh_up, sh_down, bias, sgw)
+    return LayerWeights(cfg, router, gate, up, down, sh_gate, sh_up, sh_down,
+                        make_bias(cfg, device), make_shared_gate_w(cfg, device))
 
 
 GapFn = Callable[[np.ndarray], np.ndarray]
