@@ -184,6 +184,29 @@ moe_status_t moe_forward_timed(const moe_config_t* cfg, const moe_weights_t* wts
                                void* ws, size_t ws_bytes, moe_stream_t stream,
                                void* const* events, int32_t n_events, int32_t* n_marks);
 
+/* Bytes of the static device workspace of moe_forward_static_ws. */
+#define MOE_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
+
+/* moe_forward for callers that cannot allocate device memory (no counterpart
+ * in the pages: an addition of this library).  A plugin whose host owns every
+ * allocation, or code that is recording a CUDA graph (where cudaMalloc is not
+ * allowed), may have input and output buffers but no way to get a workspace.
+ * This call takes none: its scratch is one file-scope device array of
+ * MOE_STATIC_WORKSPACE_BYTES that every GPU which loads the library keeps until
+ * the process exits.  It allocates nothing and calls no allocating routine.
+ *   Arguments, outputs and errors: as moe_forward, without ws / ws_bytes.
+ *   A call that would need more than MOE_STATIC_WORKSPACE_BYTES of workspace
+ *   (moe_workspace_bytes(cfg, n)) returns MOE_ERR_WORKSPACE and launches nothing.
+ *   The first call on each device looks up the array's device address and
+ *   clears its control block, synchronously; make that first call before any
+ *   stream capture.
+ *   Every call shares the one array: calls whose work overlaps on the GPU
+ *   (other streams, other host threads) race on it and must be serialised by
+ *   the caller. */
+moe_status_t moe_forward_static_ws(const moe_config_t* cfg, const moe_weights_t* wts,
+                                   const void* x, int32_t n, void* out,
+                                   int32_t* idx, float* w, moe_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char* moe_status_string(moe_status_t status);
 

@@ -36,7 +36,9 @@ MOE_PATH_GROUPED = 2
 
 # Every function include/moe.h declares.
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_experts", "moe_forward",
-            "moe_forward_timed", "moe_status_string", "moe_abi_version")
+            "moe_forward_timed", "moe_forward_static_ws", "moe_status_string", "moe_abi_version")
+
+MOE_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
 class moe_config_t(ctypes.Structure):
@@ -90,6 +92,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.moe_forward_timed.argtypes = [cfgp, wp, P, I32, P, P, P, P, S, P, P, I32,
                                       ctypes.POINTER(I32)]
     lib.moe_forward_timed.restype = ctypes.c_int
+    lib.moe_forward_static_ws.argtypes = [cfgp, wp, P, I32, P, P, P, P]
+    lib.moe_forward_static_ws.restype = ctypes.c_int
     lib.moe_status_string.argtypes = [ctypes.c_int]
     lib.moe_status_string.restype = ctypes.c_char_p
     lib.moe_abi_version.argtypes = []
@@ -151,6 +155,12 @@ def moe_forward_timed(cfg, wts, x, n, out, idx, w, ws, ws_bytes, stream, events)
                                  _ptr(w), _ptr(ws), int(ws_bytes), _stream(stream), arr,
                                  len(events), ctypes.byref(nm))
     return s, nm.value
+
+
+def moe_forward_static_ws(cfg, wts, x, n, out, idx, w, stream=None) -> int:
+    """moe_forward with the library's static device workspace (no ws argument)."""
+    return load().moe_forward_static_ws(_ref(cfg), _ref(wts), _ptr(x), int(n), _ptr(out), _ptr(idx),
+                                        _ptr(w), _stream(stream))
 
 
 def moe_status_string(status: int) -> str:

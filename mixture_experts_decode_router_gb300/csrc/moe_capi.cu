@@ -388,3 +388,14 @@ const char* moe_status_string(moe_status_t status) {
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
 
 }  // extern "C"
+
+namespace moe {
+// moe_forward with a workspace the caller of this function chose (used by the
+// static-workspace entry point in moe_noalloc.cu).
+moe_status_t forward_with_workspace(const moe_config_t* cfg, const moe_weights_t* wts, const void* x,
+                                    int32_t n, void* out, int32_t* idx, float* w, void* ws,
+                                    size_t ws_bytes, moe_stream_t stream) {
+    Marks mk;
+    return forward_impl(cfg, wts, x, n, out, idx, w, ws, ws_bytes, stream, mk);
+}
+}  // namespace moe
