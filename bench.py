@@ -30,7 +30,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer µs/call, tokens/s and HBM GB/s (frac of ~8 TB/s) at N=1–256"
-STAGES = ["router", "topk", "group", "gate_up", "down_blend"]
+# Kernel sequence of each expert path, by the number of stage markers a call records.
+STAGES_BY_MARKS = {
+    2: ["fused"],
+    6: ["router", "topk", "group", "gate_up", "down_blend"],
+    8: ["router", "topk", "group", "gather", "gate_up", "down", "combine"],
+}
 
 
 def parse_args(argv=None):
@@ -137,6 +142,22 @@ class ClockSampler:
         sms.sort()
         return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sms)}
+
+
+def max_over_ranks(v: float, device="cpu") -> float:
+    """The largest value any rank holds (the slowest rank's time), or v alone."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(world: int, n_tokens: int, steps: int, max_ms: float) -> float:
+    """Tokens all ranks processed over the slowest rank's device time."""
+    return world * n_tokens * steps / (max_ms * 1e-3)
 
 
 def _dist():
@@ -305,11 +326,7 @@ def run_ours(args):
         dist.barrier()
     clk = clocks.stop()
     per = np.array([a.elapsed_time(b) for a, b in zip(ev_s, ev_e)])   # ms
-    dev_ms = float(per.sum())
-    if world > 1:
-        tt = torch.tensor([dev_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        dev_ms = float(tt.item())
+    dev_ms = max_over_ranks(float(per.sum()), dev)
 
     # Touched bytes from this input's routing (constant over the steps).
     idx_h = idx.cpu().numpy()
@@ -318,42 +335,54 @@ def run_ours(args):
 
     # Per-stage durations (moe_forward_timed: events between the kernels).
     Kp = min(K, 500)
-    nst = len(STAGES) + 1
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(Kp)]
+    nev = 10
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(Kp)]
     for row in evs:          # torch creates the CUDA event on its first record
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
+    nm = 0
     for i in range(Kp):
         flush.zero_()
         s, nm = B.moe_forward_timed(layer.c_cfg, layer.c_w, x, n, out, idx, wts, layer.ws,
                                     layer.ws_bytes, sptr, [e.cuda_event for e in evs[i]])
-        if s != B.MOE_OK or nm != nst:
+        if s != B.MOE_OK or nm not in STAGES_BY_MARKS:
             raise B.MoeError(f"timed forward: status {s}, markers {nm}")
     torch.cuda.synchronize()
-    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(nst - 1)]
+    stages_run = STAGES_BY_MARKS[nm]
+    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(nm - 1)]
                          for i in range(Kp)]).mean(axis=0)
+    dev_err = layer.device_error()
+    if dev_err:
+        raise B.MoeError(f"device error word {dev_err}")
 
     # Algorithmic bytes per launch of each stage.
     H, I, S, E, k = cfg.hidden, cfg.inter, cfg.shared_inter, cfg.num_experts, cfg.top_k
     mb = synth.matrix_bytes
     fmt = cfg.expert_fmt
+    nk = n * k
+    w_gu = distinct * 2 * mb(fmt, I, H) + (2 * mb(fmt, S, H) if S else 0)
+    w_dn = distinct * mb(fmt, H, I) + (mb(fmt, H, S) if S else 0)
     alg = {
+        "fused": touched,
         "router": E * H * 2 + n * H * 2 + n * E * 4,
-        "topk": n * E * 4 + n * k * 8 + (4 * E if lw.correction_bias is not None else 0),
-        "group": n * k * 4 + 4 * (3 * E + 1) + n * k * 4,
-        "gate_up": distinct * 2 * mb(fmt, I, H) + (2 * mb(fmt, S, H) if S else 0) + n * H * 2
-        + 4 * (n * k * I + n * S),
-        "down_blend": distinct * mb(fmt, H, I) + (mb(fmt, H, S) if S else 0)
-        + 4 * (n * k * I + n * S) + n * H * 2 + n * k * 8,
+        "topk": n * E * 4 + nk * 8 + (4 * E if lw.correction_bias is not None else 0),
+        "group": nk * 4 + 4 * (3 * E + 1) + nk * 4,
+        # token-major: fp32 activations; grouped: 16-bit activations
+        "gate_up": w_gu + n * H * 2 + (4 if nm == 6 else 2) * (nk * I + n * S)
+        + (2 * (nk * H + (n * H if fmt == "nvfp4" else 0)) if nm == 8 else 0),
+        "down_blend": w_dn + 4 * (nk * I + n * S) + n * H * 2 + nk * 8,
+        "gather": 2 * 2 * (nk * H + (n * H if fmt == "nvfp4" else 0)),
+        "down": w_dn + 2 * (nk * I + n * S) + 4 * (nk * H + (n * H if S else 0)),
+        "combine": 4 * (nk * H + (n * H if S else 0)) + n * H * 2 + nk * 4,
     }
     peak, peak_kind = _peaks()
-    dom = STAGES[int(np.argmax(stage_ms))]
-    dom_ms = float(stage_ms[STAGES.index(dom)])
+    dom = stages_run[int(np.argmax(stage_ms))]
+    dom_ms = float(stage_ms[stages_run.index(dom)])
     achieved = alg[dom] / (dom_ms * 1e-3) / 1e9
     stages = {s: {"us": round(float(stage_ms[j]) * 1e3, 3), "alg_bytes": int(alg[s]),
                   "gbs": round(alg[s] / (stage_ms[j] * 1e-3) / 1e9, 1)}
-              for j, s in enumerate(STAGES)}
+              for j, s in enumerate(stages_run)}
 
     # End to end through the public API: pinned host input, H2D, call, D2H.
     x_h = x.cpu().pin_memory()
@@ -373,11 +402,7 @@ def run_ours(args):
         out_h.copy_(out, non_blocking=True)
         e2e_[i].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = float(np.sum([a.elapsed_time(b) for a, b in zip(e2s, e2e_)]))
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(float(np.sum([a.elapsed_time(b) for a, b in zip(e2s, e2e_)])), dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -385,7 +410,7 @@ def run_ours(args):
 
     if rank == 0:
         ms_step = dev_ms / K
-        tok_s = world * n * K / (dev_ms * 1e-3)
+        tok_s = whole_job_tokens_per_s(world, n, K, dev_ms)
         line = {
             "metric": METRIC,
             "value": round(tok_s, 2),
@@ -412,14 +437,14 @@ def run_ours(args):
                        "l2": "flushed between steps (2.5x L2 write), flush outside the events",
                        "parallelism": f"replicas{world}" if world > 1 else "single"},
             "wall_s_timed_loop": round(t1 - t0, 3),
-            "gpu_launches": K * len(STAGES),
+            "gpu_launches": K * len(stages_run),
             "stages": stages,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": _traffic(dom, cfg.name),
                          "alg_bytes_per_launch": int(alg[dom]),
                          "avg_launch_us": round(dom_ms * 1e3, 3)},
-            "e2e": {"value": round(world * n * Ke / (e2e_ms * 1e-3), 2), "unit": "tokens/s",
+            "e2e": {"value": round(whole_job_tokens_per_s(world, n, Ke, e2e_ms), 2), "unit": "tokens/s",
                     "h2d_bytes_per_step": n * H * 2, "d2h_bytes_per_step": n * H * 2,
                     "us_per_call": round(e2e_ms / Ke * 1e3, 3)},
             "clocks": clk,

@@ -37,9 +37,15 @@
  *  - Asynchronous device faults are not reported by the call that enqueued
  *    the work; they surface from the next CUDA call as usual.
  *  - n == 0 is a valid no-op (MOE_OK, nothing launched).
- *  - The workspace is scratch the layer reuses across its steps; its content
- *    is not meaningful between calls.  Two calls that run at the same time on
- *    the GPU must not share a workspace.
+ *  - The workspace is scratch the layer reuses across its steps.  Its first 256
+ *    bytes are a control block that must be zero before the first call (for
+ *    example cudaMemsetAsync(ws, 0, 256, stream) after allocating it); every
+ *    call leaves it zero again.  The rest is not meaningful between calls.  Two
+ *    calls that run at the same time on the GPU must not share a workspace.
+ *  - Device-side failures that the kernels detect themselves (a bounded wait
+ *    that gave up after 2 s, or a control block that was not zeroed) end the
+ *    kernel early and set an error word in the workspace: read it with
+ *    moe_workspace_check().  The output of such a call is not valid.
  *
  * Tensor layouts (row-major, C order)
  * -----------------------------------
@@ -206,6 +212,17 @@ moe_status_t moe_forward_timed(const moe_config_t* cfg, const moe_weights_t* wts
 moe_status_t moe_forward_static_ws(const moe_config_t* cfg, const moe_weights_t* wts,
                                    const void* x, int32_t n, void* out,
                                    int32_t* idx, float* w, moe_stream_t stream);
+
+/* Reads, then clears, the device error word of a workspace.  Synchronises
+ * `stream` (the only entry point that does).
+ *   device_error (out)  0: no failure since the last check; 11-16: a bounded
+ *                       wait of the single-token kernel gave up; 1-4: a bounded
+ *                       wait of the grouped tensor-core kernels gave up; 20: the
+ *                       workspace control block was not zeroed before use.
+ * Errors: MOE_ERR_NULL, MOE_ERR_ALIGNMENT, MOE_ERR_WORKSPACE (ws_bytes < 256),
+ * MOE_ERR_CUDA. */
+moe_status_t moe_workspace_check(void* ws, size_t ws_bytes, int32_t* device_error,
+                                 moe_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char* moe_status_string(moe_status_t status);

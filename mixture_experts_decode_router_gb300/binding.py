@@ -36,7 +36,8 @@ MOE_PATH_GROUPED = 2
 
 # Every function include/moe.h declares.
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_experts", "moe_forward",
-            "moe_forward_timed", "moe_forward_static_ws", "moe_status_string", "moe_abi_version")
+            "moe_forward_timed", "moe_forward_static_ws", "moe_workspace_check", "moe_status_string",
+            "moe_abi_version")
 
 MOE_STATIC_WORKSPACE_BYTES = 16 << 20
 
@@ -94,6 +95,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.moe_forward_timed.restype = ctypes.c_int
     lib.moe_forward_static_ws.argtypes = [cfgp, wp, P, I32, P, P, P, P]
     lib.moe_forward_static_ws.restype = ctypes.c_int
+    lib.moe_workspace_check.argtypes = [P, S, ctypes.POINTER(I32), P]
+    lib.moe_workspace_check.restype = ctypes.c_int
     lib.moe_status_string.argtypes = [ctypes.c_int]
     lib.moe_status_string.restype = ctypes.c_char_p
     lib.moe_abi_version.argtypes = []
@@ -161,6 +164,13 @@ def moe_forward_static_ws(cfg, wts, x, n, out, idx, w, stream=None) -> int:
     """moe_forward with the library's static device workspace (no ws argument)."""
     return load().moe_forward_static_ws(_ref(cfg), _ref(wts), _ptr(x), int(n), _ptr(out), _ptr(idx),
                                         _ptr(w), _stream(stream))
+
+
+def moe_workspace_check(ws, ws_bytes, stream=None):
+    """(status, device error word); reads and clears the word, syncing the stream."""
+    v = ctypes.c_int32(0)
+    s = load().moe_workspace_check(_ptr(ws), int(ws_bytes), ctypes.byref(v), _stream(stream))
+    return s, v.value
 
 
 def moe_status_string(status: int) -> str:

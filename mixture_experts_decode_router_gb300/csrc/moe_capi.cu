@@ -146,7 +146,7 @@ static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w,
 }
 
 // Token counts up to this use the token-major CUDA-core kernels under AUTO.
-constexpr int kTokenMajorMaxN = 1 << 30;   // grouped path: forced only, until verified on the GPU
+constexpr int kTokenMajorMaxN = 16;
 
 // The grouped tensor-core expert stage (after the grouping kernel).
 static moe_status_t enqueue_grouped(const moe_config_t* c, const moe_weights_t* w, const void* x,
@@ -347,6 +347,42 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const moe_weights_t* w
     int32_t* idx_p = idx ? idx : at<int32_t>(ws, L.idx);
     float* w_p = w ? w : at<float>(ws, L.w);
     mk.mark(st);
+    if (n == 1 && cfg->path != MOE_PATH_GROUPED) {
+        // One token: the whole layer in one cooperative launch when its
+        // shared-memory plan fits (same arithmetic as the kernels below).
+        const int sms = device_sm_count();
+        FusedParams fp{};
+        if (fused_plan(cfg, sms, &fp)) {
+            const int H = cfg->hidden, I = cfg->inter, S = cfg->shared_inter;
+            fp.x = static_cast<const uint16_t*>(x);
+            fp.H = H; fp.E = cfg->num_experts; fp.k = cfg->top_k; fp.I = I; fp.S = S;
+            fp.routing = cfg->routing; fp.norm = cfg->norm_topk_prob; fp.scale = cfg->routed_scaling_factor;
+            fp.router = static_cast<const uint16_t*>(wts->router_w);
+            fp.gw = static_cast<const uint16_t*>(wts->shared_gate_w);
+            fp.bias = wts->correction_bias;
+            fp.gate = qdev(wts->gate, I, H);
+            fp.up = qdev(wts->up, I, H);
+            fp.down = qdev(wts->down, H, I);
+            if (S > 0) {
+                fp.sh_gate = qdev(wts->sh_gate, S, H);
+                fp.sh_up = qdev(wts->sh_up, S, H);
+                fp.sh_down = qdev(wts->sh_down, H, S);
+            }
+            fp.logits = at<float>(ws, L.logits);
+            fp.sg_logit = at<float>(ws, L.sg_logit);
+            fp.act = at<float>(ws, L.act);
+            fp.act_sh = at<float>(ws, L.act_sh);
+            fp.idx_out = idx_p;
+            fp.w_out = w_p;
+            fp.out = static_cast<uint16_t*>(out);
+            fp.ctrl = at<Ctrl>(ws, L.ctrl);
+            if (launch_fused_n1(cfg->expert_fmt, fp, sms, st) == cudaSuccess) {
+                mk.mark(st);
+                return MOE_OK;
+            }
+            (void)cudaGetLastError();   // not launchable here: the multi-kernel path below
+        }
+    }
     if ((s = enqueue_route(cfg, wts, x, n, idx_p, w_p, nullptr, ws, L, st, mk)) != MOE_OK) return s;
     return enqueue_experts(cfg, wts, x, n, idx_p, w_p, out, ws, L, true, st, mk);
 }
@@ -369,6 +405,20 @@ moe_status_t moe_forward_timed(const moe_config_t* cfg, const moe_weights_t* wts
     const moe_status_t s = forward_impl(cfg, wts, x, n, out, idx, w, ws, ws_bytes, stream, mk);
     if (n_marks) *n_marks = mk.next;
     return s;
+}
+
+moe_status_t moe_workspace_check(void* ws, size_t ws_bytes, int32_t* device_error, moe_stream_t stream) {
+    if (!ws || !device_error) return MOE_ERR_NULL;
+    if (!aligned16(ws)) return MOE_ERR_ALIGNMENT;
+    if (ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Ctrl* c = static_cast<Ctrl*>(ws);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, &c->err, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(&c->err, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    *device_error = v;
+    return MOE_OK;
 }
 
 const char* moe_status_string(moe_status_t status) {

@@ -1,0 +1,466 @@
+// moe_fused_n1.cu -- the whole layer for one decode token in one launch (sm_103a).
+//
+// MoeLayer::forward (page "metrale_model_layers/layers/moe/forward.rs") runs
+// gate, topk, exp_gate_up, exp_silu_down and wsum_blend as separate launches
+// for one token.  At one token every step is a short weight stream, so the
+// launch and drain gaps between them cost more than the streams.  This kernel
+// does all of it in one cooperative, persistent launch (one CTA per SM), with
+// two grid barriers:
+//
+//  phase 0  every CTA computes its router rows (and the shared-gate row) and
+//           starts streaming the routing-independent work: its share of the
+//           shared expert's gate/up rows and its slice of the shared down rows.
+//           Grid barrier 1: all logits are written.
+//  phase 1  every CTA ranks the logits itself (block-wide, by counting) and
+//           streams its share of the routed experts' gate/up rows through a
+//           ring of TMA bulk copies, while the same copy engine prefetches its
+//           slice of the routed down rows into shared memory.
+//           Grid barrier 2: all SiLU(g)*u values are written.
+//  phase 2  every CTA computes its output columns from the down rows already
+//           in shared memory: down projection, routing-weighted sum and the
+//           shared expert, written as BF16.
+//
+// The arithmetic of every dot product, the top-k weights and the blend is the
+// same, operation for operation, as the token-major kernels' for one token,
+// so a token's output bits do not depend on which path or batch computed it.
+//
+// Warp 15 (one lane) issues the copies; warps 0-14 compute.  Every wait is
+// bounded (2 s), records an error code in the workspace and ends the kernel.
+#include <mutex>
+
+#include "moe_launch.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kFThreads = 512;
+constexpr int kFComputeWarps = 15;
+constexpr int kFCompute = kFComputeWarps * 32;
+constexpr int kRing = 8;
+
+template <int FMT>
+__device__ __forceinline__ void decode_at(const uint8_t* row, int c, float (&v)[8]) {
+    WChunk<FMT> ch;
+    if constexpr (FMT == MOE_W_BF16) ch.raw = *reinterpret_cast<const uint4*>(row + c * 16);
+    else if constexpr (FMT == MOE_W_FP8_B128) ch.raw = *reinterpret_cast<const uint2*>(row + c * 8);
+    else ch.raw = *reinterpret_cast<const uint32_t*>(row + c * 4);
+    ch.decode(v);
+}
+
+__device__ __forceinline__ size_t row_bytes_of(int fmt, int in_dim) {
+    return fmt == MOE_W_BF16 ? (size_t)in_dim * 2 : (fmt == MOE_W_FP8_B128 ? (size_t)in_dim : (size_t)in_dim / 2);
+}
+
+template <int FMT>
+__device__ __forceinline__ const uint8_t* row_ptr(const QMatDev& m, int e, int row) {
+    return m.w + ((size_t)e * m.out_dim + row) * row_bytes_of(FMT, m.in_dim);
+}
+
+// Lane partial of one down-projection row against an activation vector, with
+// the token-major kernel's chunk order and per-chunk scale.
+template <int FMT>
+__device__ __forceinline__ float row_partial_smem(const uint8_t* drow, const float* a, const QMatDev& M, int e,
+                                                  int h, int K, int lane) {
+    float acc2 = 0.f;
+    for (int c = lane; c < (K >> 3); c += 32) {
+        float wv[8], av[8];
+        decode_at<FMT>(drow, c, wv);
+        WChunk<FMT> sch;
+        const float cs = sch.scale(M, e, h, c);
+        const float4 a0 = reinterpret_cast<const float4*>(a)[2 * c];
+        const float4 a1 = reinterpret_cast<const float4*>(a)[2 * c + 1];
+        av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
+        av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
+        acc2 = fmaf(dot8(wv, av), cs, acc2);
+    }
+    return acc2;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParams p) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x, cta = blockIdx.x;
+    const int H = p.H, E = p.E, k = p.k, I = p.I, S = p.S;
+
+    uint16_t* sx = reinterpret_cast<uint16_t*>(sm + p.off_x);
+    float* slg = reinterpret_cast<float*>(sm + p.off_lg);
+    float* ssc = reinterpret_cast<float*>(sm + p.off_sc);
+    int* ssel = reinterpret_cast<int*>(sm + p.off_sel);
+    float* sselw = reinterpret_cast<float*>(sm + p.off_sel + 128);
+    uint8_t* sring = sm + p.off_ring;
+    uint8_t* sdown = sm + p.off_down;
+    float* sact = reinterpret_cast<float*>(sm + p.off_act);
+    // Ring items are consumed by different warps, so a slot's phase parity
+    // cannot tell a warp whether its own item or an older one is in the slot:
+    // each item has its own single-use "full" barrier.  The slots' "empty"
+    // barriers have one in-order waiter (the producer) and stay per slot.
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.off_bar);
+    uint64_t* empty = bars;
+    uint64_t* dfull = bars + kRing;
+    uint64_t* dshfull = dfull + 1;
+    uint64_t* sel_ready = dshfull + 1;
+    volatile int* abort_f = reinterpret_cast<volatile int*>(sel_ready + 1);
+    volatile int* s_go = abort_f + 1;   // phase decision, written by tid 0 before a barrier
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + p.off_bar + (kRing + 3) * 8 + 16);   // [max_items]
+    Ctrl* ctrl = p.ctrl;
+    int32_t* err = &ctrl->err;
+
+    if (tid == 0) {
+        for (int s = 0; s < kRing; ++s) ptx::mbar_init(&empty[s], 1);
+        for (int s = 0; s < p.max_items; ++s) ptx::mbar_init(&full[s], 1);
+        ptx::mbar_init(dfull, 1);
+        ptx::mbar_init(dshfull, 1);
+        ptx::mbar_init(sel_ready, 1);
+        // The control block must be clean at the start of a call (zeroed once,
+        // kept zero by every call); anything else is a workspace that was not
+        // initialised: refuse before touching it.
+        const bool clean = ptx::ld_acquire_gpu(&ctrl->gexit) == 0 &&
+                           ptx::ld_acquire_gpu(&ctrl->gbar) < (uint32_t)G;
+        if (!clean) atomicExch(err, 20);
+        *abort_f = clean ? 0 : 2;
+        ptx::fence_mbar_init();
+    }
+    for (int i = tid; i < H / 8; i += kFThreads)
+        reinterpret_cast<uint4*>(sx)[i] = __ldg(reinterpret_cast<const uint4*>(p.x) + i);
+    __syncthreads();
+    const bool refused = *abort_f == 2;
+
+    // Work of this CTA.
+    const int rpc = p.rpc;
+    const int h0 = cta * rpc, h1 = min(H, h0 + rpc), nrows = max(0, h1 - h0);
+    const int sh_b = (int)((int64_t)S * cta / G), sh_e = (int)((int64_t)S * (cta + 1) / G);
+    const int64_t Q = (int64_t)k * I;
+    const int r_b = (int)(Q * cta / G), r_e = (int)(Q * (cta + 1) / G);
+    const int n_sh = sh_e - sh_b, n_r = r_e - r_b;
+    const uint32_t row_bytes = p.row_bytes;   // one gate/up row (H elements)
+    const uint32_t slot_bytes = 2 * row_bytes;
+    const int C = H >> 3;
+
+    if (refused) {
+        // nothing: the error word says why
+    } else if (warp == kFComputeWarps) {
+        // ------------------------------------------------------------ copy producer
+        if (lane == 0) {
+            uint32_t seq = 0;
+            bool ok = true;
+            auto issue_pair = [&](const QMatDev& Gm, const QMatDev& Um, int e, int row) -> bool {
+                const uint32_t slot = seq % kRing;
+                if (!ptx::mbar_wait(&empty[slot], ((seq / kRing) & 1) ^ 1, abort_f, err, 11)) return false;
+                ptx::mbar_arrive_expect_tx(&full[seq], slot_bytes);
+                ptx::bulk_load(sring + slot * slot_bytes, row_ptr<FMT>(Gm, e, row), row_bytes, &full[seq]);
+                ptx::bulk_load(sring + slot * slot_bytes + row_bytes, row_ptr<FMT>(Um, e, row), row_bytes,
+                               &full[seq]);
+                ++seq;
+                return true;
+            };
+            // Shared down slice, then the shared gate/up rows (routing-independent).
+            if (S > 0 && nrows > 0) {
+                ptx::mbar_arrive_expect_tx(dshfull, nrows * p.dsh_row_bytes);
+                ptx::bulk_load(sdown + (size_t)k * rpc * p.drow_bytes, row_ptr<FMT>(p.sh_down, 0, h0),
+                               nrows * p.dsh_row_bytes, dshfull);
+            } else {
+                ptx::mbar_arrive(dshfull);
+            }
+            for (int i = sh_b; ok && i < sh_e; ++i) ok = issue_pair(p.sh_gate, p.sh_up, 0, i);
+            // Routed work, once this CTA has its routing.
+            if (ok) ok = ptx::mbar_wait(sel_ready, 0, abort_f, err, 12);
+            if (ok) {
+                if (nrows > 0) {
+                    ptx::mbar_arrive_expect_tx(dfull, (uint32_t)(k * nrows * p.drow_bytes));
+                    for (int j = 0; j < k; ++j)
+                        ptx::bulk_load(sdown + (size_t)j * rpc * p.drow_bytes, row_ptr<FMT>(p.down, ssel[j], h0),
+                                       nrows * p.drow_bytes, dfull);
+                } else {
+                    ptx::mbar_arrive(dfull);
+                }
+                for (int q = r_b; ok && q < r_e; ++q) {
+                    const int j = q / I, i = q - j * I;
+                    ok = issue_pair(p.gate, p.up, ssel[j], i);
+                }
+            }
+            if (!ok) {
+                // Let every copy issued land before the CTA exits.
+                const uint32_t nb = seq < (uint32_t)kRing ? seq : kRing;
+                for (uint32_t q = 0; q < nb; ++q) ptx::mbar_wait_quiet(&full[seq - 1 - q], 0, 100000000ull);
+                ptx::mbar_wait_quiet(dfull, 0, 100000000ull);
+                ptx::mbar_wait_quiet(dshfull, 0, 100000000ull);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ compute warps
+        // Phase 0a: router rows r = cta + G * warp (r == E: the shared-gate row),
+        // with the router kernel's chunk order.
+        {
+            const int r = cta + G * warp;
+            if (r < E + (p.gw ? 1 : 0)) {
+                const uint16_t* wrow = (r < E) ? p.router + (size_t)r * H : p.gw;
+                float acc = 0.f;
+                for (int c = lane; c < C; c += 32) {
+                    float wv[8], xv[8];
+                    bf16x8_to_float(__ldg(reinterpret_cast<const uint4*>(wrow) + c), wv);
+                    bf16x8_to_float(reinterpret_cast<const uint4*>(sx)[c], xv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], xv[i], acc);
+                }
+                const float s = warp_sum(acc);
+                if (lane == 0) {
+                    if (r < E) p.logits[r] = s;
+                    else *p.sg_logit = s;
+                }
+            }
+        }
+        ptx::named_bar(1, kFCompute);
+        if (tid == 0) {
+            __threadfence();
+            atomicAdd(&ctrl->gbar, 1u);
+        }
+
+        // One gate/up ring item: SiLU(g) * u of weight row `row`, written to dst,
+        // with the token-major gate_up kernel's arithmetic.
+        auto consume = [&](uint32_t seq, const QMatDev& Gm, const QMatDev& Um, int e, int row, float msg,
+                           float msu, float* dst) -> bool {
+            const uint32_t slot = seq % kRing;
+            if (!ptx::mbar_wait_warp(&full[seq], 0, abort_f, err, 13)) return false;
+            const uint8_t* gr = sring + slot * slot_bytes;
+            const uint8_t* ur = gr + row_bytes;
+            float ag = 0.f, au = 0.f;
+            for (int c = lane; c < C; c += 32) {
+                float wg[8], wu[8], xv[8];
+                decode_at<FMT>(gr, c, wg);
+                decode_at<FMT>(ur, c, wu);
+                WChunk<FMT> sch;
+                const float sg = sch.scale(Gm, e, row, c), su = sch.scale(Um, e, row, c);
+                bf16x8_to_float(reinterpret_cast<const uint4*>(sx)[c], xv);
+                ag = fmaf(dot8(wg, xv), sg, ag);
+                au = fmaf(dot8(wu, xv), su, au);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&empty[slot]);
+            const float g = warp_sum(ag) * msg;
+            const float u = warp_sum(au) * msu;
+            if (lane == 0) *dst = silu(g) * u;
+            return true;
+        };
+
+        // Phase 0b: the shared expert's gate/up rows of this CTA.
+        const float msg_sh = S > 0 ? matrix_scale<FMT>(p.sh_gate, 0) : 1.f;
+        const float msu_sh = S > 0 ? matrix_scale<FMT>(p.sh_up, 0) : 1.f;
+        bool ok = true;
+        for (int s = warp; ok && s < n_sh; s += kFComputeWarps)
+            ok = consume(s, p.sh_gate, p.sh_up, 0, sh_b + s, msg_sh, msu_sh, p.act_sh + sh_b + s);
+
+        // Grid barrier 1: every logit is written.
+        ptx::named_bar(1, kFCompute);
+        if (tid == 0) {
+            const uint64_t t0 = ptx::globaltimer();
+            while (ptx::ld_acquire_gpu(&ctrl->gbar) < (uint32_t)G) {
+                if (*abort_f) break;
+                if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+                    atomicExch(err, 14);
+                    *abort_f = 1;
+                    break;
+                }
+            }
+            *s_go = *abort_f ? 0 : 1;
+        }
+        ptx::named_bar(1, kFCompute);
+        const bool go1 = *s_go != 0;    // the same value for every compute thread
+
+        if (go1) {
+            // Phase 1a: routing, computed by every CTA for itself.
+            for (int e = tid; e < E; e += kFCompute) {
+                const float l = __ldcg(p.logits + e);
+                float sc;
+                if (p.routing == MOE_ROUTE_SOFTMAX) sc = l;
+                else sc = 1.0f / (1.0f + expf(-l)) + p.bias[e];
+                if (sc != sc) sc = -INFINITY;
+                slg[e] = l;
+                ssc[e] = sc;
+            }
+            ptx::named_bar(1, kFCompute);
+            // Rank = experts ahead in (score desc, index asc): selected iff rank < k.
+            for (int e = tid; e < E; e += kFCompute) {
+                const float v = ssc[e];
+                int rank = 0;
+                for (int f = 0; f < E; ++f) {
+                    const float u = ssc[f];
+                    rank += (u > v || (u == v && f < e)) ? 1 : 0;
+                }
+                if (rank < k) ssel[rank] = e;
+            }
+            ptx::named_bar(1, kFCompute);
+            if (tid == 0) ptx::mbar_arrive(sel_ready);
+            if (warp == 0) {
+                // Routing weights, with the top-k kernel's arithmetic.
+                const int sel_e = lane < k ? ssel[lane] : -1;
+                const float sel_l = lane < k ? slg[sel_e] : 0.f;
+                float pr;
+                if (p.routing == MOE_ROUTE_SOFTMAX) {
+                    const float mx = __shfl_sync(0xffffffffu, sel_l, 0);
+                    float z = 0.f;
+                    for (int i = 0; lane + 32 * i < E; ++i) z += expf(slg[lane + 32 * i] - mx);
+                    z = warp_sum(z);
+                    pr = (lane < k) ? expf(sel_l - mx) / z : 0.f;
+                } else {
+                    pr = (lane < k) ? 1.0f / (1.0f + expf(-sel_l)) : 0.f;
+                }
+                if (p.norm) {
+                    const float tot = warp_sum(pr);
+                    pr = pr / tot;
+                }
+                if (lane < k) {
+                    sselw[lane] = pr * p.scale;
+                    if (cta == 0) {
+                        p.idx_out[lane] = sel_e;
+                        p.w_out[lane] = pr * p.scale;
+                    }
+                }
+            }
+            ptx::named_bar(1, kFCompute);
+
+            // Phase 1b: the routed gate/up rows of this CTA.
+            for (int s = warp; ok && s < n_sh + n_r; s += kFComputeWarps) {
+                if (s < n_sh) continue;
+                const int q = r_b + (s - n_sh);
+                const int j = q / I, i = q - j * I, e = ssel[j];
+                ok = consume(s, p.gate, p.up, e, i, matrix_scale<FMT>(p.gate, e), matrix_scale<FMT>(p.up, e),
+                             p.act + (size_t)j * I + i);
+            }
+        }
+
+        // Grid barrier 2: every SiLU(g) * u is written.
+        ptx::named_bar(1, kFCompute);
+        if (tid == 0) {
+            if (!*abort_f) {
+                __threadfence();
+                atomicAdd(&ctrl->gbar, 1u);
+                const uint64_t t0 = ptx::globaltimer();
+                while (ptx::ld_acquire_gpu(&ctrl->gbar) < 2u * G) {
+                    if (*abort_f) break;
+                    if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+                        atomicExch(err, 15);
+                        *abort_f = 1;
+                        break;
+                    }
+                }
+            }
+            *s_go = *abort_f ? 0 : 1;
+        }
+        ptx::named_bar(1, kFCompute);
+        const bool go2 = *s_go != 0;
+
+        if (go2 && nrows > 0) {
+            // Phase 2: down rows [h0, h1) from shared memory.
+            for (int i = tid; i < k * I; i += kFCompute) sact[i] = __ldcg(p.act + i);
+            for (int i = tid; i < S; i += kFCompute) sact[k * I + i] = __ldcg(p.act_sh + i);
+            ptx::named_bar(1, kFCompute);
+            const bool ok_d = ptx::mbar_wait_warp(dfull, 0, abort_f, err, 16) &&
+                              ptx::mbar_wait_warp(dshfull, 0, abort_f, err, 16);
+            if (ok_d) {
+                float gs = 1.0f;
+                if (p.gw) gs = 1.0f / (1.0f + expf(-__ldcg(p.sg_logit)));
+                if (S > 0) gs *= matrix_scale<FMT>(p.sh_down, 0);
+                for (int h = h0 + warp; h < h1; h += kFComputeWarps) {
+                    float acc = 0.f;
+                    for (int j = 0; j < k; ++j) {
+                        const int e = ssel[j];
+                        const float wt = sselw[j] * matrix_scale<FMT>(p.down, e);
+                        const uint8_t* drow = sdown + ((size_t)j * rpc + (h - h0)) * p.drow_bytes;
+                        acc = fmaf(row_partial_smem<FMT>(drow, sact + (size_t)j * I, p.down, e, h, I, lane), wt,
+                                   acc);
+                    }
+                    if (S > 0) {
+                        const uint8_t* drow =
+                            sdown + (size_t)k * rpc * p.drow_bytes + (size_t)(h - h0) * p.dsh_row_bytes;
+                        acc = fmaf(row_partial_smem<FMT>(drow, sact + (size_t)k * I, p.sh_down, 0, h, S, lane), gs,
+                                   acc);
+                    }
+                    const float s = warp_sum(acc);
+                    if (lane == 0) {
+                        const __nv_bfloat16 b = __float2bfloat16_rn(s);
+                        p.out[h] = *reinterpret_cast<const uint16_t*>(&b);
+                    }
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (tid == 0 && !refused) {
+        // The last CTA out returns the control block to zero for the next call.
+        __threadfence();
+        const uint32_t prev = atomicAdd(&ctrl->gexit, 1u);
+        if (prev == (uint32_t)G - 1) {
+            atomicExch(&ctrl->gbar, 0u);
+            atomicExch(&ctrl->gexit, 0u);
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace
+
+// Shared-memory plan of the fused kernel; returns false if it does not fit.
+bool fused_plan(const moe_config_t* c, int num_sms, FusedParams* p) {
+    const int H = c->hidden, E = c->num_experts, k = c->top_k, I = c->inter, S = c->shared_inter;
+    auto rb = [&](int in_dim) -> uint32_t {
+        return c->expert_fmt == MOE_W_BF16 ? in_dim * 2 : (c->expert_fmt == MOE_W_FP8_B128 ? in_dim : in_dim / 2);
+    };
+    p->rpc = (H + num_sms - 1) / num_sms;
+    p->row_bytes = rb(H);
+    p->drow_bytes = rb(I);
+    p->dsh_row_bytes = rb(S > 0 ? S : 32);
+    if (S > 0 && p->dsh_row_bytes > p->drow_bytes) return false;   // the shared slice uses the routed slot size
+    if (E + 1 > kFComputeWarps * num_sms) return false;              // one router row per compute warp
+    size_t off = 0;
+    auto take = [&](size_t b, size_t al) { off = (off + al - 1) / al * al; size_t o = off; off += b; return (uint32_t)o; };
+    p->off_x = take((size_t)H * 2, 128);
+    p->off_lg = take((size_t)E * 4, 16);
+    p->off_sc = take((size_t)E * 4, 16);
+    p->off_sel = take(256, 16);
+    p->off_ring = take((size_t)kRing * 2 * p->row_bytes, 128);
+    p->off_down = take((size_t)(k + 1) * p->rpc * p->drow_bytes, 128);
+    p->off_act = take(((size_t)k * I + (S > 0 ? S : 0)) * 4, 16);
+    // empty[kRing], dfull, dshfull, sel_ready, abort + phase flags, full[max_items]
+    p->max_items = (S + num_sms - 1) / num_sms + (int)(((int64_t)k * I + num_sms - 1) / num_sms) + 1;
+    p->off_bar = take((kRing + 3) * 8 + 16 + (size_t)p->max_items * 8, 8);
+    p->smem_bytes = (uint32_t)off;
+    return off <= 227 * 1024 && k <= 32 && (size_t)k * p->rpc * p->drow_bytes < (1u << 20);
+}
+
+cudaError_t launch_fused_n1(int fmt, const FusedParams& p, int num_sms, cudaStream_t st) {
+    const void* fn = nullptr;
+    switch (fmt) {
+        case MOE_W_BF16: fn = reinterpret_cast<const void*>(fused_n1_kernel<MOE_W_BF16>); break;
+        case MOE_W_FP8_B128: fn = reinterpret_cast<const void*>(fused_n1_kernel<MOE_W_FP8_B128>); break;
+        case MOE_W_NVFP4: fn = reinterpret_cast<const void*>(fused_n1_kernel<MOE_W_NVFP4>); break;
+        default: return cudaErrorInvalidValue;
+    }
+    // Per device and format: the largest dynamic shared memory configured so
+    // far (set once, re-set only when a larger plan arrives).
+    static std::mutex mu;
+    static uint32_t configured[128][3] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (configured[dev][fmt] < p.smem_bytes) {
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)p.smem_bytes);
+            if (e != cudaSuccess) return e;
+            int per_sm = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kFThreads, p.smem_bytes);
+            if (e != cudaSuccess) return e;
+            if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+            configured[dev][fmt] = p.smem_bytes;
+        }
+    }
+    FusedParams pc = p;
+    void* args[] = {&pc};
+    return cudaLaunchCooperativeKernel(fn, dim3(num_sms), dim3(kFThreads), args, p.smem_bytes, st);
+}
+
+}  // namespace moe

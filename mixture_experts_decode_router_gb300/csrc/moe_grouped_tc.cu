@@ -29,6 +29,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "moe_launch.cuh"
 #include "tc_ptx.cuh"
 
@@ -510,8 +512,18 @@ template <int FMT, bool GU>
 cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int num_sms, cudaStream_t st) {
     using C = TcCfg<FMT, GU>;
     auto kern = grouped_tc_kernel<FMT, GU>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static bool configured[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!configured[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+            if (e != cudaSuccess) return e;
+            configured[dev] = true;
+        }
+    }
     kern<<<num_sms, C::kThreads, C::kSmem, st>>>(maps, p);
     return cudaGetLastError();
 }

@@ -70,6 +70,32 @@ cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const
 cudaError_t launch_combine(const float* y, const float* ysh, const int32_t* inv, int n, int H, int k,
                            int has_shared, uint16_t* out, int num_sms, cudaStream_t st);
 
+// Fused single-token kernel (moe_fused_n1.cu).
+struct FusedParams {
+    const uint16_t* x;
+    int H, E, k, I, S, routing, norm;
+    float scale;
+    const uint16_t* router;
+    const uint16_t* gw;       // shared-gate weight or NULL
+    const float* bias;
+    QMatDev gate, up, down, sh_gate, sh_up, sh_down;
+    float* logits;            // [E]
+    float* sg_logit;          // [1]
+    float* act;               // [k * I]
+    float* act_sh;            // [S]
+    int32_t* idx_out;         // [k]
+    float* w_out;             // [k]
+    uint16_t* out;            // [H]
+    Ctrl* ctrl;
+    int rpc;                  // output columns per CTA
+    int max_items;            // gate/up ring items a CTA can have (one barrier each)
+    uint32_t row_bytes, drow_bytes, dsh_row_bytes;
+    uint32_t off_x, off_lg, off_sc, off_sel, off_ring, off_down, off_act, off_bar, smem_bytes;
+};
+
+bool fused_plan(const moe_config_t* c, int num_sms, FusedParams* p);
+cudaError_t launch_fused_n1(int fmt, const FusedParams& p, int num_sms, cudaStream_t st);
+
 cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, int E,
                           const uint16_t* gw, float* logits, float* sg_logit, int num_sms,
                           cudaStream_t st);

@@ -66,7 +66,8 @@ class MoeLayer:
         if self.ws_bytes == 0:
             raise B.MoeError("invalid layer configuration")
         dev = weights.router_w.device
-        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        # The control block (first 256 bytes) must start at zero; calls keep it zero.
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.max_tokens = max_tokens
 
     def forward(self, x: torch.Tensor, out=None, idx=None, w=None, stream=None):
@@ -79,6 +80,12 @@ class MoeLayer:
         B.check(B.moe_forward(self.c_cfg, self.c_w, x, n, out, idx, w, self.ws, self.ws_bytes,
                               stream))
         return out, idx, w
+
+    def device_error(self, stream=None) -> int:
+        """Reads and clears the workspace's device error word (syncs the stream)."""
+        s, v = B.moe_workspace_check(self.ws, self.ws_bytes, stream)
+        B.check(s)
+        return v
 
     def route(self, x: torch.Tensor, logits: bool = True, stream=None):
         n, k, E = x.shape[0], self.cfg.top_k, self.cfg.num_experts

@@ -146,8 +146,9 @@ def test_zero_tokens_is_a_noop():
     assert out.shape == (0, cfg.hidden)
 
 
-@pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_NVFP4])
-def test_rows_do_not_depend_on_the_batch(fmt):
+@pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_FP8_B128, synth.FMT_NVFP4])
+def test_rows_do_not_depend_on_the_batch_token_major(fmt):
+    """N <= 16 (one token: the fused kernel, which keeps the token-major arithmetic)."""
     cfg = small("invariance", expert_fmt=fmt, num_experts=32, top_k=4,
                 routing=synth.ROUTE_SIGMOID_BIAS, routed_scaling_factor=2.5)
     lw = synth.make_weights(cfg, "cuda")
@@ -158,11 +159,31 @@ def test_rows_do_not_depend_on_the_batch(fmt):
     perm = torch.randperm(12, generator=torch.Generator().manual_seed(3)).cuda()
     permuted, _, _ = layer.forward(x[perm])
     alone = torch.cat([layer.forward(x[r:r + 1])[0] for r in range(12)])
-    dup, _, _ = layer.forward(torch.cat([x, x[:5]]))
+    dup, _, _ = layer.forward(torch.cat([x, x[:4]]))
     torch.cuda.synchronize()
     assert torch.equal(permuted, full[perm])
     assert torch.equal(alone, full)
-    assert torch.equal(dup[12:], full[:5])
+    assert torch.equal(dup[12:], full[:4])
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_FP8_B128, synth.FMT_NVFP4])
+def test_rows_do_not_depend_on_the_batch_grouped(fmt):
+    """N > 16: the expert-grouped tensor-core path."""
+    cfg = small("invariance_g", expert_fmt=fmt, num_experts=32, top_k=4,
+                routing=synth.ROUTE_SIGMOID_BIAS, routed_scaling_factor=2.5)
+    lw = synth.make_weights(cfg, "cuda")
+    L = oracle_layer(lw)
+    x = synth.make_input(cfg, 40, "cuda", gap_fn=gap_fn_for(L))
+    layer = MoeLayer(lw, 300)
+    full, _, _ = layer.forward(x)
+    perm = torch.randperm(40, generator=torch.Generator().manual_seed(4)).cuda()
+    permuted, _, _ = layer.forward(x[perm])
+    part, _, _ = layer.forward(x[:17])
+    many, _, _ = layer.forward(x.repeat(7, 1))        # 280 rows: experts past 128 tokens
+    torch.cuda.synchronize()
+    assert torch.equal(permuted, full[perm])
+    assert torch.equal(part, full[:17])
+    assert torch.equal(many[-40:], full)
 
 
 # ---------------------------------------------------------------- the five workloads at full size
@@ -177,3 +198,36 @@ def test_rows_do_not_depend_on_the_batch(fmt):
 def test_workloads_full_size(name, rows):
     cfg = synth.WORKLOADS[name]
     _check(cfg, rows=rows)
+
+
+# ---------------------------------------------------------------- device error word
+
+def test_workspace_check_clean_after_calls():
+    cfg = synth.WORKLOADS["decode_n1"]
+    lw = synth.make_weights(cfg, "cuda")
+    layer = MoeLayer(lw, 16)
+    for n in (1, 16):
+        layer.forward(synth.make_input(cfg, n, "cuda"))
+    assert layer.device_error() == 0
+    # The control block is back to zero after every call.
+    assert int(layer.ws[:256].count_nonzero()) == 0
+
+
+def test_single_token_kernel_refuses_a_dirty_control_block():
+    cfg = small("dirty", num_experts=32, top_k=4)
+    lw = synth.make_weights(cfg, "cuda")
+    L = oracle_layer(lw)
+    x = synth.make_input(cfg, 1, "cuda", gap_fn=gap_fn_for(L))
+    layer = MoeLayer(lw, 1)
+    good, _, _ = layer.forward(x)
+    torch.cuda.synchronize()
+    # A control block that was never zeroed (here: a grid-barrier word of all ones).
+    layer.ws[12:16] = 255
+    sentinel = torch.full_like(good, 7)
+    out, _, _ = layer.forward(x, out=sentinel.clone())
+    assert layer.device_error() == 20
+    assert torch.equal(out, sentinel)          # refused: nothing written
+    layer.ws[:256] = 0
+    again, _, _ = layer.forward(x)
+    assert layer.device_error() == 0
+    assert torch.equal(again, good)
