@@ -370,9 +370,9 @@ def run_ours(args):
         "group": nk * 4 + 4 * (3 * E + 1) + nk * 4,
         # token-major: fp32 activations; grouped: 16-bit activations
         "gate_up": w_gu + n * H * 2 + (4 if nm == 6 else 2) * (nk * I + n * S)
-        + (2 * (nk * H + (n * H if fmt == "nvfp4" else 0)) if nm == 8 else 0),
+        + (2 * (nk * H + (n * H if fmt != "bf16" else 0)) if nm == 8 else 0),
         "down_blend": w_dn + 4 * (nk * I + n * S) + n * H * 2 + nk * 8,
-        "gather": 2 * 2 * (nk * H + (n * H if fmt == "nvfp4" else 0)),
+        "gather": 2 * 2 * (nk * H + (n * H if fmt != "bf16" else 0)),
         "down": w_dn + 2 * (nk * I + n * S) + 4 * (nk * H + (n * H if S else 0)),
         "combine": 4 * (nk * H + (n * H if S else 0)) + n * H * 2 + nk * 4,
     }

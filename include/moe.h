@@ -40,7 +40,8 @@
  *  - The workspace is scratch the layer reuses across its steps.  Its first 256
  *    bytes are a control block that must be zero before the first call (for
  *    example cudaMemsetAsync(ws, 0, 256, stream) after allocating it); every
- *    call leaves it zero again.  The rest is not meaningful between calls.  Two
+ *    call leaves it valid for the next one.  The rest is not meaningful between
+ *    calls.  Two
  *    calls that run at the same time on the GPU must not share a workspace.
  *  - Device-side failures that the kernels detect themselves (a bounded wait
  *    that gave up after 2 s, or a control block that was not zeroed) end the

@@ -21,11 +21,13 @@
 // tokens (padded to a multiple of 16), so a thin token set still fills the
 // MMA.  Weights: BF16 arrive by TMA straight in the 128-byte swizzled K-major
 // layout the MMA reads; FP8 and NVFP4 arrive raw by TMA and eight dequant warps
-// rewrite them as BF16 (FP8: RNE(e4m3 * block scale)) or f16 (NVFP4:
-// e2m1 * e4m3 scale, exact in f16; the fp32 scale2 is applied to the
-// accumulator) in that layout.  NVFP4 tiles therefore run the f16 MMA with f16
-// activations.  Warp roles: 0 TMA producer, 1 MMA issuer (one thread) and TMEM
-// owner, 2-5 epilogue (TMEM -> registers -> global), 6-13 dequant.
+// rewrite them as f16 in that layout (FP8: RNE_f16(e4m3 * block scale), one
+// rounding with an 11-bit significand; NVFP4: e2m1 * e4m3 scale, exact in f16,
+// with the fp32 scale2 applied to the accumulator).  Those tiles run the f16
+// MMA with f16 activations (exact for BF16 inputs in f16's normal range,
+// saturated at +-65504).  Warp roles: 0 TMA producer, 1 MMA issuer (one
+// thread) and TMEM owner, 2-5 epilogue (TMEM -> registers -> global), 6-13
+// dequant.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -45,7 +47,7 @@ constexpr int NT = kTcTokensPerTile;   // tokens per tile (max MMA N)
 template <int FMT, bool GU>
 struct TcCfg {
     static constexpr bool kDeq = FMT != MOE_W_BF16;
-    static constexpr bool kF16 = FMT == MOE_W_NVFP4;
+    static constexpr bool kF16 = FMT != MOE_W_BF16;   // FP8 and NVFP4 tiles: f16 operands
     static constexpr int kMats = GU ? 2 : 1;
     static constexpr int kAMat = BM * BK * 2;
     static constexpr int kAStage = kMats * kAMat;
@@ -110,6 +112,11 @@ __device__ __forceinline__ Tile decode_tile(int tau, const TcParams& p, int n_ss
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
@@ -403,8 +410,8 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                             for (int i = 0; i < 4; ++i) {
                                 const float2 lo = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] & 0xffffu));
                                 const float2 hi = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] >> 16));
-                                o[2 * i] = pack_bf16(lo.x * s, lo.y * s);
-                                o[2 * i + 1] = pack_bf16(hi.x * s, hi.y * s);
+                                o[2 * i] = pack_f16(lo.x * s, lo.y * s);
+                                o[2 * i + 1] = pack_f16(hi.x * s, hi.y * s);
                             }
                             const uint32_t rowb = a_mat + r * 128;
                             st_shared_v4(rowb + (((2 * ch) ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
@@ -504,7 +511,7 @@ bool weight_map(CUtensorMap* m, int fmt, const void* w, int rows_total, int in_d
 }
 
 bool act_map(CUtensorMap* m, int fmt, const void* a, int rows, int cols) {
-    return make_map(m, a, fmt == MOE_W_NVFP4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+    return make_map(m, a, fmt != MOE_W_BF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                     2, cols, rows > 0 ? rows : 1, BK, 16, true);
 }
 
@@ -590,7 +597,7 @@ cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const
                           const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, int num_sms,
                           cudaStream_t st) {
     const int grid = 2 * num_sms;
-    if (fmt == MOE_W_NVFP4) gather_kernel<true><<<grid, 256, 0, st>>>(x, n, H, k, perm, offsets, E, xs, xh);
+    if (fmt != MOE_W_BF16) gather_kernel<true><<<grid, 256, 0, st>>>(x, n, H, k, perm, offsets, E, xs, xh);
     else gather_kernel<false><<<grid, 256, 0, st>>>(x, n, H, k, perm, offsets, E, xs, xh);
     return cudaGetLastError();
 }
