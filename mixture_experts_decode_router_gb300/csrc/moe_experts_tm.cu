@@ -121,80 +121,54 @@ gate_up_tm_kernel(const GateUpParams p) {
 }
 
 template <int FMT>
+__device__ __forceinline__ float row_dot_act(const QMatDev& M, int e, int h, const float* a, int K,
+                                             int lane) {
+    float acc = 0.f;
+    const int C = K >> 3;
+#pragma unroll 2
+    for (int c = lane; c < C; c += 32) {
+        WChunk<FMT> ch;
+        ch.load(M, e, h, c);
+        const float cs = ch.scale(M, e, h, c);
+        float wv[8], av[8];
+        ch.decode(wv);
+        const float4 a0 = __ldg(reinterpret_cast<const float4*>(a) + 2 * c);
+        const float4 a1 = __ldg(reinterpret_cast<const float4*>(a) + 2 * c + 1);
+        av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
+        av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
+        acc = fmaf(dot8(wv, av), cs, acc);
+    }
+    return acc;
+}
+
+template <int FMT>
 __global__ void __launch_bounds__(256, 2)
 down_blend_tm_kernel(const DownParams p) {
     const int lane = threadIdx.x & 31;
     const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
 
-    // Per lane, chunks c = lane + 32 i of each slot's down row (slot order), then
-    // of the shared row: the same order of operations as one row_dot_act per
-    // slot, but walked as one flat sequence whose loads are issued 8 at a time.
-    const int CI = p.I >> 3, CS = p.S >> 3;
-    const int cpl_i = lane < CI ? (CI - lane + 31) / 32 : 0;     // this lane's chunks per routed row
-    const int cpl_s = lane < CS ? (CS - lane + 31) / 32 : 0;     // ... per shared row
-    constexpr int B = 8;
     for (int h = gwarp; h < p.H; h += nwarps) {
         for (int t = 0; t < p.n; ++t) {
-            float gs = 1.0f;
+            float acc = 0.f;
+            for (int j = 0; j < p.k; ++j) {
+                const int r = t * p.k + j;
+                const int e = __ldg(p.idx + r);
+                if (e < 0 || e >= p.E) continue;   // dropped route (see the grouping)
+                const float wt = __ldg(p.w + r) * matrix_scale<FMT>(p.down, e);
+                acc = fmaf(row_dot_act<FMT>(p.down, e, h, p.act + (size_t)r * p.I, p.I, lane), wt, acc);
+            }
             if (p.S > 0) {
+                float gs = 1.0f;
                 if (p.sg_logit) gs = 1.0f / (1.0f + expf(-__ldg(p.sg_logit + t)));
                 gs *= matrix_scale<FMT>(p.sh_down, 0);
-            }
-            const int n_r = p.k * cpl_i;
-            const int total = n_r + (p.S > 0 ? cpl_s : 0);
-            float acc = 0.f, acc2 = 0.f;
-            for (int f0 = 0; f0 < total; f0 += B) {
-                WChunk<FMT> wch[B];
-                float4 a0[B], a1[B];
-                int ee[B];
-#pragma unroll
-                for (int b = 0; b < B; ++b) {
-                    const int f = f0 + b;
-                    ee[b] = -1;
-                    if (f < total) {
-                        const bool sh = f >= n_r;
-                        const int j = sh ? p.k : f / cpl_i;
-                        const int i = sh ? f - n_r : f - j * cpl_i;
-                        const int c = lane + 32 * i;
-                        const int e = sh ? 0 : __ldg(p.idx + t * p.k + j);
-                        if (sh || (e >= 0 && e < p.E)) {
-                            const QMatDev& M = sh ? p.sh_down : p.down;
-                            const float* a = sh ? p.act_sh + (size_t)t * p.S : p.act + (size_t)(t * p.k + j) * p.I;
-                            wch[b].load(M, e, h, c);
-                            a0[b] = __ldg(reinterpret_cast<const float4*>(a) + 2 * c);
-                            a1[b] = __ldg(reinterpret_cast<const float4*>(a) + 2 * c + 1);
-                            ee[b] = e;
-                        }
-                    }
-                }
-#pragma unroll
-                for (int b = 0; b < B; ++b) {
-                    const int f = f0 + b;
-                    if (f < total && ee[b] >= 0) {
-                        const bool sh = f >= n_r;
-                        const int j = sh ? p.k : f / cpl_i;
-                        const int i = sh ? f - n_r : f - j * cpl_i;
-                        const int c = lane + 32 * i;
-                        const QMatDev& M = sh ? p.sh_down : p.down;
-                        if (i == 0) acc2 = 0.f;
-                        float wv[8], av[8];
-                        wch[b].decode(wv);
-                        av[0] = a0[b].x; av[1] = a0[b].y; av[2] = a0[b].z; av[3] = a0[b].w;
-                        av[4] = a1[b].x; av[5] = a1[b].y; av[6] = a1[b].z; av[7] = a1[b].w;
-                        acc2 = fmaf(dot8(wv, av), wch[b].scale(M, ee[b], h, c), acc2);
-                        const int last = (sh ? cpl_s : cpl_i) - 1;
-                        if (i == last) {
-                            const float wt = sh ? gs : __ldg(p.w + t * p.k + j) * matrix_scale<FMT>(p.down, ee[b]);
-                            acc = fmaf(acc2, wt, acc);
-                        }
-                    }
-                }
+                acc = fmaf(row_dot_act<FMT>(p.sh_down, 0, h, p.act_sh + (size_t)t * p.S, p.S, lane), gs,
+                           acc);
             }
             const float s = warp_sum(acc);
             if (lane == 0) {
-                const __nv_bfloat16 bv = __float2bfloat16_rn(s);
-                p.out[(size_t)t * p.H + h] = *reinterpret_cast<const uint16_t*>(&bv);
+                const __nv_bfloat16 b = __float2bfloat16_rn(s);
+                p.out[(size_t)t * p.H + h] = *reinterpret_cast<const uint16_t*>(&b);
             }
         }
     }

@@ -12,9 +12,10 @@
 //           shared expert's gate/up rows and its slice of the shared down rows.
 //           Grid barrier 1: all logits are written.
 //  phase 1  every CTA ranks the logits itself (block-wide, by counting) and
-//           streams its share of the routed experts' gate/up rows through a
-//           ring of TMA bulk copies, while the same copy engine prefetches its
-//           slice of the routed down rows into shared memory.
+//           streams its share of the routed experts' gate/up rows straight
+//           into registers (15 warps, ~120 KB of loads in flight per SM),
+//           while the TMA bulk-copy engine prefetches its slice of the routed
+//           down rows into shared memory.
 //           Grid barrier 2: all SiLU(g)*u values are written.
 //  phase 2  every CTA computes its output columns from the down rows already
 //           in shared memory: down projection, routing-weighted sum and the
@@ -24,7 +25,7 @@
 // same, operation for operation, as the token-major kernels' for one token,
 // so a token's output bits do not depend on which path or batch computed it.
 //
-// Warp 15 (one lane) issues the copies; warps 0-14 compute.  Every wait is
+// Warp 15 (one lane) issues the bulk copies; warps 0-14 compute.  Every wait is
 // bounded (2 s), records an error code in the workspace and ends the kernel.
 #include <mutex>
 
@@ -38,7 +39,7 @@ namespace {
 constexpr int kFThreads = 512;
 constexpr int kFComputeWarps = 15;
 constexpr int kFCompute = kFComputeWarps * 32;
-constexpr int kRing = 8;
+constexpr int kSeg = 8;   // row chunks per lane loaded before they are used
 
 template <int FMT>
 __device__ __forceinline__ void decode_at(const uint8_t* row, int c, float (&v)[8]) {
@@ -90,27 +91,18 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
     float* ssc = reinterpret_cast<float*>(sm + p.off_sc);
     int* ssel = reinterpret_cast<int*>(sm + p.off_sel);
     float* sselw = reinterpret_cast<float*>(sm + p.off_sel + 128);
-    uint8_t* sring = sm + p.off_ring;
     uint8_t* sdown = sm + p.off_down;
     float* sact = reinterpret_cast<float*>(sm + p.off_act);
-    // Ring items are consumed by different warps, so a slot's phase parity
-    // cannot tell a warp whether its own item or an older one is in the slot:
-    // each item has its own single-use "full" barrier.  The slots' "empty"
-    // barriers have one in-order waiter (the producer) and stay per slot.
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.off_bar);
-    uint64_t* empty = bars;
-    uint64_t* dfull = bars + kRing;
-    uint64_t* dshfull = dfull + 1;
-    uint64_t* sel_ready = dshfull + 1;
-    volatile int* abort_f = reinterpret_cast<volatile int*>(sel_ready + 1);
+    uint64_t* dfull = bars;
+    uint64_t* dshfull = bars + 1;
+    uint64_t* sel_ready = bars + 2;
+    volatile int* abort_f = reinterpret_cast<volatile int*>(bars + 3);
     volatile int* s_go = abort_f + 1;   // phase decision, written by tid 0 before a barrier
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + p.off_bar + (kRing + 3) * 8 + 16);   // [max_items]
     Ctrl* ctrl = p.ctrl;
     int32_t* err = &ctrl->err;
 
     if (tid == 0) {
-        for (int s = 0; s < kRing; ++s) ptx::mbar_init(&empty[s], 1);
-        for (int s = 0; s < p.max_items; ++s) ptx::mbar_init(&full[s], 1);
         ptx::mbar_init(dfull, 1);
         ptx::mbar_init(dshfull, 1);
         ptx::mbar_init(sel_ready, 1);
@@ -122,6 +114,20 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
         if (!clean) atomicExch(err, 20);
         *abort_f = clean ? 0 : 2;
         ptx::fence_mbar_init();
+    }
+    // Router row of this warp (r == E: the shared-gate row): its first chunks
+    // are requested before x is staged, so the two loads overlap.
+    const int C = H >> 3;
+    const int r_row = cta + G * warp;
+    const bool has_row = warp < kFComputeWarps && r_row < E + (p.gw ? 1 : 0);
+    const uint16_t* wrow = has_row ? ((r_row < E) ? p.router + (size_t)r_row * H : p.gw) : nullptr;
+    uint4 rw[kSeg];
+    if (has_row) {
+#pragma unroll
+        for (int i = 0; i < kSeg; ++i) {
+            const int c = lane + 32 * i;
+            if (c < C) rw[i] = __ldg(reinterpret_cast<const uint4*>(wrow) + c);
+        }
     }
     for (int i = tid; i < H / 8; i += kFThreads)
         reinterpret_cast<uint4*>(sx)[i] = __ldg(reinterpret_cast<const uint4*>(p.x) + i);
@@ -135,28 +141,14 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
     const int64_t Q = (int64_t)k * I;
     const int r_b = (int)(Q * cta / G), r_e = (int)(Q * (cta + 1) / G);
     const int n_sh = sh_e - sh_b, n_r = r_e - r_b;
-    const uint32_t row_bytes = p.row_bytes;   // one gate/up row (H elements)
-    const uint32_t slot_bytes = 2 * row_bytes;
-    const int C = H >> 3;
 
     if (refused) {
         // nothing: the error word says why
     } else if (warp == kFComputeWarps) {
         // ------------------------------------------------------------ copy producer
         if (lane == 0) {
-            uint32_t seq = 0;
             bool ok = true;
-            auto issue_pair = [&](const QMatDev& Gm, const QMatDev& Um, int e, int row) -> bool {
-                const uint32_t slot = seq % kRing;
-                if (!ptx::mbar_wait(&empty[slot], ((seq / kRing) & 1) ^ 1, abort_f, err, 11)) return false;
-                ptx::mbar_arrive_expect_tx(&full[seq], slot_bytes);
-                ptx::bulk_load(sring + slot * slot_bytes, row_ptr<FMT>(Gm, e, row), row_bytes, &full[seq]);
-                ptx::bulk_load(sring + slot * slot_bytes + row_bytes, row_ptr<FMT>(Um, e, row), row_bytes,
-                               &full[seq]);
-                ++seq;
-                return true;
-            };
-            // Shared down slice, then the shared gate/up rows (routing-independent).
+            // Shared down slice (routing-independent), then the routed ones.
             if (S > 0 && nrows > 0) {
                 ptx::mbar_arrive_expect_tx(dshfull, nrows * p.dsh_row_bytes);
                 ptx::bulk_load(sdown + (size_t)k * rpc * p.drow_bytes, row_ptr<FMT>(p.sh_down, 0, h0),
@@ -164,52 +156,42 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
             } else {
                 ptx::mbar_arrive(dshfull);
             }
-            for (int i = sh_b; ok && i < sh_e; ++i) ok = issue_pair(p.sh_gate, p.sh_up, 0, i);
-            // Routed work, once this CTA has its routing.
-            if (ok) ok = ptx::mbar_wait(sel_ready, 0, abort_f, err, 12);
-            if (ok) {
-                if (nrows > 0) {
-                    ptx::mbar_arrive_expect_tx(dfull, (uint32_t)(k * nrows * p.drow_bytes));
-                    for (int j = 0; j < k; ++j)
-                        ptx::bulk_load(sdown + (size_t)j * rpc * p.drow_bytes, row_ptr<FMT>(p.down, ssel[j], h0),
-                                       nrows * p.drow_bytes, dfull);
-                } else {
-                    ptx::mbar_arrive(dfull);
-                }
-                for (int q = r_b; ok && q < r_e; ++q) {
-                    const int j = q / I, i = q - j * I;
-                    ok = issue_pair(p.gate, p.up, ssel[j], i);
-                }
-            }
-            if (!ok) {
-                // Let every copy issued land before the CTA exits.
-                const uint32_t nb = seq < (uint32_t)kRing ? seq : kRing;
-                for (uint32_t q = 0; q < nb; ++q) ptx::mbar_wait_quiet(&full[seq - 1 - q], 0, 100000000ull);
-                ptx::mbar_wait_quiet(dfull, 0, 100000000ull);
+            ok = ptx::mbar_wait(sel_ready, 0, abort_f, err, 12);
+            if (ok && nrows > 0) {
+                ptx::mbar_arrive_expect_tx(dfull, (uint32_t)(k * nrows * p.drow_bytes));
+                for (int j = 0; j < k; ++j)
+                    ptx::bulk_load(sdown + (size_t)j * rpc * p.drow_bytes, row_ptr<FMT>(p.down, ssel[j], h0),
+                                   nrows * p.drow_bytes, dfull);
+            } else if (ok) {
+                ptx::mbar_arrive(dfull);
+            } else {
+                // Let the copies issued land before the CTA exits.
                 ptx::mbar_wait_quiet(dshfull, 0, 100000000ull);
             }
         }
     } else {
         // ------------------------------------------------------------ compute warps
-        // Phase 0a: router rows r = cta + G * warp (r == E: the shared-gate row),
-        // with the router kernel's chunk order.
-        {
-            const int r = cta + G * warp;
-            if (r < E + (p.gw ? 1 : 0)) {
-                const uint16_t* wrow = (r < E) ? p.router + (size_t)r * H : p.gw;
-                float acc = 0.f;
-                for (int c = lane; c < C; c += 32) {
-                    float wv[8], xv[8];
-                    bf16x8_to_float(__ldg(reinterpret_cast<const uint4*>(wrow) + c), wv);
-                    bf16x8_to_float(reinterpret_cast<const uint4*>(sx)[c], xv);
+        // Phase 0a: the router row of this warp, with the router kernel's chunk order.
+        if (has_row) {
+            float acc = 0.f;
+            for (int c0 = 0; c0 < C; c0 += 32 * kSeg) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], xv[i], acc);
+                for (int i = 0; i < kSeg; ++i) {
+                    const int c = c0 + lane + 32 * i;
+                    if (c < C) {
+                        const uint4 raw = (c0 == 0) ? rw[i] : __ldg(reinterpret_cast<const uint4*>(wrow) + c);
+                        float wv[8], xv[8];
+                        bf16x8_to_float(raw, wv);
+                        bf16x8_to_float(reinterpret_cast<const uint4*>(sx)[c], xv);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) acc = fmaf(wv[q], xv[q], acc);
+                    }
                 }
-                const float s = warp_sum(acc);
-                if (lane == 0) {
-                    if (r < E) p.logits[r] = s;
-                    else *p.sg_logit = s;
-                }
+            }
+            const float s = warp_sum(acc);
+            if (lane == 0) {
+                if (r_row < E) p.logits[r_row] = s;
+                else *p.sg_logit = s;
             }
         }
         ptx::named_bar(1, kFCompute);
@@ -218,39 +200,46 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
             atomicAdd(&ctrl->gbar, 1u);
         }
 
-        // One gate/up ring item: SiLU(g) * u of weight row `row`, written to dst,
-        // with the token-major gate_up kernel's arithmetic.
-        auto consume = [&](uint32_t seq, const QMatDev& Gm, const QMatDev& Um, int e, int row, float msg,
-                           float msu, float* dst) -> bool {
-            const uint32_t slot = seq % kRing;
-            if (!ptx::mbar_wait_warp(&full[seq], 0, abort_f, err, 13)) return false;
-            const uint8_t* gr = sring + slot * slot_bytes;
-            const uint8_t* ur = gr + row_bytes;
+        // One gate/up row pair: SiLU(g) * u of weight row `row`, written to dst,
+        // with the token-major gate_up kernel's arithmetic.  Each segment's
+        // loads are all issued before any is used.
+        auto consume = [&](const QMatDev& Gm, const QMatDev& Um, int e, int row, float msg, float msu,
+                           float* dst) {
             float ag = 0.f, au = 0.f;
-            for (int c = lane; c < C; c += 32) {
-                float wg[8], wu[8], xv[8];
-                decode_at<FMT>(gr, c, wg);
-                decode_at<FMT>(ur, c, wu);
-                WChunk<FMT> sch;
-                const float sg = sch.scale(Gm, e, row, c), su = sch.scale(Um, e, row, c);
-                bf16x8_to_float(reinterpret_cast<const uint4*>(sx)[c], xv);
-                ag = fmaf(dot8(wg, xv), sg, ag);
-                au = fmaf(dot8(wu, xv), su, au);
+            for (int c0 = lane; c0 < C; c0 += 32 * kSeg) {
+                WChunk<FMT> cg[kSeg], cu[kSeg];
+#pragma unroll
+                for (int i = 0; i < kSeg; ++i) {
+                    const int c = c0 + 32 * i;
+                    if (c < C) {
+                        cg[i].load(Gm, e, row, c);
+                        cu[i].load(Um, e, row, c);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < kSeg; ++i) {
+                    const int c = c0 + 32 * i;
+                    if (c < C) {
+                        float wg[8], wu[8], xv[8];
+                        cg[i].decode(wg);
+                        cu[i].decode(wu);
+                        const float sg = cg[i].scale(Gm, e, row, c), su = cu[i].scale(Um, e, row, c);
+                        bf16x8_to_float(reinterpret_cast<const uint4*>(sx)[c], xv);
+                        ag = fmaf(dot8(wg, xv), sg, ag);
+                        au = fmaf(dot8(wu, xv), su, au);
+                    }
+                }
             }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&empty[slot]);
             const float g = warp_sum(ag) * msg;
             const float u = warp_sum(au) * msu;
             if (lane == 0) *dst = silu(g) * u;
-            return true;
         };
 
         // Phase 0b: the shared expert's gate/up rows of this CTA.
         const float msg_sh = S > 0 ? matrix_scale<FMT>(p.sh_gate, 0) : 1.f;
         const float msu_sh = S > 0 ? matrix_scale<FMT>(p.sh_up, 0) : 1.f;
-        bool ok = true;
-        for (int s = warp; ok && s < n_sh; s += kFComputeWarps)
-            ok = consume(s, p.sh_gate, p.sh_up, 0, sh_b + s, msg_sh, msu_sh, p.act_sh + sh_b + s);
+        for (int s = warp; s < n_sh; s += kFComputeWarps)
+            consume(p.sh_gate, p.sh_up, 0, sh_b + s, msg_sh, msu_sh, p.act_sh + sh_b + s);
 
         // Grid barrier 1: every logit is written.
         ptx::named_bar(1, kFCompute);
@@ -322,12 +311,14 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
             ptx::named_bar(1, kFCompute);
 
             // Phase 1b: the routed gate/up rows of this CTA.
-            for (int s = warp; ok && s < n_sh + n_r; s += kFComputeWarps) {
+            // Items continue the shared ones' warp rotation, so the CTA's warps
+            // stay evenly loaded.
+            for (int s = warp; s < n_sh + n_r; s += kFComputeWarps) {
                 if (s < n_sh) continue;
                 const int q = r_b + (s - n_sh);
                 const int j = q / I, i = q - j * I, e = ssel[j];
-                ok = consume(s, p.gate, p.up, e, i, matrix_scale<FMT>(p.gate, e), matrix_scale<FMT>(p.up, e),
-                             p.act + (size_t)j * I + i);
+                consume(p.gate, p.up, e, i, matrix_scale<FMT>(p.gate, e), matrix_scale<FMT>(p.up, e),
+                        p.act + (size_t)j * I + i);
             }
         }
 
@@ -421,12 +412,10 @@ bool fused_plan(const moe_config_t* c, int num_sms, FusedParams* p) {
     p->off_lg = take((size_t)E * 4, 16);
     p->off_sc = take((size_t)E * 4, 16);
     p->off_sel = take(256, 16);
-    p->off_ring = take((size_t)kRing * 2 * p->row_bytes, 128);
     p->off_down = take((size_t)(k + 1) * p->rpc * p->drow_bytes, 128);
     p->off_act = take(((size_t)k * I + (S > 0 ? S : 0)) * 4, 16);
-    // empty[kRing], dfull, dshfull, sel_ready, abort + phase flags, full[max_items]
-    p->max_items = (S + num_sms - 1) / num_sms + (int)(((int64_t)k * I + num_sms - 1) / num_sms) + 1;
-    p->off_bar = take((kRing + 3) * 8 + 16 + (size_t)p->max_items * 8, 8);
+    // dfull, dshfull, sel_ready, abort + phase flags
+    p->off_bar = take(3 * 8 + 16, 8);
     p->smem_bytes = (uint32_t)off;
     return off <= 227 * 1024 && k <= 32 && (size_t)k * p->rpc * p->drow_bytes < (1u << 20);
 }

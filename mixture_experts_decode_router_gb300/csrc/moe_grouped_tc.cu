@@ -378,27 +378,54 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
     } else if constexpr (C::kDeq) {
         // ------------------------------------------------------------ dequant
+        // Block scales come from global memory; each stage's are requested
+        // kPf stages ahead (the loop is unrolled by kPf so every prefetched
+        // value stays in its own register until it is used).
         const int dt = threadIdx.x - 6 * 32;        // 0 .. 255
-        const int dwarp = dt >> 5;
         uint32_t it = 0;
+        constexpr int kPf = 4;
+        struct Scales { float f[2]; uint32_t h[2][2]; };   // FP8: f[m]; NVFP4: f16x2 per 16-block
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
             const bool sh = t.e < 0;
             const int KB = (t.K + BK - 1) / BK;
-            bool ok = true;
-            for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int rs = it % C::kRawStages, as = it % C::kAStages;
-                if (!ptx::mbar_wait_warp(&raw_full[rs], (it / C::kRawStages) & 1, s_abort, err, 4)) { ok = false; break; }
-                if (!ptx::mbar_wait_warp(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 4)) { ok = false; break; }
+            const int eix = sh ? 0 : t.e;
+            // This thread's rows: FP8 chunks qd = dt + 256c (rows qd >> 2), NVFP4 row dt >> 1.
+            auto load_scales = [&](int kb) {
+                Scales sc{};
+                if (kb >= KB) return sc;
                 const int k0 = kb * BK;
+#pragma unroll
+                for (int m = 0; m < C::kMats; ++m) {
+                    if constexpr (FMT == MOE_W_FP8_B128) {
+                        const int ob = (t.out + 127) >> 7, ib = (t.K + 127) >> 7;
+                        const float* sp = reinterpret_cast<const float*>(sh ? p.sh_scale[m] : p.scale[m]);
+                        sc.f[m] = __ldg(sp + (size_t)eix * ob * ib + (t.m0 >> 7) * ib + (k0 >> 7));
+                    } else {
+                        const int r = dt >> 1, ch = dt & 1;
+                        const int kc = k0 + 32 * ch, mrow = t.m0 + r;
+                        sc.h[m][0] = sc.h[m][1] = 0u;
+                        if (mrow < t.out && kc < t.K) {
+                            const uint8_t* sp = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]) +
+                                                ((size_t)eix * t.out + mrow) * (t.K / 16) + kc / 16;
+                            sc.h[m][0] = __ldg(sp);
+                            sc.h[m][1] = __ldg(sp + 1);
+                        }
+                    }
+                }
+                return sc;
+            };
+            auto stage = [&](int kb, const Scales& sc) -> bool {
+                const int rs = it % C::kRawStages, as = it % C::kAStages;
+                if (!ptx::mbar_wait_warp(&raw_full[rs], (it / C::kRawStages) & 1, s_abort, err, 4)) return false;
+                if (!ptx::mbar_wait_warp(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 4)) return false;
+#pragma unroll
                 for (int m = 0; m < C::kMats; ++m) {
                     const uint8_t* raw = sRaw + rs * C::kRawStage + m * C::kRawMat;
                     const uint32_t a_mat = ptx::smem_u32(sA + as * C::kAStage + m * C::kAMat);
                     if constexpr (FMT == MOE_W_FP8_B128) {
                         // One fp32 scale per 128x128 block: uniform over this stage.
-                        const int ob = (t.out + 127) >> 7, ib = (t.K + 127) >> 7;
-                        const float* sc = reinterpret_cast<const float*>(sh ? p.sh_scale[m] : p.scale[m]);
-                        const float s = __ldg(sc + (size_t)(sh ? 0 : t.e) * ob * ib + (t.m0 >> 7) * ib + (k0 >> 7));
+                        const float s = sc.f[m];
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
                             const int qd = dt + 256 * c;           // 512 chunks of 16 codes
@@ -418,19 +445,13 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                             st_shared_v4(rowb + (((2 * ch + 1) ^ (r & 7)) << 4), o[4], o[5], o[6], o[7]);
                         }
                     } else {
-                        // NVFP4: 256 chunks of 32 codes (16 bytes), one per thread.
+                        // NVFP4: 256 chunks of 32 codes (16 bytes), one per thread; the
+                        // two E4M3 block scales as f16x2 (0 outside the matrix).
                         const int r = dt >> 1, ch = dt & 1;
                         const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 32 + ch * 16);
-                        const int kc = k0 + 32 * ch;
-                        const int mrow = t.m0 + r;
-                        uint32_t s0 = 0, s1 = 0;   // f16x2 of the two block scales (0 outside the matrix)
-                        if (mrow < t.out && kc < t.K) {
-                            const uint8_t* sc = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]) +
-                                                ((size_t)(sh ? 0 : t.e) * t.out + mrow) * (t.K / 16) + kc / 16;
-                            const uint32_t b0 = __ldg(sc), b1 = __ldg(sc + 1);
-                            s0 = e4m3x2_to_f16x2(b0 | (b0 << 8));
-                            s1 = e4m3x2_to_f16x2(b1 | (b1 << 8));
-                        }
+                        const uint32_t b0 = sc.h[m][0], b1 = sc.h[m][1];
+                        const uint32_t s0 = e4m3x2_to_f16x2(b0 | (b0 << 8));
+                        const uint32_t s1 = e4m3x2_to_f16x2(b1 | (b1 << 8));
                         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
                         uint32_t o[16];
 #pragma unroll
@@ -453,10 +474,20 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                     ptx::mbar_arrive(&raw_empty[rs]);
                     ptx::mbar_arrive(&a_full[as]);
                 }
+                ++it;
+                return true;
+            };
+            Scales pf0 = load_scales(0), pf1 = load_scales(1), pf2 = load_scales(2), pf3 = load_scales(3);
+            bool ok = true;
+            for (int kb = 0; ok && kb < KB; kb += kPf) {
+                ok = stage(kb, pf0);
+                pf0 = load_scales(kb + 4);
+                if (ok && kb + 1 < KB) { ok = stage(kb + 1, pf1); pf1 = load_scales(kb + 5); }
+                if (ok && kb + 2 < KB) { ok = stage(kb + 2, pf2); pf2 = load_scales(kb + 6); }
+                if (ok && kb + 3 < KB) { ok = stage(kb + 3, pf3); pf3 = load_scales(kb + 7); }
             }
             if (!ok) break;
         }
-        (void)dwarp;
     }
 
     ptx::tc_fence_before();

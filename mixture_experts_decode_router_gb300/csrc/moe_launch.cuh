@@ -88,9 +88,8 @@ struct FusedParams {
     uint16_t* out;            // [H]
     Ctrl* ctrl;
     int rpc;                  // output columns per CTA
-    int max_items;            // gate/up ring items a CTA can have (one barrier each)
     uint32_t row_bytes, drow_bytes, dsh_row_bytes;
-    uint32_t off_x, off_lg, off_sc, off_sel, off_ring, off_down, off_act, off_bar, smem_bytes;
+    uint32_t off_x, off_lg, off_sc, off_sel, off_down, off_act, off_bar, smem_bytes;
 };
 
 bool fused_plan(const moe_config_t* c, int num_sms, FusedParams* p);

@@ -11,7 +11,7 @@
 // hit L1/L2.
 //
 // Top-k: the "topk" step (moe_topk_softmax_batched / moe_topk_sigmoid_batched
-// on the same pages): one warp per token row.
+// on the same pages): one CTA per token row.
 #include "moe_launch.cuh"
 
 namespace moe {
@@ -68,121 +68,167 @@ router_kernel(const uint16_t* __restrict__ x, int n, int H,
     }
 }
 
-// One warp per token row; lane l holds experts l, l+32, ..., (VPL per lane).
-// Selection ranks the fp32 score (softmax: the logit; sigmoid: sigmoid(l) +
-// bias); equal scores go to the lower expert index; slots are written in
-// descending score.  Weights: softmax p = exp(l - max) / sum over all experts,
-// sigmoid p = sigmoid(l) (the bias only selects); renormalised over the k
-// selected when norm != 0; then multiplied by `scale`.
-template <int VPL>
+// Register-tiled router: each warp computes RE router rows x RT token rows.
+// For every (token, expert) pair the arithmetic is the one above -- lane l
+// chains fmaf over its chunks l, l+32, ... in order, then the same butterfly
+// -- so tiling changes nothing but how often each chunk is loaded.
+template <int RE, int RT>
 __global__ void __launch_bounds__(256)
-topk_kernel(const float* __restrict__ logits, int n, int E, int k, int routing,
-            const float* __restrict__ bias, int norm, float scale,
-            int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
+router_tiled_kernel(const uint16_t* __restrict__ x, int n, int H,
+                    const uint16_t* __restrict__ wr, int E,
+                    const uint16_t* __restrict__ gw,
+                    float* __restrict__ logits, float* __restrict__ sg_logit) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x >> 5) + warp;
-    if (t >= n) return;
-    const float* lrow = logits + (size_t)t * E;
-
-    float lg[VPL], sc[VPL];
-    uint32_t taken = 0;
+    const int rows = E + (gw ? 1 : 0);
+    const int r0 = (blockIdx.x * (blockDim.x >> 5) + warp) * RE;
+    if (r0 >= rows) return;
+    const int t0 = blockIdx.y * RT;
+    const int C = H >> 3;
+    const uint16_t* wrow[RE];
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) {
-            lg[i] = lrow[e];
-            if (routing == MOE_ROUTE_SOFTMAX) {
-                sc[i] = lg[i];
-            } else {
-                const float s = 1.0f / (1.0f + expf(-lg[i]));
-                sc[i] = s + bias[e];
+    for (int a = 0; a < RE; ++a) {
+        const int r = min(r0 + a, rows - 1);
+        wrow[a] = (r < E) ? wr + (size_t)r * H : gw;
+    }
+    float acc[RE][RT];
+#pragma unroll
+    for (int a = 0; a < RE; ++a)
+#pragma unroll
+        for (int b = 0; b < RT; ++b) acc[a][b] = 0.f;
+#pragma unroll 2
+    for (int c = lane; c < C; c += 32) {
+        uint4 wv4[RE], xv4[RT];
+#pragma unroll
+        for (int a = 0; a < RE; ++a) wv4[a] = __ldg(reinterpret_cast<const uint4*>(wrow[a]) + c);
+#pragma unroll
+        for (int b = 0; b < RT; ++b)
+            xv4[b] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)min(t0 + b, n - 1) * H) + c);
+#pragma unroll
+        for (int b = 0; b < RT; ++b) {
+            float xv[8];
+            bf16x8_to_float(xv4[b], xv);
+#pragma unroll
+            for (int a = 0; a < RE; ++a) {
+                float wv[8];
+                bf16x8_to_float(wv4[a], wv);
+                float s = acc[a][b];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) s = fmaf(wv[i], xv[i], s);
+                acc[a][b] = s;
             }
-            // A NaN score ranks last (as -inf), so every slot still names a
-            // valid expert and nothing downstream reads outside the weights.
-            if (sc[i] != sc[i]) sc[i] = -INFINITY;
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < RE; ++a)
+#pragma unroll
+        for (int b = 0; b < RT; ++b) {
+            const float v = warp_sum(acc[a][b]);
+            const int r = r0 + a, t = t0 + b;
+            if (lane == 0 && r < rows && t < n) {
+                if (r < E) logits[(size_t)t * E + r] = v;
+                else sg_logit[t] = v;
+            }
+        }
+}
+
+// One CTA per token row.  Selection ranks the fp32 score (softmax: the logit;
+// sigmoid: sigmoid(l) + bias, the bias only selects); every thread ranks its
+// experts against all E scores (rank = experts ahead in score-descending,
+// index-ascending order; selected iff rank < k), which needs no serial shuffle
+// chain, and slot j holds the expert of rank j.  Warp 0 forms the weights:
+// softmax p = exp(l - max) / sum over all experts (lane l summing experts
+// l, l+32, ... in order, then a butterfly), sigmoid p = sigmoid(l);
+// renormalised over the k selected when norm != 0; multiplied by `scale`.
+// The single-token kernel repeats this arithmetic exactly.
+__global__ void __launch_bounds__(256)
+topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int routing,
+                  const float* __restrict__ bias, int norm, float scale,
+                  int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
+    extern __shared__ float smf[];
+    float* slg = smf;          // [E]
+    float* ssc = smf + E;      // [E]
+    __shared__ int ssel[kMaxTopK];
+    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+    const float* lrow = logits + (size_t)t * E;
+    for (int e = tid; e < E; e += blockDim.x) {
+        const float l = lrow[e];
+        float sc;
+        if (routing == MOE_ROUTE_SOFTMAX) sc = l;
+        else sc = 1.0f / (1.0f + expf(-l)) + bias[e];
+        if (sc != sc) sc = -INFINITY;
+        slg[e] = l;
+        ssc[e] = sc;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        const float v = ssc[e];
+        int rank = 0;
+        for (int f = 0; f < E; ++f) {
+            const float u = ssc[f];
+            rank += (u > v || (u == v && f < e)) ? 1 : 0;
+        }
+        if (rank < k) ssel[rank] = e;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        const int sel_e = lane < k ? ssel[lane] : -1;
+        const float sel_l = lane < k ? slg[sel_e] : 0.f;
+        float p;
+        if (routing == MOE_ROUTE_SOFTMAX) {
+            const float mx = __shfl_sync(0xffffffffu, sel_l, 0);
+            float z = 0.f;
+            for (int i = 0; lane + 32 * i < E; ++i) z += expf(slg[lane + 32 * i] - mx);
+            z = warp_sum(z);
+            p = (lane < k) ? expf(sel_l - mx) / z : 0.f;
         } else {
-            lg[i] = -INFINITY;
-            sc[i] = -INFINITY;
-            taken |= 1u << i;   // never selectable
+            p = (lane < k) ? 1.0f / (1.0f + expf(-sel_l)) : 0.f;
         }
-    }
-
-    int sel_e = -1;          // lane j keeps slot j
-    float sel_l = 0.f;
-    for (int j = 0; j < k; ++j) {
-        // Local best: strictly greater wins, so the lowest index keeps a tie.
-        float bv = -INFINITY; int be = 0x7fffffff; float bl = 0.f;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const bool free_i = !((taken >> i) & 1u);
-            const int e = lane + 32 * i;
-            if (free_i && (sc[i] > bv || (sc[i] == bv && e < be))) { bv = sc[i]; be = e; bl = lg[i]; }
+        if (norm) {
+            const float tot = warp_sum(p);
+            p = p / tot;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
-            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; bl = ol; }
+        if (lane < k) {
+            idx_out[(size_t)t * k + lane] = sel_e;
+            w_out[(size_t)t * k + lane] = p * scale;
         }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        if (lane == j) { sel_e = be; sel_l = bl; }
-    }
-
-    float p = 0.f;
-    if (routing == MOE_ROUTE_SOFTMAX) {
-        // max logit = the first selected score.
-        const float mx = __shfl_sync(0xffffffffu, sel_l, 0);
-        float z = 0.f;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i)
-            if (lane + 32 * i < E) z += expf(lg[i] - mx);
-        z = warp_sum(z);
-        p = (lane < k) ? expf(sel_l - mx) / z : 0.f;
-    } else {
-        p = (lane < k) ? 1.0f / (1.0f + expf(-sel_l)) : 0.f;
-    }
-    if (norm) {
-        const float tot = warp_sum(p);
-        p = p / tot;
-    }
-    if (lane < k) {
-        idx_out[(size_t)t * k + lane] = sel_e;
-        w_out[(size_t)t * k + lane] = p * scale;
     }
 }
 
 cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, int E,
                           const uint16_t* gw, float* logits, float* sg_logit, int num_sms,
                           cudaStream_t st) {
-    const int warps = 4;
     const int rows = E + (gw ? 1 : 0);
-    dim3 grid((rows + warps - 1) / warps, 1);
-    int gy = (2 * num_sms + (int)grid.x - 1) / (int)grid.x;
-    gy = max(1, min(gy, (n + 3) / 4));
-    int rpb = (n + gy - 1) / gy;
-    rpb = (rpb + 3) / 4 * 4;
-    gy = (n + rpb - 1) / rpb;
-    grid.y = gy;
-    router_kernel<<<grid, warps * 32, 0, st>>>(x, n, H, wr, E, gw, logits, sg_logit, rpb);
-    return cudaGetLastError();
+    if (n <= 2) {
+        // Few tokens: one router row per warp, all tokens in the warp's loop.
+        const int warps = 4;
+        dim3 grid((rows + warps - 1) / warps, 1);
+        router_kernel<<<grid, warps * 32, 0, st>>>(x, n, H, wr, E, gw, logits, sg_logit, 4);
+        return cudaGetLastError();
+    }
+    // RT tokens x RE router rows per warp, 8 warps per CTA; RE as large as keeps
+    // at least one CTA per SM.
+    const int rt = n >= 8 ? 8 : 4;
+    const int gy = (n + rt - 1) / rt;
+    int re = 4;
+    while (re > 1 && (long)((rows + 8 * re - 1) / (8 * re)) * gy < num_sms) re >>= 1;
+    dim3 grid((rows + 8 * re - 1) / (8 * re), gy);
+#define MOE_ROUTER_CASE(RE_, RT_)                                                                    \
+    if (re == RE_ && rt == RT_) {                                                                    \
+        router_tiled_kernel<RE_, RT_><<<grid, 256, 0, st>>>(x, n, H, wr, E, gw, logits, sg_logit);   \
+        return cudaGetLastError();                                                                   \
+    }
+    MOE_ROUTER_CASE(4, 8) MOE_ROUTER_CASE(2, 8) MOE_ROUTER_CASE(1, 8)
+    MOE_ROUTER_CASE(4, 4) MOE_ROUTER_CASE(2, 4) MOE_ROUTER_CASE(1, 4)
+#undef MOE_ROUTER_CASE
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_topk(const float* logits, int n, int E, int k, int routing, const float* bias,
                         int norm, float scale, int32_t* idx, float* w, cudaStream_t st) {
-    const int warps = 8;
-    dim3 grid((n + warps - 1) / warps);
-    const int vpl = (E + 31) / 32;
-#define MOE_TOPK_CASE(V)                                                                   \
-    if (vpl <= V) {                                                                        \
-        topk_kernel<V><<<grid, warps * 32, 0, st>>>(logits, n, E, k, routing, bias, norm,  \
-                                                    scale, idx, w);                        \
-        return cudaGetLastError();                                                         \
-    }
-    MOE_TOPK_CASE(1) MOE_TOPK_CASE(2) MOE_TOPK_CASE(4) MOE_TOPK_CASE(8) MOE_TOPK_CASE(16)
-    MOE_TOPK_CASE(32)
-#undef MOE_TOPK_CASE
-    return cudaErrorInvalidValue;
+    // 2 E floats of shared memory (<= 8 KB for E <= 1024).
+    topk_block_kernel<<<n, 256, 2 * E * sizeof(float), st>>>(logits, n, E, k, routing, bias, norm, scale, idx,
+                                                             w);
+    return cudaGetLastError();
 }
 
 }  // namespace moe
