@@ -46,6 +46,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="decode_n1")
     p.add_argument("--path", default="auto", choices=["auto", "token_major", "grouped"])
+    p.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--oracle-budget", type=float, default=15.0,
                    help="seconds of oracle work for the CPU baseline sample")
@@ -282,6 +283,8 @@ def run_ours(args):
     B.load()
 
     cfg = synth.WORKLOADS[args.workload]
+    if args.tokens > 0:
+        cfg = cfg.with_(n_tokens=args.tokens, name=f"{cfg.name}@n{args.tokens}")
     n = cfg.n_tokens
     lw = synth.make_weights(cfg, dev)
     x = synth.make_input(cfg, device=dev)

@@ -97,8 +97,10 @@ typedef enum {
 
 typedef enum { MOE_ROUTE_SOFTMAX = 0, MOE_ROUTE_SIGMOID_BIAS = 1 } moe_routing_t;
 typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_B128 = 1, MOE_W_NVFP4 = 2 } moe_wfmt_t;
-/* Expert-stage algorithm.  AUTO: token-major for N <= 16, expert-grouped
- * tensor-core GEMM above.  The two explicit values force one (tests). */
+/* Expert-stage algorithm.  AUTO: one token runs the single-token kernel,
+ * 2-3 tokens the token-major kernels, 4 or more the expert-grouped
+ * tensor-core GEMM.  The two explicit values force one (tests); TOKEN_MAJOR
+ * with one token still runs the single-token kernel (same arithmetic). */
 typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_TOKEN_MAJOR = 1, MOE_PATH_GROUPED = 2 } moe_path_t;
 
 /* Layer configuration (the config fields hidden_size, num_experts,
@@ -214,8 +216,10 @@ moe_status_t moe_forward_static_ws(const moe_config_t* cfg, const moe_weights_t*
                                    const void* x, int32_t n, void* out,
                                    int32_t* idx, float* w, moe_stream_t stream);
 
-/* Reads, then clears, the device error word of a workspace.  Synchronises
- * `stream` (the only entry point that does).
+/* Reads, then clears, the device error word of a workspace, and resets the
+ * single-token kernel's barrier word (which a call that ended early leaves
+ * non-zero), so the workspace serves the next call.  Synchronises `stream`
+ * (the only entry point that does).
  *   device_error (out)  0: no failure since the last check; 11-16: a bounded
  *                       wait of the single-token kernel gave up; 1-4: a bounded
  *                       wait of the grouped tensor-core kernels gave up; 20: the

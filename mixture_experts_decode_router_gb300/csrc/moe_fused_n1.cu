@@ -106,11 +106,10 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
         ptx::mbar_init(dfull, 1);
         ptx::mbar_init(dshfull, 1);
         ptx::mbar_init(sel_ready, 1);
-        // The control block must be clean at the start of a call (zeroed once,
-        // kept zero by every call); anything else is a workspace that was not
-        // initialised: refuse before touching it.
-        const bool clean = ptx::ld_acquire_gpu(&ctrl->gexit) == 0 &&
-                           ptx::ld_acquire_gpu(&ctrl->gbar) < (uint32_t)G;
+        // The barrier word must be below G at the start of a call (zeroed once,
+        // returned to zero by every call); anything else is a workspace that
+        // was not initialised (or a call that failed): refuse before touching it.
+        const bool clean = ptx::ld_acquire_gpu(&ctrl->gbar) < (uint32_t)G;
         if (!clean) atomicExch(err, 20);
         *abort_f = clean ? 0 : 2;
         ptx::fence_mbar_init();
@@ -195,10 +194,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
             }
         }
         ptx::named_bar(1, kFCompute);
-        if (tid == 0) {
-            __threadfence();
-            atomicAdd(&ctrl->gbar, 1u);
-        }
+        if (tid == 0) ptx::red_add_release_gpu(&ctrl->gbar, 1u);   // barrier 1 arrival
 
         // One gate/up row pair: SiLU(g) * u of weight row `row`, written to dst,
         // with the token-major gate_up kernel's arithmetic.  Each segment's
@@ -326,15 +322,23 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
         ptx::named_bar(1, kFCompute);
         if (tid == 0) {
             if (!*abort_f) {
-                __threadfence();
-                atomicAdd(&ctrl->gbar, 1u);
-                const uint64_t t0 = ptx::globaltimer();
-                while (ptx::ld_acquire_gpu(&ctrl->gbar) < 2u * G) {
-                    if (*abort_f) break;
-                    if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
-                        atomicExch(err, 15);
-                        *abort_f = 1;
-                        break;
+                // The last CTA to arrive returns the word to zero for the next
+                // call; the others stop waiting at 2G or at that zero (the word
+                // cannot be zero again before this call ends).
+                const uint32_t old = ptx::atom_add_acq_rel_gpu(&ctrl->gbar, 1u);
+                if (old == 2u * G - 1) {
+                    ptx::st_relaxed_gpu(&ctrl->gbar, 0u);
+                } else {
+                    const uint64_t t0 = ptx::globaltimer();
+                    for (;;) {
+                        const uint32_t v = ptx::ld_acquire_gpu(&ctrl->gbar);
+                        if (v >= 2u * G || v == 0) break;
+                        if (*abort_f) break;
+                        if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+                            atomicExch(err, 15);
+                            *abort_f = 1;
+                            break;
+                        }
                     }
                 }
             }
@@ -380,16 +384,6 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
     }
 
     __syncthreads();
-    if (tid == 0 && !refused) {
-        // The last CTA out returns the control block to zero for the next call.
-        __threadfence();
-        const uint32_t prev = atomicAdd(&ctrl->gexit, 1u);
-        if (prev == (uint32_t)G - 1) {
-            atomicExch(&ctrl->gbar, 0u);
-            atomicExch(&ctrl->gexit, 0u);
-            __threadfence();
-        }
-    }
 }
 
 }  // namespace

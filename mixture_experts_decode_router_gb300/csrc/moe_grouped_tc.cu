@@ -56,6 +56,9 @@ struct TcCfg {
     static constexpr int kRawMat = BM * kRawRow;
     static constexpr int kRawStage = kMats * kRawMat;
     static constexpr int kAStages = kDeq ? (GU ? 3 : 4) : (GU ? 4 : 6);
+    // Dequantised tiles: the token (B) tiles have a ring of their own, so they
+    // are fetched ahead instead of after the MMA frees an A slot.
+    static constexpr int kBStages = kDeq ? (GU ? 4 : 6) : kAStages;
     static constexpr int kRawStages = !kDeq ? 0 : ((FMT == MOE_W_FP8_B128 && GU) ? 4 : 8);
     static constexpr int kAccCols = kMats * NT;
     static constexpr int kTmemCols = 2 * kAccCols;
@@ -63,11 +66,11 @@ struct TcCfg {
     static constexpr int kThreads = (6 + kDeqWarps) * 32;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kAStages * kAStage;
-    static constexpr int kOffRaw = kOffB + kAStages * kBStage;
+    static constexpr int kOffRaw = kOffB + kBStages * kBStage;
     static constexpr int kOffBar = kOffRaw + kRawStages * kRawStage;
-    // a_full, a_empty, b_full per A stage; raw_full, raw_empty per raw stage;
-    // acc_full[2], acc_empty[2], drain.
-    static constexpr int kNumBars = 3 * kAStages + 2 * kRawStages + 5;
+    // a_full, a_empty per A stage; b_full, b_empty per B stage; raw_full,
+    // raw_empty per raw stage; acc_full[2], acc_empty[2], drain.
+    static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kRawStages + 5;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;   // + alignment slack
     static_assert(kSmem <= 232448, "shared memory budget");
@@ -165,7 +168,8 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     uint64_t* a_full = bars;
     uint64_t* a_empty = bars + C::kAStages;
     uint64_t* b_full = bars + 2 * C::kAStages;
-    uint64_t* raw_full = bars + 3 * C::kAStages;
+    uint64_t* b_empty = b_full + C::kBStages;
+    uint64_t* raw_full = b_empty + C::kBStages;
     uint64_t* raw_empty = raw_full + C::kRawStages;
     uint64_t* acc_full = raw_empty + C::kRawStages;
     uint64_t* acc_empty = acc_full + 2;
@@ -179,7 +183,10 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         for (int s = 0; s < C::kAStages; ++s) {
             ptx::mbar_init(&a_full[s], C::kDeq ? C::kDeqWarps : 1);
             ptx::mbar_init(&a_empty[s], 1);
+        }
+        for (int s = 0; s < C::kBStages; ++s) {
             ptx::mbar_init(&b_full[s], 1);
+            ptx::mbar_init(&b_empty[s], 1);
         }
         for (int s = 0; s < C::kRawStages; ++s) {
             ptx::mbar_init(&raw_full[s], 1);
@@ -227,10 +234,10 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                             ptx::tma_load_2d(sRaw + rs * C::kRawStage + m * C::kRawMat,
                                              sh ? &maps.ws[m] : &maps.w[m], xr, wrow, &raw_full[rs]);
                     }
-                    const int as = it % C::kAStages;
-                    if (!ptx::mbar_wait(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 1))
-                        break;
                     if constexpr (!C::kDeq) {
+                        const int as = it % C::kAStages;
+                        if (!ptx::mbar_wait(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 1))
+                            break;
                         ptx::mbar_arrive_expect_tx(&a_full[as], C::kAStage + nbox * 2048);
                         for (int m = 0; m < C::kMats; ++m)
                             ptx::tma_load_2d(sA + as * C::kAStage + m * C::kAMat,
@@ -239,21 +246,24 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                             ptx::tma_load_2d(sB + as * C::kBStage + j * 2048, bmap, k0, t.pos0 + 16 * j,
                                              &a_full[as]);
                     } else {
-                        ptx::mbar_arrive_expect_tx(&b_full[as], nbox * 2048);
+                        const int bs = it % C::kBStages;
+                        if (!ptx::mbar_wait(&b_empty[bs], ((it / C::kBStages) & 1) ^ 1, s_abort, err, 1))
+                            break;
+                        ptx::mbar_arrive_expect_tx(&b_full[bs], nbox * 2048);
                         for (int j = 0; j < nbox; ++j)
-                            ptx::tma_load_2d(sB + as * C::kBStage + j * 2048, bmap, k0, t.pos0 + 16 * j,
-                                             &b_full[as]);
+                            ptx::tma_load_2d(sB + bs * C::kBStage + j * 2048, bmap, k0, t.pos0 + 16 * j,
+                                             &b_full[bs]);
                     }
                 }
             }
             if (*s_abort) {
                 // Let every copy this thread issued land before the CTA exits:
                 // wait (bounded) on the last phase of each ring stage it used.
-                const uint32_t na = it < (uint32_t)C::kAStages ? it : C::kAStages;
+                constexpr uint32_t kRing = C::kDeq ? C::kBStages : C::kAStages;
+                const uint32_t na = it < kRing ? it : kRing;
                 for (uint32_t q = 0; q < na; ++q) {
-                    const uint32_t i2 = it - 1 - q, s2 = i2 % C::kAStages;
-                    ptx::mbar_wait_quiet(C::kDeq ? &b_full[s2] : &a_full[s2], (i2 / C::kAStages) & 1,
-                                         100000000ull);
+                    const uint32_t i2 = it - 1 - q, s2 = i2 % kRing;
+                    ptx::mbar_wait_quiet(C::kDeq ? &b_full[s2] : &a_full[s2], (i2 / kRing) & 1, 100000000ull);
                 }
                 if constexpr (C::kDeq) {
                     const uint32_t nr = it < (uint32_t)C::kRawStages ? it : C::kRawStages;
@@ -280,13 +290,16 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                 bool ok = true;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int as = it % C::kAStages;
-                    const uint32_t ph = (it / C::kAStages) & 1;
-                    if (!ptx::mbar_wait(&a_full[as], ph, s_abort, err, 2)) { ok = false; break; }
+                    const int bs = C::kDeq ? (int)(it % C::kBStages) : as;
+                    if (!ptx::mbar_wait(&a_full[as], (it / C::kAStages) & 1, s_abort, err, 2)) { ok = false; break; }
                     if constexpr (C::kDeq)
-                        if (!ptx::mbar_wait(&b_full[as], ph, s_abort, err, 2)) { ok = false; break; }
+                        if (!ptx::mbar_wait(&b_full[bs], (it / C::kBStages) & 1, s_abort, err, 2)) {
+                            ok = false;
+                            break;
+                        }
                     ptx::tc_fence_after();
                     const uint32_t a_base = ptx::smem_u32(sA + as * C::kAStage);
-                    const uint32_t b_base = ptx::smem_u32(sB + as * C::kBStage);
+                    const uint32_t b_base = ptx::smem_u32(sB + bs * C::kBStage);
 #pragma unroll
                     for (int m = 0; m < C::kMats; ++m)
 #pragma unroll
@@ -295,6 +308,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                                          ptx::sw128_desc(b_base + kk * 32), idesc,
                                          (kb > 0 || kk > 0) ? 1u : 0u);
                     ptx::mma_commit(&a_empty[as]);
+                    if constexpr (C::kDeq) ptx::mma_commit(&b_empty[bs]);
                 }
                 if (!ok) break;
                 ptx::mma_commit(&acc_full[ab]);
@@ -378,54 +392,27 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
     } else if constexpr (C::kDeq) {
         // ------------------------------------------------------------ dequant
-        // Block scales come from global memory; each stage's are requested
-        // kPf stages ahead (the loop is unrolled by kPf so every prefetched
-        // value stays in its own register until it is used).
         const int dt = threadIdx.x - 6 * 32;        // 0 .. 255
+        const int dwarp = dt >> 5;
         uint32_t it = 0;
-        constexpr int kPf = 4;
-        struct Scales { float f[2]; uint32_t h[2][2]; };   // FP8: f[m]; NVFP4: f16x2 per 16-block
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
             const bool sh = t.e < 0;
             const int KB = (t.K + BK - 1) / BK;
-            const int eix = sh ? 0 : t.e;
-            // This thread's rows: FP8 chunks qd = dt + 256c (rows qd >> 2), NVFP4 row dt >> 1.
-            auto load_scales = [&](int kb) {
-                Scales sc{};
-                if (kb >= KB) return sc;
-                const int k0 = kb * BK;
-#pragma unroll
-                for (int m = 0; m < C::kMats; ++m) {
-                    if constexpr (FMT == MOE_W_FP8_B128) {
-                        const int ob = (t.out + 127) >> 7, ib = (t.K + 127) >> 7;
-                        const float* sp = reinterpret_cast<const float*>(sh ? p.sh_scale[m] : p.scale[m]);
-                        sc.f[m] = __ldg(sp + (size_t)eix * ob * ib + (t.m0 >> 7) * ib + (k0 >> 7));
-                    } else {
-                        const int r = dt >> 1, ch = dt & 1;
-                        const int kc = k0 + 32 * ch, mrow = t.m0 + r;
-                        sc.h[m][0] = sc.h[m][1] = 0u;
-                        if (mrow < t.out && kc < t.K) {
-                            const uint8_t* sp = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]) +
-                                                ((size_t)eix * t.out + mrow) * (t.K / 16) + kc / 16;
-                            sc.h[m][0] = __ldg(sp);
-                            sc.h[m][1] = __ldg(sp + 1);
-                        }
-                    }
-                }
-                return sc;
-            };
-            auto stage = [&](int kb, const Scales& sc) -> bool {
+            bool ok = true;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int rs = it % C::kRawStages, as = it % C::kAStages;
-                if (!ptx::mbar_wait_warp(&raw_full[rs], (it / C::kRawStages) & 1, s_abort, err, 4)) return false;
-                if (!ptx::mbar_wait_warp(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 4)) return false;
-#pragma unroll
+                if (!ptx::mbar_wait_warp(&raw_full[rs], (it / C::kRawStages) & 1, s_abort, err, 4)) { ok = false; break; }
+                if (!ptx::mbar_wait_warp(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 4)) { ok = false; break; }
+                const int k0 = kb * BK;
                 for (int m = 0; m < C::kMats; ++m) {
                     const uint8_t* raw = sRaw + rs * C::kRawStage + m * C::kRawMat;
                     const uint32_t a_mat = ptx::smem_u32(sA + as * C::kAStage + m * C::kAMat);
                     if constexpr (FMT == MOE_W_FP8_B128) {
                         // One fp32 scale per 128x128 block: uniform over this stage.
-                        const float s = sc.f[m];
+                        const int ob = (t.out + 127) >> 7, ib = (t.K + 127) >> 7;
+                        const float* sc = reinterpret_cast<const float*>(sh ? p.sh_scale[m] : p.scale[m]);
+                        const float s = __ldg(sc + (size_t)(sh ? 0 : t.e) * ob * ib + (t.m0 >> 7) * ib + (k0 >> 7));
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
                             const int qd = dt + 256 * c;           // 512 chunks of 16 codes
@@ -445,13 +432,19 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                             st_shared_v4(rowb + (((2 * ch + 1) ^ (r & 7)) << 4), o[4], o[5], o[6], o[7]);
                         }
                     } else {
-                        // NVFP4: 256 chunks of 32 codes (16 bytes), one per thread; the
-                        // two E4M3 block scales as f16x2 (0 outside the matrix).
+                        // NVFP4: 256 chunks of 32 codes (16 bytes), one per thread.
                         const int r = dt >> 1, ch = dt & 1;
                         const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 32 + ch * 16);
-                        const uint32_t b0 = sc.h[m][0], b1 = sc.h[m][1];
-                        const uint32_t s0 = e4m3x2_to_f16x2(b0 | (b0 << 8));
-                        const uint32_t s1 = e4m3x2_to_f16x2(b1 | (b1 << 8));
+                        const int kc = k0 + 32 * ch;
+                        const int mrow = t.m0 + r;
+                        uint32_t s0 = 0, s1 = 0;   // f16x2 of the two block scales (0 outside the matrix)
+                        if (mrow < t.out && kc < t.K) {
+                            const uint8_t* sc = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]) +
+                                                ((size_t)(sh ? 0 : t.e) * t.out + mrow) * (t.K / 16) + kc / 16;
+                            const uint32_t b0 = __ldg(sc), b1 = __ldg(sc + 1);
+                            s0 = e4m3x2_to_f16x2(b0 | (b0 << 8));
+                            s1 = e4m3x2_to_f16x2(b1 | (b1 << 8));
+                        }
                         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
                         uint32_t o[16];
 #pragma unroll
@@ -474,20 +467,10 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                     ptx::mbar_arrive(&raw_empty[rs]);
                     ptx::mbar_arrive(&a_full[as]);
                 }
-                ++it;
-                return true;
-            };
-            Scales pf0 = load_scales(0), pf1 = load_scales(1), pf2 = load_scales(2), pf3 = load_scales(3);
-            bool ok = true;
-            for (int kb = 0; ok && kb < KB; kb += kPf) {
-                ok = stage(kb, pf0);
-                pf0 = load_scales(kb + 4);
-                if (ok && kb + 1 < KB) { ok = stage(kb + 1, pf1); pf1 = load_scales(kb + 5); }
-                if (ok && kb + 2 < KB) { ok = stage(kb + 2, pf2); pf2 = load_scales(kb + 6); }
-                if (ok && kb + 3 < KB) { ok = stage(kb + 3, pf3); pf3 = load_scales(kb + 7); }
             }
             if (!ok) break;
         }
+        (void)dwarp;
     }
 
     ptx::tc_fence_before();

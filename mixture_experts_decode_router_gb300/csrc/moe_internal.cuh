@@ -22,9 +22,8 @@ struct Ctrl {
     int32_t n_active;      // experts with at least one route (written by the group kernel)
     int32_t n_rsegs;       // routed token segments of <= kTcTokensPerTile (group kernel)
     int32_t err;           // sticky device error code (bounded waits that gave up); 0 = none
-    uint32_t gbar;         // grid-barrier arrivals of the fused kernel (0 between calls)
-    uint32_t gexit;        // CTAs that finished the fused kernel (0 between calls)
-    int32_t pad[59];
+    uint32_t gbar;         // grid-barrier arrivals of the single-token kernel (0 between calls)
+    int32_t pad[60];
 };
 
 // Tokens per tile of the grouped tensor-core path (its MMA N is at most this).

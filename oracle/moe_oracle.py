@@ -180,6 +180,9 @@ class OracleLayer:
     sh_down: Optional[QMat] = None             # [1, H, S]
     correction_bias: Optional[np.ndarray] = None   # float32 [E]
     shared_gate_w: Optional[np.ndarray] = None     # uint16 BF16 [H]
+    pre_expert_norm_w: Optional[np.ndarray] = None  # uint16 BF16 [H] (RMSNorm weight) or None
+    rms_norm_eps: float = 1e-6
+    router_q: Optional["QMat"] = None              # NVFP4 router [1, E, H]; replaces router_w
     _cache: Dict = field(default_factory=dict, repr=False)
 
 
@@ -187,15 +190,32 @@ class OracleLayer:
 # Routing: router, selection, weights
 # --------------------------------------------------------------------------
 
-def router_logits(x: np.ndarray, router_w_bits: np.ndarray) -> np.ndarray:
+def router_logits(x: np.ndarray, router_w_bits) -> np.ndarray:
     """Router logits [N, E] = x [N, H] . Wr[E, H]^T, all in float64 (the
-    ``gate`` step: ``decode_gate_gemv`` for one row, ``dense_gemm`` for N)."""
-    wr = bf16_decode(router_w_bits)
+    ``gate`` step: ``decode_gate_gemv`` for one row, ``dense_gemm`` for N).
+    ``router_w_bits``: BF16 bits [E, H], or an already decoded float matrix."""
+    wr = router_w_bits if np.asarray(router_w_bits).dtype == np.float64 else bf16_decode(router_w_bits)
     x = np.atleast_2d(np.asarray(x, dtype=np.float64))
     # One matrix-vector product per row, so a row's logits never depend on
     # which other rows are in the call (a batched BLAS product may block them).
     return np.stack([wr @ x[t] for t in range(x.shape[0])]) if x.shape[0] else \
         np.zeros((0, wr.shape[0]))
+
+
+def rms_norm(x: np.ndarray, w_bits: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm of each row of x: x / sqrt(mean(x^2) + eps) * w (the
+    ``pre_expert_norm`` step of MoeLayer::forward: the expert input only)."""
+    x = np.atleast_2d(np.asarray(x, dtype=np.float64))
+    w = bf16_decode(w_bits)
+    ms = np.array([float(x[t] @ x[t]) / x.shape[1] for t in range(x.shape[0])])
+    return x / np.sqrt(ms + eps)[:, None] * w
+
+
+def router_weights(layer) -> np.ndarray:
+    """The router matrix [E, H] in float64: BF16, or NVFP4 (``gate_nvfp4``)."""
+    if layer.router_q is not None:
+        return layer.router_q.expert(0)
+    return bf16_decode(layer.router_w)
 
 
 def sigmoid(v):
@@ -285,31 +305,45 @@ def swiglu_mlp(x: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.ndarray) ->
     return wd @ (silu(g) * u)
 
 
-def moe_forward(layer: OracleLayer, x_bits: np.ndarray, rows=None):
+def moe_forward(layer: OracleLayer, x_bits: np.ndarray, rows=None, experts=None,
+                include_shared: bool = True):
     """The whole layer for the tokens ``rows`` (default: all) of the BF16 input
     ``x_bits`` (uint16 [N, H]).  Returns (out float64 [R, H], indices int64
     [R, k], weights float64 [R, k], logits float64 [R, E]) for those rows.
 
     Each row is computed on its own, so the result for a row cannot depend on
     which other rows share the call.  Experts are decoded one at a time and
-    every routed (token, slot) pair of that expert is evaluated with it."""
+    every routed (token, slot) pair of that expert is evaluated with it.
+
+    Expert parallelism (the EP branch of MoeLayer::forward and
+    forward_token_major_decode): ``experts`` = (begin, end) keeps only the
+    routes to experts in [begin, end) -- one rank's partial output, routing
+    still computed over all experts -- and ``include_shared=False`` leaves the
+    shared expert out (it is added once, after the partials are summed).
+
+    With a pre-expert RMSNorm weight, the experts (routed and shared) take
+    ``rms_norm(x)``; the router and the shared-expert gate take ``x``."""
     x_all = bf16_decode(x_bits)
     rows = np.arange(x_all.shape[0]) if rows is None else np.asarray(rows)
     x = x_all[rows]
-    logits = router_logits(x, layer.router_w)
+    logits = router_logits(x, router_weights(layer))
     idx, w = route(logits, layer.routing, layer.top_k, layer.norm_topk_prob,
                    layer.routed_scaling_factor, layer.correction_bias)
+    xe = x if layer.pre_expert_norm_w is None else rms_norm(x, layer.pre_expert_norm_w,
+                                                            layer.rms_norm_eps)
     n, h = x.shape
     out = np.zeros((n, h), dtype=np.float64)
     # Routed experts: one expert decoded at a time.
     for e in np.unique(idx):
+        if experts is not None and not (experts[0] <= e < experts[1]):
+            continue
         wg, wu, wd = layer.gate.expert(e), layer.up.expert(e), layer.down.expert(e)
         tok, slot = np.nonzero(idx == e)
-        d = swiglu_mlp(x[tok], wg, wu, wd)
+        d = swiglu_mlp(xe[tok], wg, wu, wd)
         out[tok] += w[tok, slot][:, None] * d
     # Always-on shared expert.
-    if layer.shared_inter > 0 and layer.sh_gate is not None:
-        ds = swiglu_mlp(x, layer.sh_gate.expert(0), layer.sh_up.expert(0),
+    if include_shared and layer.shared_inter > 0 and layer.sh_gate is not None:
+        ds = swiglu_mlp(xe, layer.sh_gate.expert(0), layer.sh_up.expert(0),
                         layer.sh_down.expert(0))
         if layer.shared_gate_w is not None:
             gw = bf16_decode(layer.shared_gate_w)
@@ -326,20 +360,22 @@ def moe_forward_slotwise(layer: OracleLayer, x_bits: np.ndarray):
     tokens by expert.  Small inputs only; used to pin ``moe_forward``'s
     expert-major evaluation order."""
     x = bf16_decode(x_bits)
-    logits = router_logits(x, layer.router_w)
+    logits = router_logits(x, router_weights(layer))
     idx, w = route(logits, layer.routing, layer.top_k, layer.norm_topk_prob,
                    layer.routed_scaling_factor, layer.correction_bias)
+    xe = x if layer.pre_expert_norm_w is None else rms_norm(x, layer.pre_expert_norm_w,
+                                                            layer.rms_norm_eps)
     n, h = x.shape
     out = np.zeros((n, h))
     for t in range(n):
         acc = np.zeros(h)
         for j in range(layer.top_k):
             e = idx[t, j]
-            d = swiglu_mlp(x[t], layer.gate.expert(e), layer.up.expert(e),
+            d = swiglu_mlp(xe[t], layer.gate.expert(e), layer.up.expert(e),
                            layer.down.expert(e))
             acc = acc + w[t, j] * d
         if layer.shared_inter > 0 and layer.sh_gate is not None:
-            ds = swiglu_mlp(x[t], layer.sh_gate.expert(0), layer.sh_up.expert(0),
+            ds = swiglu_mlp(xe[t], layer.sh_gate.expert(0), layer.sh_up.expert(0),
                             layer.sh_down.expert(0))
             gs = 1.0 if layer.shared_gate_w is None else float(
                 sigmoid(x[t] @ bf16_decode(layer.shared_gate_w)))

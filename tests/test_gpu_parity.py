@@ -89,7 +89,7 @@ SMALL_CASES = [
 
 
 @pytest.mark.parametrize("cfg", SMALL_CASES, ids=lambda c: c.name)
-@pytest.mark.parametrize("n", [1, 3, 16, 17, 40])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 16, 17, 40])
 def test_small_layers(cfg, n):
     _check(cfg, n)
 
@@ -148,13 +148,14 @@ def test_zero_tokens_is_a_noop():
 
 @pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_FP8_B128, synth.FMT_NVFP4])
 def test_rows_do_not_depend_on_the_batch_token_major(fmt):
-    """N <= 16 (one token: the fused kernel, which keeps the token-major arithmetic)."""
+    """The token-major kernels (forced), and one token alone: the single-token
+    kernel, which keeps the token-major arithmetic."""
     cfg = small("invariance", expert_fmt=fmt, num_experts=32, top_k=4,
                 routing=synth.ROUTE_SIGMOID_BIAS, routed_scaling_factor=2.5)
     lw = synth.make_weights(cfg, "cuda")
     L = oracle_layer(lw)
     x = synth.make_input(cfg, 12, "cuda", gap_fn=gap_fn_for(L))
-    layer = MoeLayer(lw, 64)
+    layer = MoeLayer(lw, 64, path="token_major")
     full, _, _ = layer.forward(x)
     perm = torch.randperm(12, generator=torch.Generator().manual_seed(3)).cuda()
     permuted, _, _ = layer.forward(x[perm])
@@ -168,7 +169,7 @@ def test_rows_do_not_depend_on_the_batch_token_major(fmt):
 
 @pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_FP8_B128, synth.FMT_NVFP4])
 def test_rows_do_not_depend_on_the_batch_grouped(fmt):
-    """N > 16: the expert-grouped tensor-core path."""
+    """N >= 4: the expert-grouped tensor-core path."""
     cfg = small("invariance_g", expert_fmt=fmt, num_experts=32, top_k=4,
                 routing=synth.ROUTE_SIGMOID_BIAS, routed_scaling_factor=2.5)
     lw = synth.make_weights(cfg, "cuda")

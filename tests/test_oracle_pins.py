@@ -267,7 +267,7 @@ def _python_loop_forward(L, xb):
     """The layer for one token in plain Python loops over scalars."""
     x = [float(v) for v in O.bf16_decode(xb)]
     H, E, k = L.hidden, L.num_experts, L.top_k
-    wr = O.bf16_decode(L.router_w)
+    wr = L.router_q.expert(0) if L.router_q is not None else O.bf16_decode(L.router_w)
     logit = [sum(x[h] * float(wr[e, h]) for h in range(H)) for e in range(E)]
     if L.routing == O.ROUTE_SOFTMAX:
         m = max(logit)
@@ -284,10 +284,16 @@ def _python_loop_forward(L, xb):
         wsel = [v / tot for v in wsel]
     wsel = [v * L.routed_scaling_factor for v in wsel]
 
+    xe = x
+    if L.pre_expert_norm_w is not None:
+        nw = O.bf16_decode(L.pre_expert_norm_w)
+        inv = 1.0 / math.sqrt(sum(v * v for v in x) / H + L.rms_norm_eps)
+        xe = [x[h] * inv * float(nw[h]) for h in range(H)]
+
     def mlp(wg, wu, wd):
         inner = wg.shape[0]
-        g = [sum(float(wg[i, h]) * x[h] for h in range(H)) for i in range(inner)]
-        u = [sum(float(wu[i, h]) * x[h] for h in range(H)) for i in range(inner)]
+        g = [sum(float(wg[i, h]) * xe[h] for h in range(H)) for i in range(inner)]
+        u = [sum(float(wu[i, h]) * xe[h] for h in range(H)) for i in range(inner)]
         a = [g[i] / (1 + math.exp(-g[i])) * u[i] for i in range(inner)]
         return [sum(float(wd[o, i]) * a[i] for i in range(inner)) for o in range(H)]
 
@@ -390,3 +396,73 @@ def test_rows_do_not_depend_on_grouping():
     dup = np.concatenate([xb, xb[:4]])
     d_out, _, _, _ = O.moe_forward(L, dup)
     assert np.array_equal(d_out[12:], full[:4])
+
+
+# ------------------------------------------------------------------ next rows
+
+def test_rms_norm_closed_form_and_scale_invariance():
+    x = np.array([[3.0, 4.0]])
+    w = _bf16_bits(np.array([1.0, 2.0]))
+    y = O.rms_norm(x, w, 0.0)
+    r = math.sqrt(12.5)
+    assert abs(y[0, 0] - 3.0 / r) < 1e-15 and abs(y[0, 1] - 8.0 / r) < 1e-15
+    rng = np.random.default_rng(21)
+    xs = rng.normal(size=(4, 64))
+    ws = _bf16_bits(rng.normal(size=64))
+    assert np.array_equal(O.rms_norm(2.0 * xs, ws, 0.0), O.rms_norm(xs, ws, 0.0))
+    # eps moves the result toward zero by the closed-form factor
+    y1 = O.rms_norm(x, w, 3.5)
+    assert abs(y1[0, 0] - 3.0 / 4.0) < 1e-15
+
+
+@pytest.mark.parametrize("fmt", [O.FMT_BF16, O.FMT_NVFP4])
+def test_pre_expert_norm_matches_python_loops(fmt):
+    rng = np.random.default_rng(22)
+    L = _tiny_layer(rng, fmt, E=5, H=32, I=32, S=32, k=2, routing=O.ROUTE_SIGMOID_BIAS,
+                    scale=2.5, shared_gate=True)
+    L.pre_expert_norm_w = _bf16_bits(rng.uniform(0.5, 1.5, size=32))
+    L.rms_norm_eps = 1e-5
+    xb = _bf16_bits(rng.normal(size=(3, 32)) * 3.0)
+    out, idx, w, _ = O.moe_forward(L, xb)
+    for t in range(3):
+        ref, order, wsel = _python_loop_forward(L, xb[t])
+        assert idx[t].tolist() == order
+        assert np.allclose(out[t], ref, rtol=1e-11, atol=1e-12)
+
+
+def test_nvfp4_router_matches_python_loops():
+    rng = np.random.default_rng(23)
+    L = _tiny_layer(rng, O.FMT_BF16, E=6, H=64, I=32, S=32, k=2)
+    p = rng.integers(0, 256, size=(1, 6, 32), dtype=np.uint8)
+    s16 = rng.integers(0x30, 0x40, size=(1, 6, 4), dtype=np.uint8)
+    L.router_q = O.QMat(O.FMT_NVFP4, p, s16, np.array([0.05], np.float32))
+    xb = _bf16_bits(rng.normal(size=(3, 64)))
+    out, idx, w, lg = O.moe_forward(L, xb)
+    wr = O.dequant_nvfp4(p[0], s16[0], float(np.float32(0.05)))
+    assert np.allclose(lg, O.bf16_decode(xb) @ wr.T, rtol=1e-13, atol=1e-14)
+    for t in range(3):
+        ref, order, _ = _python_loop_forward(L, xb[t])
+        assert idx[t].tolist() == order
+        assert np.allclose(out[t], ref, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("ranks", [2, 3, 5])
+def test_expert_parallel_partials_sum_to_the_layer(ranks):
+    """Each rank keeps its experts' routes, the shared expert is left out of
+    every partial and added once after the sum (the EP branch)."""
+    rng = np.random.default_rng(24)
+    L = _tiny_layer(rng, O.FMT_FP8_B128, E=10, H=128, I=64, S=64, k=3,
+                    routing=O.ROUTE_SIGMOID_BIAS, scale=2.5, shared_gate=True)
+    xb = _bf16_bits(rng.normal(size=(7, 128)))
+    full, idx, w, _ = O.moe_forward(L, xb)
+    bounds = np.linspace(0, 10, ranks + 1).astype(int)
+    parts = [O.moe_forward(L, xb, experts=(bounds[r], bounds[r + 1]), include_shared=False)[0]
+             for r in range(ranks)]
+    shared_only = O.moe_forward(L, xb, experts=(0, 0), include_shared=True)[0]
+    assert np.allclose(sum(parts) + shared_only, full, rtol=1e-12, atol=1e-13)
+    # A rank whose experts no token chose contributes exactly zero.
+    unused = sorted(set(range(10)) - set(idx.ravel().tolist()))
+    if unused:
+        e = unused[0]
+        z = O.moe_forward(L, xb, experts=(e, e + 1), include_shared=False)[0]
+        assert not z.any()
