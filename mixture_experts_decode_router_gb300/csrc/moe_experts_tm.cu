@@ -31,6 +31,7 @@ gate_up_tm_kernel(const GateUpParams p) {
     const int lane = threadIdx.x & 31;
     const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    pdl_wait();
     const int n_active = p.ctrl->n_active;
     const int64_t routed_rows = (int64_t)n_active * p.I;
     const int64_t R = routed_rows + (p.S > 0 ? p.S : 0);
@@ -118,6 +119,7 @@ gate_up_tm_kernel(const GateUpParams p) {
             }
         }
     }
+    pdl_trigger();
 }
 
 template <int FMT>
@@ -144,6 +146,7 @@ __device__ __forceinline__ float row_dot_act(const QMatDev& M, int e, int h, con
 template <int FMT>
 __global__ void __launch_bounds__(256, 2)
 down_blend_tm_kernel(const DownParams p) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -172,6 +175,7 @@ down_blend_tm_kernel(const DownParams p) {
             }
         }
     }
+    pdl_trigger();
 }
 
 template <int FMT>
@@ -181,10 +185,10 @@ static cudaError_t launch_gate_up_fmt(const GateUpParams& gu, int num_sms, cudaS
     // (BF16) or 4 (FP8 / NVFP4, whose dequantisation needs more registers).
     constexpr int kMaxTB = (FMT == MOE_W_BF16) ? 8 : 4;
     const int tb = gu.n >= kMaxTB ? kMaxTB : (gu.n >= 4 ? 4 : (gu.n >= 2 ? 2 : 1));
-    if (tb == 1) gate_up_tm_kernel<FMT, 1><<<grid, block, 0, st>>>(gu);
-    else if (tb == 2) gate_up_tm_kernel<FMT, 2><<<grid, block, 0, st>>>(gu);
-    else if (tb == 4) gate_up_tm_kernel<FMT, 4><<<grid, block, 0, st>>>(gu);
-    else gate_up_tm_kernel<FMT, kMaxTB><<<grid, block, 0, st>>>(gu);
+    if (tb == 1) launch_pdl(gate_up_tm_kernel<FMT, 1>, grid, block, 0, st, gu);
+    else if (tb == 2) launch_pdl(gate_up_tm_kernel<FMT, 2>, grid, block, 0, st, gu);
+    else if (tb == 4) launch_pdl(gate_up_tm_kernel<FMT, 4>, grid, block, 0, st, gu);
+    else launch_pdl(gate_up_tm_kernel<FMT, kMaxTB>, grid, block, 0, st, gu);
     return cudaGetLastError();
 }
 
@@ -200,9 +204,9 @@ cudaError_t launch_gate_up_tm(int fmt, const GateUpParams& gu, int num_sms, cuda
 cudaError_t launch_down_blend_tm(int fmt, const DownParams& dn, int num_sms, cudaStream_t st) {
     const dim3 grid(2 * num_sms), block(256);
     switch (fmt) {
-        case MOE_W_BF16: down_blend_tm_kernel<MOE_W_BF16><<<grid, block, 0, st>>>(dn); break;
-        case MOE_W_FP8_B128: down_blend_tm_kernel<MOE_W_FP8_B128><<<grid, block, 0, st>>>(dn); break;
-        case MOE_W_NVFP4: down_blend_tm_kernel<MOE_W_NVFP4><<<grid, block, 0, st>>>(dn); break;
+        case MOE_W_BF16: launch_pdl(down_blend_tm_kernel<MOE_W_BF16>, grid, block, 0, st, dn); break;
+        case MOE_W_FP8_B128: launch_pdl(down_blend_tm_kernel<MOE_W_FP8_B128>, grid, block, 0, st, dn); break;
+        case MOE_W_NVFP4: launch_pdl(down_blend_tm_kernel<MOE_W_NVFP4>, grid, block, 0, st, dn); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -33,6 +33,7 @@ group_kernel(const int32_t* __restrict__ idx, int nk, int E,
     int32_t* tot = sm + kSegWarps * E;           // [E]
     __shared__ int32_t warp_sums[3][32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();
 
     for (int i = tid; i < kSegWarps * E; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
@@ -136,6 +137,7 @@ group_kernel(const int32_t* __restrict__ idx, int nk, int E,
             __syncwarp();
         }
     }
+    pdl_trigger();
 }
 
 cudaError_t launch_group(const int32_t* idx, int nk, int E, int32_t* counts, int32_t* offsets,
@@ -143,7 +145,7 @@ cudaError_t launch_group(const int32_t* idx, int nk, int E, int32_t* counts, int
                          cudaStream_t st) {
     const size_t smem = sizeof(int32_t) * (size_t)(kSegWarps + 1) * E;
     // (kSegWarps + 1) * E ints <= 36 KB for E <= 1024: under the 48 KB default.
-    group_kernel<<<1, kGroupThreads, smem, st>>>(idx, nk, E, counts, offsets, perm, inv, active, segs,
+    launch_pdl(group_kernel, 1, kGroupThreads, smem, st, idx, nk, E, counts, offsets, perm, inv, active, segs,
                                                   ctrl);
     return cudaGetLastError();
 }

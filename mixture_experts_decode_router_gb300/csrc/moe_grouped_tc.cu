@@ -205,6 +205,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    pdl_wait();
 
     const int n_rsegs = p.ctrl->n_rsegs;
     const int n_ssegs = (p.sh_out > 0) ? (p.n + NT - 1) / NT : 0;
@@ -473,6 +474,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         (void)dwarp;
     }
 
+    pdl_trigger();
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -545,7 +547,7 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int num_sms, cudaSt
             configured[dev] = true;
         }
     }
-    kern<<<num_sms, C::kThreads, C::kSmem, st>>>(maps, p);
+    launch_pdl(kern, num_sms, C::kThreads, C::kSmem, st, maps, p);
     return cudaGetLastError();
 }
 
@@ -556,6 +558,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
                                                      const int32_t* __restrict__ perm,
                                                      const int32_t* __restrict__ offsets, int E,
                                                      uint16_t* __restrict__ xs, uint16_t* __restrict__ xh) {
+    pdl_wait();
     const int n_routes = offsets[E];
     const int rows = n_routes + (F16 ? n : 0);
     const int C8 = H >> 3;
@@ -579,12 +582,14 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
         uint16_t* dst = routed ? xs + (size_t)r * H : xh + (size_t)(r - n_routes) * H;
         reinterpret_cast<uint4*>(dst)[c] = v;
     }
+    pdl_trigger();
 }
 
 // out[t, h] = bf16( sum_j y[inv[t*k + j], h] (slot order) + y_sh[t, h] ).
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ ysh,
                                                       const int32_t* __restrict__ inv, int n, int H, int k,
                                                       int has_shared, uint16_t* __restrict__ out) {
+    pdl_wait();
     const int C4 = H >> 2;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)n * C4;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -603,6 +608,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         const uint32_t lo = pack_bf16(acc.x, acc.y), hi = pack_bf16(acc.z, acc.w);
         reinterpret_cast<uint2*>(out + (size_t)t * H)[c] = make_uint2(lo, hi);
     }
+    pdl_trigger();
 }
 
 }  // namespace
@@ -611,14 +617,14 @@ cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const
                           const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, int num_sms,
                           cudaStream_t st) {
     const int grid = 2 * num_sms;
-    if (fmt != MOE_W_BF16) gather_kernel<true><<<grid, 256, 0, st>>>(x, n, H, k, perm, offsets, E, xs, xh);
-    else gather_kernel<false><<<grid, 256, 0, st>>>(x, n, H, k, perm, offsets, E, xs, xh);
+    if (fmt != MOE_W_BF16) launch_pdl(gather_kernel<true>, grid, 256, 0, st, x, n, H, k, perm, offsets, E, xs, xh);
+    else launch_pdl(gather_kernel<false>, grid, 256, 0, st, x, n, H, k, perm, offsets, E, xs, xh);
     return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const float* y, const float* ysh, const int32_t* inv, int n, int H, int k,
                            int has_shared, uint16_t* out, int num_sms, cudaStream_t st) {
-    combine_kernel<<<2 * num_sms, 256, 0, st>>>(y, ysh, inv, n, H, k, has_shared, out);
+    launch_pdl(combine_kernel, 2 * num_sms, 256, 0, st, y, ysh, inv, n, H, k, has_shared, out);
     return cudaGetLastError();
 }
 

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -81,6 +83,34 @@ struct QMatDev {
     const float* scale2;    // NVFP4 per-expert
     int out_dim, in_dim;
 };
+
+// ----------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of a multi-kernel sequence is
+// launched with programmatic stream serialisation, so its launch and prologue
+// overlap the tail of the kernel before it.  Each kernel calls pdl_wait()
+// before its first global-memory access (it returns once every earlier kernel
+// on the stream has completed and its writes are visible), and pdl_trigger()
+// once its own main work is done -- never earlier, so all CTAs of a grid have
+// started before a dependent grid may take SM resources.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ----------------------------------------------------------------------------
 // Small device helpers.

@@ -32,6 +32,7 @@ router_kernel(const uint16_t* __restrict__ x, int n, int H,
     const int r = blockIdx.x * (blockDim.x >> 5) + warp;
     const int n_rows_router = E + (gw ? 1 : 0);
     if (r >= n_rows_router) return;
+    pdl_wait();
     const uint16_t* wrow = (r < E) ? wr + (size_t)r * H : gw;
     const int t_begin = blockIdx.y * rows_per_block;
     const int t_end = min(n, t_begin + rows_per_block);
@@ -66,6 +67,7 @@ router_kernel(const uint16_t* __restrict__ x, int n, int H,
             }
         }
     }
+    pdl_trigger();
 }
 
 // Register-tiled router: each warp computes RE router rows x RT token rows.
@@ -82,6 +84,7 @@ router_tiled_kernel(const uint16_t* __restrict__ x, int n, int H,
     const int rows = E + (gw ? 1 : 0);
     const int r0 = (blockIdx.x * (blockDim.x >> 5) + warp) * RE;
     if (r0 >= rows) return;
+    pdl_wait();
     const int t0 = blockIdx.y * RT;
     const int C = H >> 3;
     const uint16_t* wrow[RE];
@@ -129,6 +132,7 @@ router_tiled_kernel(const uint16_t* __restrict__ x, int n, int H,
                 else sg_logit[t] = v;
             }
         }
+    pdl_trigger();
 }
 
 // One CTA per token row.  Selection ranks the fp32 score (softmax: the logit;
@@ -150,6 +154,7 @@ topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int rou
     __shared__ int ssel[kMaxTopK];
     const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
     const float* lrow = logits + (size_t)t * E;
+    pdl_wait();
     for (int e = tid; e < E; e += blockDim.x) {
         const float l = lrow[e];
         float sc;
@@ -192,6 +197,7 @@ topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int rou
             w_out[(size_t)t * k + lane] = p * scale;
         }
     }
+    pdl_trigger();
 }
 
 cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, int E,
@@ -202,7 +208,7 @@ cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, i
         // Few tokens: one router row per warp, all tokens in the warp's loop.
         const int warps = 4;
         dim3 grid((rows + warps - 1) / warps, 1);
-        router_kernel<<<grid, warps * 32, 0, st>>>(x, n, H, wr, E, gw, logits, sg_logit, 4);
+        launch_pdl(router_kernel, grid, warps * 32, 0, st, x, n, H, wr, E, gw, logits, sg_logit, 4);
         return cudaGetLastError();
     }
     // RT tokens x RE router rows per warp, 8 warps per CTA; RE as large as keeps
@@ -214,7 +220,7 @@ cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, i
     dim3 grid((rows + 8 * re - 1) / (8 * re), gy);
 #define MOE_ROUTER_CASE(RE_, RT_)                                                                    \
     if (re == RE_ && rt == RT_) {                                                                    \
-        router_tiled_kernel<RE_, RT_><<<grid, 256, 0, st>>>(x, n, H, wr, E, gw, logits, sg_logit);   \
+        launch_pdl(router_tiled_kernel<RE_, RT_>, grid, 256, 0, st, x, n, H, wr, E, gw, logits, sg_logit);   \
         return cudaGetLastError();                                                                   \
     }
     MOE_ROUTER_CASE(4, 8) MOE_ROUTER_CASE(2, 8) MOE_ROUTER_CASE(1, 8)
@@ -226,7 +232,7 @@ cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, i
 cudaError_t launch_topk(const float* logits, int n, int E, int k, int routing, const float* bias,
                         int norm, float scale, int32_t* idx, float* w, cudaStream_t st) {
     // 2 E floats of shared memory (<= 8 KB for E <= 1024).
-    topk_block_kernel<<<n, 256, 2 * E * sizeof(float), st>>>(logits, n, E, k, routing, bias, norm, scale, idx,
+    launch_pdl(topk_block_kernel, n, 256, 2 * E * sizeof(float), st, logits, n, E, k, routing, bias, norm, scale, idx,
                                                              w);
     return cudaGetLastError();
 }
