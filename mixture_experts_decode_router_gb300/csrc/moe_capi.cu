@@ -173,6 +173,7 @@ static moe_status_t enqueue_grouped(const moe_config_t* c, const moe_weights_t* 
     p.segs = at<int32_t>(ws, L.segs);
     p.ctrl = at<Ctrl>(ws, L.ctrl);
     p.err = &at<Ctrl>(ws, L.ctrl)->err;
+    p.zero4 = &at<Ctrl>(ws, L.ctrl)->pad[0];   // never written: zero
     p.perm = at<int32_t>(ws, L.perm);
     p.route_w = wt;
     p.sg_logit = w->shared_gate_w ? sg_logit : nullptr;

@@ -59,7 +59,7 @@ struct TcCfg {
     // Dequantised tiles: the token (B) tiles have a ring of their own, so they
     // are fetched ahead instead of after the MMA frees an A slot.
     static constexpr int kBStages = kDeq ? (GU ? 4 : 6) : kAStages;
-    static constexpr int kRawStages = !kDeq ? 0 : ((FMT == MOE_W_FP8_B128 && GU) ? 4 : 8);
+    static constexpr int kRawStages = !kDeq ? 0 : (GU ? (FMT == MOE_W_FP8_B128 ? 4 : 6) : 8);
     static constexpr int kAccCols = kMats * NT;
     static constexpr int kTmemCols = 2 * kAccCols;
     static constexpr int kDeqWarps = kDeq ? 8 : 0;
@@ -67,7 +67,11 @@ struct TcCfg {
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kAStages * kAStage;
     static constexpr int kOffRaw = kOffB + kBStages * kBStage;
-    static constexpr int kOffBar = kOffRaw + kRawStages * kRawStage;
+    // Block scales of each raw stage, fetched by the producer warp with the
+    // raw codes: FP8 one fp32 per matrix; NVFP4 4 E4M3 bytes per row per matrix.
+    static constexpr int kScaleStage = FMT == MOE_W_FP8_B128 ? 16 : (FMT == MOE_W_NVFP4 ? kMats * BM * 4 : 0);
+    static constexpr int kOffScale = kOffRaw + kRawStages * kRawStage;
+    static constexpr int kOffBar = kOffScale + kRawStages * kScaleStage;
     // a_full, a_empty per A stage; b_full, b_empty per B stage; raw_full,
     // raw_empty per raw stage; acc_full[2], acc_empty[2], drain.
     static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kRawStages + 5;
@@ -164,6 +168,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     uint8_t* sA = smem + C::kOffA;
     uint8_t* sB = smem + C::kOffB;
     uint8_t* sRaw = smem + C::kOffRaw;
+    uint8_t* sScale = smem + C::kOffScale;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint64_t* a_full = bars;
     uint64_t* a_empty = bars + C::kAStages;
@@ -189,7 +194,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             ptx::mbar_init(&b_empty[s], 1);
         }
         for (int s = 0; s < C::kRawStages; ++s) {
-            ptx::mbar_init(&raw_full[s], 1);
+            ptx::mbar_init(&raw_full[s], 1 + 32);   // TMA expect_tx + the producer warp's scale copies
             ptx::mbar_init(&raw_empty[s], C::kDeqWarps);
         }
         for (int b = 0; b < 2; ++b) {
@@ -214,31 +219,75 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            uint32_t it = 0;
-            for (int tau = blockIdx.x; tau < n_tiles && !*s_abort; tau += gridDim.x) {
-                const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
-                const bool sh = t.e < 0;
-                const int wrow = sh ? t.m0 : t.e * t.out + t.m0;
-                const int nbox = (t.ntok + 15) >> 4;
-                const CUtensorMap* bmap = sh ? &maps.bs : &maps.b;
-                const int KB = (t.K + BK - 1) / BK;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int k0 = kb * BK;
-                    if constexpr (C::kDeq) {
-                        const int rs = it % C::kRawStages;
-                        if (!ptx::mbar_wait(&raw_empty[rs], ((it / C::kRawStages) & 1) ^ 1, s_abort, err, 1))
-                            break;
+        // The whole warp runs the loop: lane 0 issues the TMA copies; for FP8 /
+        // NVFP4 every lane also copies its share of the stage's block scales
+        // into shared memory (cp.async), completing on the raw stage's barrier.
+        uint32_t it = 0;
+        bool stop = false;
+        for (int tau = blockIdx.x; tau < n_tiles && !stop && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
+            const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
+            const bool sh = t.e < 0;
+            const int wrow = sh ? t.m0 : t.e * t.out + t.m0;
+            const int nbox = (t.ntok + 15) >> 4;
+            const CUtensorMap* bmap = sh ? &maps.bs : &maps.b;
+            const int KB = (t.K + BK - 1) / BK;
+            const bool nv_smem_scales = (FMT == MOE_W_NVFP4) && (t.K % 64 == 0);
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int k0 = kb * BK;
+                if constexpr (C::kDeq) {
+                    const int rs = it % C::kRawStages;
+                    if (!ptx::mbar_wait_warp(&raw_empty[rs], ((it / C::kRawStages) & 1) ^ 1, s_abort, err, 1)) {
+                        stop = true;
+                        break;
+                    }
+                    if (lane == 0) {
                         ptx::mbar_arrive_expect_tx(&raw_full[rs], C::kRawStage);
                         const int xr = (FMT == MOE_W_FP8_B128) ? k0 : k0 / 2;
                         for (int m = 0; m < C::kMats; ++m)
                             ptx::tma_load_2d(sRaw + rs * C::kRawStage + m * C::kRawMat,
                                              sh ? &maps.ws[m] : &maps.w[m], xr, wrow, &raw_full[rs]);
                     }
-                    if constexpr (!C::kDeq) {
-                        const int as = it % C::kAStages;
-                        if (!ptx::mbar_wait(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 1))
-                            break;
+                    uint8_t* ssc = sScale + rs * C::kScaleStage;
+                    if constexpr (FMT == MOE_W_FP8_B128) {
+                        if (lane < C::kMats) {
+                            const int ob = (t.out + 127) >> 7, ib = (t.K + 127) >> 7;
+                            const float* sp = reinterpret_cast<const float*>(sh ? p.sh_scale[lane] : p.scale[lane]);
+                            ptx::cp_async4(ssc + 4 * lane,
+                                           sp + (size_t)(sh ? 0 : t.e) * ob * ib + (t.m0 >> 7) * ib + (k0 >> 7));
+                        }
+                    } else if (nv_smem_scales) {
+                        // Row r's 4 scale bytes of this stage: columns [k0, k0 + 64).
+                        for (int m = 0; m < C::kMats; ++m) {
+                            const uint8_t* sp = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]);
+#pragma unroll
+                            for (int q = 0; q < BM / 32; ++q) {
+                                const int r = lane + 32 * q, mrow = t.m0 + r;
+                                const uint8_t* src = (mrow < t.out)
+                                    ? sp + ((size_t)(sh ? 0 : t.e) * t.out + mrow) * (t.K / 16) + k0 / 16
+                                    : reinterpret_cast<const uint8_t*>(p.zero4);
+                                ptx::cp_async4(ssc + (m * BM + r) * 4, src);
+                            }
+                        }
+                    }
+                    ptx::cp_async_mbar_arrive(&raw_full[rs]);
+                    const int bs = it % C::kBStages;
+                    if (!ptx::mbar_wait_warp(&b_empty[bs], ((it / C::kBStages) & 1) ^ 1, s_abort, err, 1)) {
+                        stop = true;
+                        break;
+                    }
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(&b_full[bs], nbox * 2048);
+                        for (int j = 0; j < nbox; ++j)
+                            ptx::tma_load_2d(sB + bs * C::kBStage + j * 2048, bmap, k0, t.pos0 + 16 * j,
+                                             &b_full[bs]);
+                    }
+                } else {
+                    const int as = it % C::kAStages;
+                    if (!ptx::mbar_wait_warp(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 1)) {
+                        stop = true;
+                        break;
+                    }
+                    if (lane == 0) {
                         ptx::mbar_arrive_expect_tx(&a_full[as], C::kAStage + nbox * 2048);
                         for (int m = 0; m < C::kMats; ++m)
                             ptx::tma_load_2d(sA + as * C::kAStage + m * C::kAMat,
@@ -246,32 +295,25 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                         for (int j = 0; j < nbox; ++j)
                             ptx::tma_load_2d(sB + as * C::kBStage + j * 2048, bmap, k0, t.pos0 + 16 * j,
                                              &a_full[as]);
-                    } else {
-                        const int bs = it % C::kBStages;
-                        if (!ptx::mbar_wait(&b_empty[bs], ((it / C::kBStages) & 1) ^ 1, s_abort, err, 1))
-                            break;
-                        ptx::mbar_arrive_expect_tx(&b_full[bs], nbox * 2048);
-                        for (int j = 0; j < nbox; ++j)
-                            ptx::tma_load_2d(sB + bs * C::kBStage + j * 2048, bmap, k0, t.pos0 + 16 * j,
-                                             &b_full[bs]);
                     }
                 }
             }
-            if (*s_abort) {
-                // Let every copy this thread issued land before the CTA exits:
-                // wait (bounded) on the last phase of each ring stage it used.
-                constexpr uint32_t kRing = C::kDeq ? C::kBStages : C::kAStages;
-                const uint32_t na = it < kRing ? it : kRing;
-                for (uint32_t q = 0; q < na; ++q) {
-                    const uint32_t i2 = it - 1 - q, s2 = i2 % kRing;
-                    ptx::mbar_wait_quiet(C::kDeq ? &b_full[s2] : &a_full[s2], (i2 / kRing) & 1, 100000000ull);
-                }
-                if constexpr (C::kDeq) {
-                    const uint32_t nr = it < (uint32_t)C::kRawStages ? it : C::kRawStages;
-                    for (uint32_t q = 0; q < nr; ++q) {
-                        const uint32_t i2 = it - 1 - q, s2 = i2 % C::kRawStages;
-                        ptx::mbar_wait_quiet(&raw_full[s2], (i2 / C::kRawStages) & 1, 100000000ull);
-                    }
+        }
+        if constexpr (C::kDeq) asm volatile("cp.async.wait_all;" ::: "memory");
+        if (lane == 0 && *s_abort) {
+            // Let every copy this warp issued land before the CTA exits:
+            // wait (bounded) on the last phase of each ring stage it used.
+            constexpr uint32_t kRing = C::kDeq ? C::kBStages : C::kAStages;
+            const uint32_t na = it < kRing ? it : kRing;
+            for (uint32_t q = 0; q < na; ++q) {
+                const uint32_t i2 = it - 1 - q, s2 = i2 % kRing;
+                ptx::mbar_wait_quiet(C::kDeq ? &b_full[s2] : &a_full[s2], (i2 / kRing) & 1, 100000000ull);
+            }
+            if constexpr (C::kDeq) {
+                const uint32_t nr = it < (uint32_t)C::kRawStages ? it : C::kRawStages;
+                for (uint32_t q = 0; q < nr; ++q) {
+                    const uint32_t i2 = it - 1 - q, s2 = i2 % C::kRawStages;
+                    ptx::mbar_wait_quiet(&raw_full[s2], (i2 / C::kRawStages) & 1, 100000000ull);
                 }
             }
         }
@@ -410,10 +452,14 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                     const uint8_t* raw = sRaw + rs * C::kRawStage + m * C::kRawMat;
                     const uint32_t a_mat = ptx::smem_u32(sA + as * C::kAStage + m * C::kAMat);
                     if constexpr (FMT == MOE_W_FP8_B128) {
-                        // One fp32 scale per 128x128 block: uniform over this stage.
-                        const int ob = (t.out + 127) >> 7, ib = (t.K + 127) >> 7;
-                        const float* sc = reinterpret_cast<const float*>(sh ? p.sh_scale[m] : p.scale[m]);
-                        const float s = __ldg(sc + (size_t)(sh ? 0 : t.e) * ob * ib + (t.m0 >> 7) * ib + (k0 >> 7));
+                        // One fp32 scale per 128x128 block: uniform over this stage
+                        // (fetched into shared memory with the codes).
+                        const float s = reinterpret_cast<const float*>(sScale + rs * C::kScaleStage)[m];
+                        // In f16's normal range the product is formed in f16x2 (the
+                        // scale and the product each rounded once to f16); else in fp32.
+                        const bool f16_scale = s >= 6.2e-5f && s <= 128.0f;
+                        const __half2 s2 = __float2half2_rn(s);
+                        const uint32_t s2u = *reinterpret_cast<const uint32_t*>(&s2);
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
                             const int qd = dt + 256 * c;           // 512 chunks of 16 codes
@@ -421,12 +467,20 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                             const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 64 + ch * 16);
                             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
                             uint32_t o[8];
+                            if (f16_scale) {
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float2 lo = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] & 0xffffu));
-                                const float2 hi = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] >> 16));
-                                o[2 * i] = pack_f16(lo.x * s, lo.y * s);
-                                o[2 * i + 1] = pack_f16(hi.x * s, hi.y * s);
+                                for (int i = 0; i < 4; ++i) {
+                                    o[2 * i] = f16x2_mul(e4m3x2_to_f16x2(w4[i] & 0xffffu), s2u);
+                                    o[2 * i + 1] = f16x2_mul(e4m3x2_to_f16x2(w4[i] >> 16), s2u);
+                                }
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float2 lo = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] & 0xffffu));
+                                    const float2 hi = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] >> 16));
+                                    o[2 * i] = pack_f16(lo.x * s, lo.y * s);
+                                    o[2 * i + 1] = pack_f16(hi.x * s, hi.y * s);
+                                }
                             }
                             const uint32_t rowb = a_mat + r * 128;
                             st_shared_v4(rowb + (((2 * ch) ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
@@ -439,7 +493,13 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                         const int kc = k0 + 32 * ch;
                         const int mrow = t.m0 + r;
                         uint32_t s0 = 0, s1 = 0;   // f16x2 of the two block scales (0 outside the matrix)
-                        if (mrow < t.out && kc < t.K) {
+                        if (t.K % 64 == 0) {
+                            // Fetched into shared memory with the codes (0 past the last row).
+                            const uint32_t w = reinterpret_cast<const uint32_t*>(sScale + rs * C::kScaleStage)[m * BM + r];
+                            const uint32_t b0 = (w >> (16 * ch)) & 0xffu, b1 = (w >> (16 * ch + 8)) & 0xffu;
+                            s0 = e4m3x2_to_f16x2(b0 | (b0 << 8));
+                            s1 = e4m3x2_to_f16x2(b1 | (b1 << 8));
+                        } else if (mrow < t.out && kc < t.K) {
                             const uint8_t* sc = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]) +
                                                 ((size_t)(sh ? 0 : t.e) * t.out + mrow) * (t.K / 16) + kc / 16;
                             const uint32_t b0 = __ldg(sc), b1 = __ldg(sc + 1);

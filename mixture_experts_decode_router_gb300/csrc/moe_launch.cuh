@@ -58,6 +58,7 @@ struct TcParams {
     const int32_t* perm;     // sorted position -> route id
     const float* sg_logit;   // shared gate logits or NULL
     int32_t* err;            // Ctrl::err
+    const void* zero4;       // 4 zero bytes (stand-in scale source past the last row)
 };
 
 bool build_tc_maps(int fmt, bool gate_up, const moe_weights_t* w, int E, int H, int I, int S, int n,
