@@ -29,7 +29,9 @@
  *    current device; the caller owns every buffer (weights, input, outputs,
  *    workspace).  The library never allocates, frees or synchronises: each call
  *    only enqueues kernels on `stream` and returns.
- *  - Device pointers must be 16-byte aligned (MOE_ERR_ALIGNMENT otherwise).
+ *  - Device pointers must be 16-byte aligned (MOE_ERR_ALIGNMENT otherwise),
+ *    except the scale and scale2 arrays of moe_qmat_t, which need 4 bytes (so
+ *    that one rank's slice of a stacked scale array can be passed as it is).
  *  - All arguments are validated on the host before anything is enqueued; an
  *    error status means nothing was launched.  There is no fallback path: a
  *    configuration the kernels do not cover is refused by name
@@ -79,7 +81,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 /* A CUDA stream handle (the same object as cudaStream_t; NULL = legacy default stream). */
 typedef struct CUstream_st* moe_stream_t;
@@ -91,7 +93,7 @@ typedef enum {
     MOE_ERR_UNSUPPORTED = 3,     /* valid, but outside what the kernels cover (named refusal)*/
     MOE_ERR_WORKSPACE = 4,       /* workspace missing or smaller than moe_workspace_bytes()  */
     MOE_ERR_CUDA = 5,            /* a CUDA call failed while enqueueing (cudaGetLastError)   */
-    MOE_ERR_ALIGNMENT = 6,       /* a device pointer is not 16-byte aligned                  */
+    MOE_ERR_ALIGNMENT = 6,       /* a device pointer is not aligned (16 bytes; 4 for scales) */
     MOE_ERR_ALIAS = 7            /* `out` overlaps `x`                                       */
 } moe_status_t;
 
@@ -103,7 +105,35 @@ typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_B128 = 1, MOE_W_NVFP4 = 2 } moe_wfmt_t;
  * with one token still runs the single-token kernel (same arithmetic). */
 typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_TOKEN_MAJOR = 1, MOE_PATH_GROUPED = 2 } moe_path_t;
 
-/* Layer configuration (the config fields hidden_size, num_experts,
+/* Pre-expert RMSNorm (the pre_expert_norm step of MoeLayer::forward, page
+ * "metrale_model_layers/layers/moe/forward.rs"): with a norm weight, the routed
+ * and shared experts take xe = BF16(x / sqrt(mean(x^2) + eps) * w); the router
+ * and the shared-expert gate keep x.
+ *
+ * Expert parallelism (the EP branch of MoeLayer::forward and
+ * forward_token_major_decode): a call with [expert_begin, expert_end) holds
+ * only those experts -- the routed weight stacks have expert_end - expert_begin
+ * entries, indexed from expert_begin -- and routes to other experts contribute
+ * nothing; routing is still computed over all E.  With exclude_shared = 1 the
+ * output is one rank's partial: the caller sums the partials over ranks (an
+ * all-reduce) and adds the shared expert once, with a call that holds no
+ * experts (expert_begin = expert_end = E) and accumulate = 1: it adds the
+ * (gated) shared expert into the summed output, as the pages' residual_add /
+ * moe_batched_blend after the all-reduce do.  A call that holds no experts and
+ * is given neither idx nor w skips routing (it computes only the shared-gate
+ * logit); on one token it still routes.
+ *
+ * accumulate = 1: every output element is BF16(out + result), with out read
+ * on entry (rounded once, in fp32); out must then hold n x H valid values.
+ *
+ * NVFP4 router (the gate_nvfp4 / w4a16_gemm branch of the router step on the
+ * same page): router_fmt = MOE_W_NVFP4 takes the router from router_q, an
+ * NVFP4 matrix [E, H] in the expert layout below with one expert (w: bytes
+ * [E, H/2]; scale: E4M3 [E, H/16]; scale2: one fp32), multiplying the BF16
+ * activations; router_w is then unused (may be NULL).  One token then runs the
+ * token-major kernels (the single-token kernel reads a BF16 router).
+ *
+ * Layer configuration (the config fields hidden_size, num_experts,
  * num_experts_per_tok, moe_intermediate_size, shared_expert_intermediate_size,
  * norm_topk_prob and routed_scaling_factor of the pages' layer).
  * Limits: 1 <= num_experts <= 1024; 1 <= top_k <= min(num_experts, 32);
@@ -120,6 +150,13 @@ typedef struct {
     float   routed_scaling_factor;
     int32_t expert_fmt;             /* moe_wfmt_t: routed and shared experts alike */
     int32_t path;                   /* moe_path_t */
+    /* ABI version 2 (a zero-filled tail keeps the version-1 behaviour): */
+    float   rms_norm_eps;           /* epsilon of the pre-expert RMSNorm (when a norm weight is given) */
+    int32_t expert_begin;           /* expert parallelism: this call holds experts   */
+    int32_t expert_end;             /*   [expert_begin, expert_end); 0 and 0 = all E  */
+    int32_t exclude_shared;         /* 1: leave the shared expert out of the output  */
+    int32_t accumulate;             /* 1: out = BF16(out + layer output)             */
+    int32_t router_fmt;             /* MOE_W_BF16 (router_w) or MOE_W_NVFP4 (router_q) */
 } moe_config_t;
 
 /* One stacked expert matrix (device pointers; see the layouts above). */
@@ -137,6 +174,9 @@ typedef struct {
     moe_qmat_t   gate, up, down;    /* routed experts */
     moe_qmat_t   sh_gate, sh_up, sh_down;   /* shared expert (E = 1) */
     const void*  shared_gate_w;     /* BF16 [H] or NULL (then the shared gate is 1) */
+    /* ABI version 2: */
+    const void*  pre_expert_norm_w; /* BF16 [H] or NULL: RMSNorm of the experts' input */
+    moe_qmat_t   router_q;          /* NVFP4 router [E, H] when router_fmt = MOE_W_NVFP4 */
 } moe_weights_t;
 
 /* Bytes of workspace a call with up to `max_tokens` tokens needs (a multiple
@@ -158,9 +198,11 @@ moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* wts,
 
 /* Routed experts, shared expert and blend for n tokens given their routing
  * (the pages' exp_gate_up, exp_silu_down and wsum_blend steps).
- *   x     device BF16 [n, H]
- *   idx   device int32 [n, k]; an entry outside [0, E) is dropped (that slot
- *         contributes nothing), so a bad index never reads outside the weights
+ *   x     device BF16 [n, H] (the layer input: with a pre-expert norm weight
+ *         the experts take its RMSNorm, and the shared gate takes x itself)
+ *   idx   device int32 [n, k]; an entry outside [expert_begin, expert_end)
+ *         (all of [0, E) by default) is dropped (that slot contributes
+ *         nothing), so a bad index never reads outside the weights
  *   w     device fp32  [n, k]
  *   out   device BF16 [n, H] (out); must not overlap x
  * Errors: as moe_route, plus MOE_ERR_ALIAS. */
@@ -184,8 +226,11 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* wts,
  *             the caller on the current device; marker i is recorded with
  *             cudaEventRecord(events[i], stream) for i < n_events
  *   n_marks   (out, optional) markers the call reached
- * Markers: 0 before the first kernel, then one after each kernel, in launch
- * order: router, top-k, expert grouping, gate+up, down+blend.
+ * Markers: 0 before the first kernel, then one after each stage, in launch
+ * order.  One token on the single-token kernel: 2 markers (before, after).
+ * Token-major kernels: 6 (router, top-k, grouping, gate+up, down+blend).
+ * Grouped tensor-core path: 8 (router, top-k, grouping, gather, gate+up, down,
+ * combine).  The pre-expert RMSNorm, when present, runs in the grouping stage.
  * Errors: as moe_forward, plus MOE_ERR_NULL for events == NULL with n_events > 0. */
 moe_status_t moe_forward_timed(const moe_config_t* cfg, const moe_weights_t* wts,
                                const void* x, int32_t n, void* out,

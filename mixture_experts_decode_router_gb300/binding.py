@@ -47,7 +47,10 @@ class moe_config_t(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("inter", ctypes.c_int32),
                 ("shared_inter", ctypes.c_int32), ("routing", ctypes.c_int32),
                 ("norm_topk_prob", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
-                ("expert_fmt", ctypes.c_int32), ("path", ctypes.c_int32)]
+                ("expert_fmt", ctypes.c_int32), ("path", ctypes.c_int32),
+                ("rms_norm_eps", ctypes.c_float), ("expert_begin", ctypes.c_int32),
+                ("expert_end", ctypes.c_int32), ("exclude_shared", ctypes.c_int32),
+                ("accumulate", ctypes.c_int32), ("router_fmt", ctypes.c_int32)]
 
 
 class moe_qmat_t(ctypes.Structure):
@@ -58,7 +61,8 @@ class moe_weights_t(ctypes.Structure):
     _fields_ = [("router_w", ctypes.c_void_p), ("correction_bias", ctypes.c_void_p),
                 ("gate", moe_qmat_t), ("up", moe_qmat_t), ("down", moe_qmat_t),
                 ("sh_gate", moe_qmat_t), ("sh_up", moe_qmat_t), ("sh_down", moe_qmat_t),
-                ("shared_gate_w", ctypes.c_void_p)]
+                ("shared_gate_w", ctypes.c_void_p), ("pre_expert_norm_w", ctypes.c_void_p),
+                ("router_q", moe_qmat_t)]
 
 
 _lib: Optional[ctypes.CDLL] = None

@@ -39,6 +39,7 @@ struct Marks {
 };
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 static moe_status_t check_config(const moe_config_t* c) {
     if (!c) return MOE_ERR_NULL;
@@ -63,23 +64,49 @@ static moe_status_t check_config(const moe_config_t* c) {
     return MOE_OK;
 }
 
+// The configuration a call runs: the expert range resolved ((0, 0) = all E)
+// and the shared expert dropped when the call leaves it out.
+static moe_status_t effective_config(const moe_config_t* c, moe_config_t* out) {
+    moe_status_t s = check_config(c);
+    if (s != MOE_OK) return s;
+    *out = *c;
+    if (c->expert_begin == 0 && c->expert_end == 0) out->expert_end = c->num_experts;
+    if (out->expert_begin < 0 || out->expert_begin > out->expert_end || out->expert_end > c->num_experts)
+        return MOE_ERR_INVALID_CONFIG;
+    if (c->exclude_shared != 0 && c->exclude_shared != 1) return MOE_ERR_INVALID_CONFIG;
+    if (c->accumulate != 0 && c->accumulate != 1) return MOE_ERR_INVALID_CONFIG;
+    if (c->router_fmt != MOE_W_BF16 && c->router_fmt != MOE_W_NVFP4) return MOE_ERR_INVALID_CONFIG;
+    if (!(c->rms_norm_eps >= 0.0f && c->rms_norm_eps <= 3.0e38f)) return MOE_ERR_INVALID_CONFIG;
+    if (c->exclude_shared) out->shared_inter = 0;
+    return MOE_OK;
+}
+
+static int local_experts(const moe_config_t* c) { return c->expert_end - c->expert_begin; }
+
 static moe_status_t check_qmat(int fmt, const moe_qmat_t& q) {
     if (!q.w) return MOE_ERR_NULL;
     if (!aligned16(q.w)) return MOE_ERR_ALIGNMENT;
+    // Scales are read 4 bytes at a time at most.
     if (fmt == MOE_W_FP8_B128 || fmt == MOE_W_NVFP4) {
         if (!q.scale) return MOE_ERR_NULL;
-        if (!aligned16(q.scale)) return MOE_ERR_ALIGNMENT;
+        if (!aligned4(q.scale)) return MOE_ERR_ALIGNMENT;
     }
     if (fmt == MOE_W_NVFP4) {
         if (!q.scale2) return MOE_ERR_NULL;
-        if (!aligned16(q.scale2)) return MOE_ERR_ALIGNMENT;
+        if (!aligned4(q.scale2)) return MOE_ERR_ALIGNMENT;
     }
     return MOE_OK;
 }
 
 static moe_status_t check_router_weights(const moe_config_t* c, const moe_weights_t* w) {
-    if (!w || !w->router_w) return MOE_ERR_NULL;
-    if (!aligned16(w->router_w)) return MOE_ERR_ALIGNMENT;
+    if (!w) return MOE_ERR_NULL;
+    if (c->router_fmt == MOE_W_NVFP4) {
+        const moe_status_t s = check_qmat(MOE_W_NVFP4, w->router_q);
+        if (s != MOE_OK) return s;
+    } else {
+        if (!w->router_w) return MOE_ERR_NULL;
+        if (!aligned16(w->router_w)) return MOE_ERR_ALIGNMENT;
+    }
     if (c->routing == MOE_ROUTE_SIGMOID_BIAS) {
         if (!w->correction_bias) return MOE_ERR_NULL;
         if (!aligned16(w->correction_bias)) return MOE_ERR_ALIGNMENT;
@@ -92,15 +119,18 @@ static moe_status_t check_router_weights(const moe_config_t* c, const moe_weight
 static moe_status_t check_expert_weights(const moe_config_t* c, const moe_weights_t* w) {
     if (!w) return MOE_ERR_NULL;
     moe_status_t s;
-    if ((s = check_qmat(c->expert_fmt, w->gate)) != MOE_OK) return s;
-    if ((s = check_qmat(c->expert_fmt, w->up)) != MOE_OK) return s;
-    if ((s = check_qmat(c->expert_fmt, w->down)) != MOE_OK) return s;
+    if (local_experts(c) > 0) {   // routed stacks, unless the call holds no expert
+        if ((s = check_qmat(c->expert_fmt, w->gate)) != MOE_OK) return s;
+        if ((s = check_qmat(c->expert_fmt, w->up)) != MOE_OK) return s;
+        if ((s = check_qmat(c->expert_fmt, w->down)) != MOE_OK) return s;
+    }
     if (c->shared_inter > 0) {
         if ((s = check_qmat(c->expert_fmt, w->sh_gate)) != MOE_OK) return s;
         if ((s = check_qmat(c->expert_fmt, w->sh_up)) != MOE_OK) return s;
         if ((s = check_qmat(c->expert_fmt, w->sh_down)) != MOE_OK) return s;
     }
     if (w->shared_gate_w && !aligned16(w->shared_gate_w)) return MOE_ERR_ALIGNMENT;
+    if (w->pre_expert_norm_w && !aligned16(w->pre_expert_norm_w)) return MOE_ERR_ALIGNMENT;
     return MOE_OK;
 }
 
@@ -117,13 +147,15 @@ template <typename T> static T* at(void* ws, size_t off) {
     return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
-static QMatDev qdev(const moe_qmat_t& q, int out_dim, int in_dim) {
+// e_base: global index of the stack's first expert (0 for the shared expert).
+static QMatDev qdev(const moe_qmat_t& q, int out_dim, int in_dim, int e_base) {
     QMatDev d;
     d.w = static_cast<const uint8_t*>(q.w);
     d.scale = q.scale;
     d.scale2 = q.scale2;
     d.out_dim = out_dim;
     d.in_dim = in_dim;
+    d.e_base = e_base;
     return d;
 }
 
@@ -133,10 +165,20 @@ static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w,
                                   const WsLayout& L, cudaStream_t st, Marks& mk) {
     const int sms = device_sm_count();
     float* lg = logits ? logits : at<float>(ws, L.logits);
-    cudaError_t e = launch_router(static_cast<const uint16_t*>(x), n, c->hidden,
-                                  static_cast<const uint16_t*>(w->router_w), c->num_experts,
-                                  static_cast<const uint16_t*>(w->shared_gate_w), lg,
-                                  at<float>(ws, L.sg_logit), sms, st);
+    cudaError_t e;
+    if (c->router_fmt == MOE_W_NVFP4) {
+        e = launch_router_nvfp4(static_cast<const uint16_t*>(x), n, c->hidden,
+                                qdev(w->router_q, c->num_experts, c->hidden, 0), c->num_experts, lg, st);
+        if (e == cudaSuccess && w->shared_gate_w)   // the BF16 shared-gate row on its own
+            e = launch_router(static_cast<const uint16_t*>(x), n, c->hidden, nullptr, 0,
+                              static_cast<const uint16_t*>(w->shared_gate_w), nullptr,
+                              at<float>(ws, L.sg_logit), sms, st);
+    } else {
+        e = launch_router(static_cast<const uint16_t*>(x), n, c->hidden,
+                          static_cast<const uint16_t*>(w->router_w), c->num_experts,
+                          static_cast<const uint16_t*>(w->shared_gate_w), lg,
+                          at<float>(ws, L.sg_logit), sms, st);
+    }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     mk.mark(st);
     e = launch_topk(lg, n, c->num_experts, c->top_k, c->routing, w->correction_bias,
@@ -153,12 +195,14 @@ static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w,
 constexpr int kTokenMajorMaxN = 3;
 
 // The grouped tensor-core expert stage (after the grouping kernel).
+// x: the experts' input (the layer input or its pre-expert RMSNorm).
 static moe_status_t enqueue_grouped(const moe_config_t* c, const moe_weights_t* w, const void* x,
                                     int32_t n, const float* wt, void* out, void* ws, const WsLayout& L,
                                     float* sg_logit, cudaStream_t st, Marks& mk) {
     const int sms = device_sm_count();
     const int fmt = c->expert_fmt;
     const int H = c->hidden, I = c->inter, S = c->shared_inter, k = c->top_k, E = c->num_experts;
+    const int E_loc = local_experts(c);
     const bool f16_ops = fmt != MOE_W_BF16;   // FP8 / NVFP4 tiles use f16 operands
     uint16_t* xs = at<uint16_t>(ws, L.xs);
     uint16_t* xh = at<uint16_t>(ws, L.xh);
@@ -170,6 +214,7 @@ static moe_status_t enqueue_grouped(const moe_config_t* c, const moe_weights_t* 
     TcParams p{};
     p.n = n;
     p.k = k;
+    p.e_base = c->expert_begin;
     p.segs = at<int32_t>(ws, L.segs);
     p.ctrl = at<Ctrl>(ws, L.ctrl);
     p.err = &at<Ctrl>(ws, L.ctrl)->err;
@@ -182,30 +227,32 @@ static moe_status_t enqueue_grouped(const moe_config_t* c, const moe_weights_t* 
     p.y = at<float>(ws, L.y);
     p.y_sh = at<float>(ws, L.ysh);
 
+    const bool tiles = E_loc > 0 || S > 0;   // otherwise the output is zero: combine alone
     // gate + up
     TcMaps maps;
-    if (!build_tc_maps(fmt, true, w, E, H, I, S, n, n * k, xs, f16_ops ? (const void*)xh : x, &maps))
+    if (tiles && !build_tc_maps(fmt, true, w, E_loc, H, I, S, n, n * k, xs, f16_ops ? (const void*)xh : x,
+                                &maps))
         return MOE_ERR_CUDA;
     p.out_dim = I; p.in_dim = H; p.sh_out = S; p.sh_in = H;
     p.scale[0] = w->gate.scale; p.scale[1] = w->up.scale;
     p.sh_scale[0] = w->sh_gate.scale; p.sh_scale[1] = w->sh_up.scale;
     p.scale2[0] = w->gate.scale2; p.scale2[1] = w->up.scale2;
     p.sh_scale2[0] = w->sh_gate.scale2; p.sh_scale2[1] = w->sh_up.scale2;
-    if ((e = launch_grouped_tc(fmt, true, maps, p, sms, st)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (tiles && (e = launch_grouped_tc(fmt, true, maps, p, sms, st)) != cudaSuccess) return MOE_ERR_CUDA;
     mk.mark(st);
 
     // down (+ routing weight / shared gate)
-    if (!build_tc_maps(fmt, false, w, E, H, I, S, n, n * k, p.act_out, p.act_sh_out, &maps))
+    if (tiles && !build_tc_maps(fmt, false, w, E_loc, H, I, S, n, n * k, p.act_out, p.act_sh_out, &maps))
         return MOE_ERR_CUDA;
     p.out_dim = H; p.in_dim = I; p.sh_out = S > 0 ? H : 0; p.sh_in = S;
     p.scale[0] = p.scale[1] = w->down.scale;
     p.sh_scale[0] = p.sh_scale[1] = w->sh_down.scale;
     p.scale2[0] = p.scale2[1] = w->down.scale2;
     p.sh_scale2[0] = p.sh_scale2[1] = w->sh_down.scale2;
-    if ((e = launch_grouped_tc(fmt, false, maps, p, sms, st)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (tiles && (e = launch_grouped_tc(fmt, false, maps, p, sms, st)) != cudaSuccess) return MOE_ERR_CUDA;
     mk.mark(st);
 
-    e = launch_combine(p.y, p.y_sh, at<int32_t>(ws, L.inv), n, H, k, S > 0 ? 1 : 0,
+    e = launch_combine(p.y, p.y_sh, at<int32_t>(ws, L.inv), n, H, k, S > 0 ? 1 : 0, c->accumulate,
                        static_cast<uint16_t*>(out), sms, st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     mk.mark(st);
@@ -230,9 +277,19 @@ static moe_status_t enqueue_experts(const moe_config_t* c, const moe_weights_t* 
                           static_cast<const uint16_t*>(w->shared_gate_w), nullptr, sg_logit, sms, st);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
-    e = launch_group(idx, n * k, E, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
-                     at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv), at<int32_t>(ws, L.active),
-                     at<int32_t>(ws, L.segs), at<Ctrl>(ws, L.ctrl), st);
+    // The experts' input: x, or its pre-expert RMSNorm (the router and the
+    // shared gate keep x).
+    const void* xin = x;
+    if (w->pre_expert_norm_w) {
+        uint16_t* xe = at<uint16_t>(ws, L.xe);
+        e = launch_rmsnorm(static_cast<const uint16_t*>(x), n, H,
+                           static_cast<const uint16_t*>(w->pre_expert_norm_w), c->rms_norm_eps, xe, st);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        xin = xe;
+    }
+    e = launch_group(idx, n * k, E, c->expert_begin, c->expert_end, at<int32_t>(ws, L.counts),
+                     at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv),
+                     at<int32_t>(ws, L.active), at<int32_t>(ws, L.segs), at<Ctrl>(ws, L.ctrl), st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     mk.mark(st);
 
@@ -240,16 +297,17 @@ static moe_status_t enqueue_experts(const moe_config_t* c, const moe_weights_t* 
                                                                         : MOE_PATH_GROUPED)
                                                 : c->path;
     if (path == MOE_PATH_GROUPED)
-        return enqueue_grouped(c, w, x, n, wt, out, ws, L, sg_logit, st, mk);
+        return enqueue_grouped(c, w, xin, n, wt, out, ws, L, sg_logit, st, mk);
 
+    const int eb = c->expert_begin;
     GateUpParams gu{};
-    gu.x = static_cast<const uint16_t*>(x);
+    gu.x = static_cast<const uint16_t*>(xin);
     gu.n = n; gu.H = H; gu.I = I; gu.S = S; gu.k = k;
-    gu.gate = qdev(w->gate, I, H);
-    gu.up = qdev(w->up, I, H);
+    gu.gate = qdev(w->gate, I, H, eb);
+    gu.up = qdev(w->up, I, H, eb);
     if (S > 0) {
-        gu.sh_gate = qdev(w->sh_gate, S, H);
-        gu.sh_up = qdev(w->sh_up, S, H);
+        gu.sh_gate = qdev(w->sh_gate, S, H, 0);
+        gu.sh_up = qdev(w->sh_up, S, H, 0);
     }
     gu.counts = at<int32_t>(ws, L.counts);
     gu.offsets = at<int32_t>(ws, L.offsets);
@@ -261,8 +319,10 @@ static moe_status_t enqueue_experts(const moe_config_t* c, const moe_weights_t* 
 
     DownParams dn{};
     dn.n = n; dn.H = H; dn.I = I; dn.S = S; dn.k = k; dn.E = E;
-    dn.down = qdev(w->down, H, I);
-    if (S > 0) dn.sh_down = qdev(w->sh_down, H, S);
+    dn.e_begin = c->expert_begin; dn.e_end = c->expert_end;
+    dn.accumulate = c->accumulate;
+    dn.down = qdev(w->down, H, I, eb);
+    if (S > 0) dn.sh_down = qdev(w->sh_down, H, S, 0);
     dn.idx = idx;
     dn.w = wt;
     dn.act = gu.act;
@@ -290,15 +350,18 @@ using namespace moe;
 
 extern "C" {
 
-size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t max_tokens) {
-    if (check_config(cfg) != MOE_OK || max_tokens < 0) return 0;
-    return ws_layout(*cfg, max_tokens).total;
+size_t moe_workspace_bytes(const moe_config_t* cfg_in, int32_t max_tokens) {
+    moe_config_t c;
+    if (effective_config(cfg_in, &c) != MOE_OK || max_tokens < 0) return 0;
+    return ws_layout(c, max_tokens).total;
 }
 
-moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* wts, const void* x, int32_t n,
+moe_status_t moe_route(const moe_config_t* cfg_in, const moe_weights_t* wts, const void* x, int32_t n,
                        int32_t* idx, float* w, float* logits, void* ws, size_t ws_bytes,
                        moe_stream_t stream) {
-    moe_status_t s = check_config(cfg);
+    moe_config_t c;
+    const moe_config_t* cfg = &c;
+    moe_status_t s = effective_config(cfg_in, &c);
     if (s != MOE_OK) return s;
     if (n < 0) return MOE_ERR_INVALID_CONFIG;
     if ((s = check_router_weights(cfg, wts)) != MOE_OK) return s;
@@ -314,14 +377,15 @@ moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* wts, const 
                          mk);
 }
 
-moe_status_t moe_experts(const moe_config_t* cfg, const moe_weights_t* wts, const void* x, int32_t n,
+moe_status_t moe_experts(const moe_config_t* cfg_in, const moe_weights_t* wts, const void* x, int32_t n,
                          const int32_t* idx, const float* w, void* out, void* ws, size_t ws_bytes,
                          moe_stream_t stream) {
-    moe_status_t s = check_config(cfg);
+    moe_config_t c;
+    const moe_config_t* cfg = &c;
+    moe_status_t s = effective_config(cfg_in, &c);
     if (s != MOE_OK) return s;
     if (n < 0) return MOE_ERR_INVALID_CONFIG;
     if ((s = check_expert_weights(cfg, wts)) != MOE_OK) return s;
-    if (wts->shared_gate_w && !wts->router_w) return MOE_ERR_NULL;
     if (n == 0) return MOE_OK;
     if (!x || !idx || !w || !out) return MOE_ERR_NULL;
     if (!aligned16(x) || !aligned16(idx) || !aligned16(w) || !aligned16(out)) return MOE_ERR_ALIGNMENT;
@@ -333,10 +397,12 @@ moe_status_t moe_experts(const moe_config_t* cfg, const moe_weights_t* wts, cons
                            reinterpret_cast<cudaStream_t>(stream), mk);
 }
 
-static moe_status_t forward_impl(const moe_config_t* cfg, const moe_weights_t* wts, const void* x,
+static moe_status_t forward_impl(const moe_config_t* cfg_in, const moe_weights_t* wts, const void* x,
                                  int32_t n, void* out, int32_t* idx, float* w, void* ws,
                                  size_t ws_bytes, moe_stream_t stream, Marks& mk) {
-    moe_status_t s = check_config(cfg);
+    moe_config_t c;
+    const moe_config_t* cfg = &c;
+    moe_status_t s = effective_config(cfg_in, &c);
     if (s != MOE_OK) return s;
     if (n < 0) return MOE_ERR_INVALID_CONFIG;
     if ((s = check_router_weights(cfg, wts)) != MOE_OK) return s;
@@ -352,7 +418,7 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const moe_weights_t* w
     int32_t* idx_p = idx ? idx : at<int32_t>(ws, L.idx);
     float* w_p = w ? w : at<float>(ws, L.w);
     mk.mark(st);
-    if (n == 1 && cfg->path != MOE_PATH_GROUPED) {
+    if (n == 1 && cfg->path != MOE_PATH_GROUPED && cfg->router_fmt == MOE_W_BF16) {
         // One token: the whole layer in one cooperative launch when its
         // shared-memory plan fits (same arithmetic as the kernels below).
         const int sms = device_sm_count();
@@ -362,16 +428,21 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const moe_weights_t* w
             fp.x = static_cast<const uint16_t*>(x);
             fp.H = H; fp.E = cfg->num_experts; fp.k = cfg->top_k; fp.I = I; fp.S = S;
             fp.routing = cfg->routing; fp.norm = cfg->norm_topk_prob; fp.scale = cfg->routed_scaling_factor;
+            fp.e_begin = cfg->expert_begin; fp.e_end = cfg->expert_end;
+            fp.accumulate = cfg->accumulate;
+            fp.norm_w = static_cast<const uint16_t*>(wts->pre_expert_norm_w);
+            fp.eps = cfg->rms_norm_eps;
             fp.router = static_cast<const uint16_t*>(wts->router_w);
             fp.gw = static_cast<const uint16_t*>(wts->shared_gate_w);
             fp.bias = wts->correction_bias;
-            fp.gate = qdev(wts->gate, I, H);
-            fp.up = qdev(wts->up, I, H);
-            fp.down = qdev(wts->down, H, I);
+            const int eb = cfg->expert_begin;
+            fp.gate = qdev(wts->gate, I, H, eb);
+            fp.up = qdev(wts->up, I, H, eb);
+            fp.down = qdev(wts->down, H, I, eb);
             if (S > 0) {
-                fp.sh_gate = qdev(wts->sh_gate, S, H);
-                fp.sh_up = qdev(wts->sh_up, S, H);
-                fp.sh_down = qdev(wts->sh_down, H, S);
+                fp.sh_gate = qdev(wts->sh_gate, S, H, 0);
+                fp.sh_up = qdev(wts->sh_up, S, H, 0);
+                fp.sh_down = qdev(wts->sh_down, H, S, 0);
             }
             fp.logits = at<float>(ws, L.logits);
             fp.sg_logit = at<float>(ws, L.sg_logit);
@@ -388,7 +459,21 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const moe_weights_t* w
             (void)cudaGetLastError();   // not launchable here: the multi-kernel path below
         }
     }
-    if ((s = enqueue_route(cfg, wts, x, n, idx_p, w_p, nullptr, ws, L, st, mk)) != MOE_OK) return s;
+    if (local_experts(cfg) == 0 && !idx && !w) {
+        // No expert held here and no routing asked for (the shared-expert call
+        // of expert parallelism): only the shared-gate logit is needed.
+        if (wts->shared_gate_w) {
+            const cudaError_t e = launch_router(static_cast<const uint16_t*>(x), n, cfg->hidden,
+                                                static_cast<const uint16_t*>(wts->router_w), 0,
+                                                static_cast<const uint16_t*>(wts->shared_gate_w), nullptr,
+                                                at<float>(ws, L.sg_logit), device_sm_count(), st);
+            if (e != cudaSuccess) return MOE_ERR_CUDA;
+        }
+        mk.mark(st);
+        mk.mark(st);
+    } else if ((s = enqueue_route(cfg, wts, x, n, idx_p, w_p, nullptr, ws, L, st, mk)) != MOE_OK) {
+        return s;
+    }
     return enqueue_experts(cfg, wts, x, n, idx_p, w_p, out, ws, L, true, st, mk);
 }
 
@@ -436,7 +521,7 @@ const char* moe_status_string(moe_status_t status) {
         case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: configuration outside what the kernels cover";
         case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing or too small";
         case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA launch failed";
-        case MOE_ERR_ALIGNMENT: return "MOE_ERR_ALIGNMENT: a device pointer is not 16-byte aligned";
+        case MOE_ERR_ALIGNMENT: return "MOE_ERR_ALIGNMENT: a device pointer is not aligned (16 bytes; scales 4)";
         case MOE_ERR_ALIAS: return "MOE_ERR_ALIAS: out overlaps x";
         default: return "unknown moe_status_t";
     }

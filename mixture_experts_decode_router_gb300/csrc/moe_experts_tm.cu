@@ -157,7 +157,7 @@ down_blend_tm_kernel(const DownParams p) {
             for (int j = 0; j < p.k; ++j) {
                 const int r = t * p.k + j;
                 const int e = __ldg(p.idx + r);
-                if (e < 0 || e >= p.E) continue;   // dropped route (see the grouping)
+                if (e < p.e_begin || e >= p.e_end) continue;   // dropped route (see the grouping)
                 const float wt = __ldg(p.w + r) * matrix_scale<FMT>(p.down, e);
                 acc = fmaf(row_dot_act<FMT>(p.down, e, h, p.act + (size_t)r * p.I, p.I, lane), wt, acc);
             }
@@ -168,10 +168,12 @@ down_blend_tm_kernel(const DownParams p) {
                 acc = fmaf(row_dot_act<FMT>(p.sh_down, 0, h, p.act_sh + (size_t)t * p.S, p.S, lane), gs,
                            acc);
             }
-            const float s = warp_sum(acc);
+            float s = warp_sum(acc);
             if (lane == 0) {
+                uint16_t* o = p.out + (size_t)t * p.H + h;
+                if (p.accumulate) s += __uint_as_float((uint32_t)*o << 16);
                 const __nv_bfloat16 b = __float2bfloat16_rn(s);
-                p.out[(size_t)t * p.H + h] = *reinterpret_cast<const uint16_t*>(&b);
+                *o = *reinterpret_cast<const uint16_t*>(&b);
             }
         }
     }

@@ -56,7 +56,7 @@ __device__ __forceinline__ size_t row_bytes_of(int fmt, int in_dim) {
 
 template <int FMT>
 __device__ __forceinline__ const uint8_t* row_ptr(const QMatDev& m, int e, int row) {
-    return m.w + ((size_t)e * m.out_dim + row) * row_bytes_of(FMT, m.in_dim);
+    return m.w + ((size_t)(e - m.e_base) * m.out_dim + row) * row_bytes_of(FMT, m.in_dim);
 }
 
 // Lane partial of one down-projection row against an activation vector, with
@@ -132,6 +132,25 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
         reinterpret_cast<uint4*>(sx)[i] = __ldg(reinterpret_cast<const uint4*>(p.x) + i);
     __syncthreads();
     const bool refused = *abort_f == 2;
+    // The experts' input: x, or its pre-expert RMSNorm (the norm kernel's
+    // arithmetic); the router keeps x.
+    const uint16_t* sxe = sx;
+    if (p.norm_w) {
+        uint16_t* sxn = reinterpret_cast<uint16_t*>(sm + p.off_xe);
+        float* s_inv = reinterpret_cast<float*>(sm + p.off_sel + 256);
+        if (warp == 0) {
+            const float inv = rms_inv_warp(sx, H, p.eps, lane);
+            if (lane == 0) *s_inv = inv;
+        }
+        __syncthreads();
+        const float inv = *s_inv;
+        for (int c = tid; c < H / 8; c += kFThreads)
+            reinterpret_cast<uint4*>(sxn)[c] = rms_apply8(reinterpret_cast<const uint4*>(sx)[c],
+                                                          __ldg(reinterpret_cast<const uint4*>(p.norm_w) + c), inv);
+        __syncthreads();
+        sxe = sxn;
+    }
+    auto local = [&](int e) { return e >= p.e_begin && e < p.e_end; };
 
     // Work of this CTA.
     const int rpc = p.rpc;
@@ -156,11 +175,15 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                 ptx::mbar_arrive(dshfull);
             }
             ok = ptx::mbar_wait(sel_ready, 0, abort_f, err, 12);
-            if (ok && nrows > 0) {
-                ptx::mbar_arrive_expect_tx(dfull, (uint32_t)(k * nrows * p.drow_bytes));
+            int n_local = 0;
+            if (ok)
+                for (int j = 0; j < k; ++j) n_local += local(ssel[j]) ? 1 : 0;
+            if (ok && nrows > 0 && n_local > 0) {
+                ptx::mbar_arrive_expect_tx(dfull, (uint32_t)(n_local * nrows * p.drow_bytes));
                 for (int j = 0; j < k; ++j)
-                    ptx::bulk_load(sdown + (size_t)j * rpc * p.drow_bytes, row_ptr<FMT>(p.down, ssel[j], h0),
-                                   nrows * p.drow_bytes, dfull);
+                    if (local(ssel[j]))
+                        ptx::bulk_load(sdown + (size_t)j * rpc * p.drow_bytes, row_ptr<FMT>(p.down, ssel[j], h0),
+                                       nrows * p.drow_bytes, dfull);
             } else if (ok) {
                 ptx::mbar_arrive(dfull);
             } else {
@@ -220,7 +243,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                         cg[i].decode(wg);
                         cu[i].decode(wu);
                         const float sg = cg[i].scale(Gm, e, row, c), su = cu[i].scale(Um, e, row, c);
-                        bf16x8_to_float(reinterpret_cast<const uint4*>(sx)[c], xv);
+                        bf16x8_to_float(reinterpret_cast<const uint4*>(sxe)[c], xv);
                         ag = fmaf(dot8(wg, xv), sg, ag);
                         au = fmaf(dot8(wu, xv), su, au);
                     }
@@ -313,6 +336,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                 if (s < n_sh) continue;
                 const int q = r_b + (s - n_sh);
                 const int j = q / I, i = q - j * I, e = ssel[j];
+                if (!local(e)) continue;   // held by another call (expert parallelism)
                 consume(p.gate, p.up, e, i, matrix_scale<FMT>(p.gate, e), matrix_scale<FMT>(p.up, e),
                         p.act + (size_t)j * I + i);
             }
@@ -362,6 +386,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                     float acc = 0.f;
                     for (int j = 0; j < k; ++j) {
                         const int e = ssel[j];
+                        if (!local(e)) continue;
                         const float wt = sselw[j] * matrix_scale<FMT>(p.down, e);
                         const uint8_t* drow = sdown + ((size_t)j * rpc + (h - h0)) * p.drow_bytes;
                         acc = fmaf(row_partial_smem<FMT>(drow, sact + (size_t)j * I, p.down, e, h, I, lane), wt,
@@ -373,8 +398,9 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                         acc = fmaf(row_partial_smem<FMT>(drow, sact + (size_t)k * I, p.sh_down, 0, h, S, lane), gs,
                                    acc);
                     }
-                    const float s = warp_sum(acc);
+                    float s = warp_sum(acc);
                     if (lane == 0) {
+                        if (p.accumulate) s += __uint_as_float((uint32_t)p.out[h] << 16);
                         const __nv_bfloat16 b = __float2bfloat16_rn(s);
                         p.out[h] = *reinterpret_cast<const uint16_t*>(&b);
                     }
@@ -403,9 +429,10 @@ bool fused_plan(const moe_config_t* c, int num_sms, FusedParams* p) {
     size_t off = 0;
     auto take = [&](size_t b, size_t al) { off = (off + al - 1) / al * al; size_t o = off; off += b; return (uint32_t)o; };
     p->off_x = take((size_t)H * 2, 128);
+    p->off_xe = take((size_t)H * 2, 128);
     p->off_lg = take((size_t)E * 4, 16);
     p->off_sc = take((size_t)E * 4, 16);
-    p->off_sel = take(256, 16);
+    p->off_sel = take(256 + 16, 16);   // 32 experts, 32 weights, the inverse RMS
     p->off_down = take((size_t)(k + 1) * p->rpc * p->drow_bytes, 128);
     p->off_act = take(((size_t)k * I + (S > 0 ? S : 0)) * 4, 16);
     // dfull, dshfull, sel_ready, abort + phase flags

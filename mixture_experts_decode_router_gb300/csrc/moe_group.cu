@@ -10,7 +10,8 @@
 //   offsets[e]  exclusive prefix sum of counts (offsets[E] = routes kept)
 //   perm[p]     route ids r = t*k + j, grouped by expert, ascending r within an
 //               expert (a stable order, independent of thread timing); a route
-//               whose index lies outside [0, E) is dropped
+//               whose expert lies outside [e_begin, e_end) -- not held by this
+//               call, or not an expert at all -- is dropped
 //   inv[r]      sorted position of route r (-1 for a dropped route)
 //   active[u]   experts with counts > 0, ascending; ctrl->n_active of them
 //   segs[s]     (expert, first sorted position, routes) for runs of at most
@@ -24,7 +25,7 @@ constexpr int kGroupThreads = 1024;
 constexpr int kSegWarps = 8;   // warps that own contiguous route segments
 
 __global__ void __launch_bounds__(kGroupThreads)
-group_kernel(const int32_t* __restrict__ idx, int nk, int E,
+group_kernel(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_end,
              int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
              int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ active,
              int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl) {
@@ -43,7 +44,7 @@ group_kernel(const int32_t* __restrict__ idx, int nk, int E,
         const int b = warp * seg, e_ = min(nk, b + seg);
         for (int r = b + lane; r < e_; r += 32) {
             const int e = idx[r];
-            if (e >= 0 && e < E) atomicAdd(&cnt[warp * E + e], 1);   // out-of-range: dropped
+            if (e >= e_begin && e < e_end) atomicAdd(&cnt[warp * E + e], 1);   // not held here: dropped
         }
     }
     __syncthreads();
@@ -122,7 +123,7 @@ group_kernel(const int32_t* __restrict__ idx, int nk, int E,
             const int r = r0 + lane;
             const bool valid = r < e_;
             const int e = valid ? idx[r] : -1;
-            const bool in_range = valid && e >= 0 && e < E;
+            const bool in_range = valid && e >= e_begin && e < e_end;
             if (valid && !in_range) inv[r] = -1;
             const unsigned vmask = __ballot_sync(0xffffffffu, in_range);
             if (in_range) {
@@ -140,12 +141,12 @@ group_kernel(const int32_t* __restrict__ idx, int nk, int E,
     pdl_trigger();
 }
 
-cudaError_t launch_group(const int32_t* idx, int nk, int E, int32_t* counts, int32_t* offsets,
-                         int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs, Ctrl* ctrl,
-                         cudaStream_t st) {
+cudaError_t launch_group(const int32_t* idx, int nk, int E, int e_begin, int e_end, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
+                         Ctrl* ctrl, cudaStream_t st) {
     const size_t smem = sizeof(int32_t) * (size_t)(kSegWarps + 1) * E;
     // (kSegWarps + 1) * E ints <= 36 KB for E <= 1024: under the 48 KB default.
-    launch_pdl(group_kernel, 1, kGroupThreads, smem, st, idx, nk, E, counts, offsets, perm, inv, active, segs,
+    launch_pdl(group_kernel, 1, kGroupThreads, smem, st, idx, nk, E, e_begin, e_end, counts, offsets, perm, inv, active, segs,
                                                   ctrl);
     return cudaGetLastError();
 }

@@ -83,6 +83,7 @@ struct TcCfg {
 
 struct Tile {
     int e;        // expert (routed) or -1 (shared)
+    int le;       // the expert's index in the weight stacks (0 for the shared expert)
     int pos0;     // first row of this tile's tokens in the activation matrix
     int ntok;     // tokens in the tile (1..NT)
     int m0;       // first weight row
@@ -97,6 +98,7 @@ __device__ __forceinline__ Tile decode_tile(int tau, const TcParams& p, int n_ss
     if (tau < n_ssegs * mbs) {
         const int s = tau / mbs, mb = tau - s * mbs;
         t.e = -1;
+        t.le = 0;
         t.pos0 = s * NT;
         t.ntok = min(NT, p.n - t.pos0);
         t.m0 = mb * BM;
@@ -107,6 +109,7 @@ __device__ __forceinline__ Tile decode_tile(int tau, const TcParams& p, int n_ss
         const int s = t2 / mbr, mb = t2 - s * mbr;
         const int32_t* sg = p.segs + 3 * s;
         t.e = sg[0];
+        t.le = sg[0] - p.e_base;
         t.pos0 = sg[1];
         t.ntok = sg[2];
         t.m0 = mb * BM;
@@ -227,7 +230,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         for (int tau = blockIdx.x; tau < n_tiles && !stop && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
             const bool sh = t.e < 0;
-            const int wrow = sh ? t.m0 : t.e * t.out + t.m0;
+            const int wrow = sh ? t.m0 : t.le * t.out + t.m0;
             const int nbox = (t.ntok + 15) >> 4;
             const CUtensorMap* bmap = sh ? &maps.bs : &maps.b;
             const int KB = (t.K + BK - 1) / BK;
@@ -253,7 +256,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                             const int ob = (t.out + 127) >> 7, ib = (t.K + 127) >> 7;
                             const float* sp = reinterpret_cast<const float*>(sh ? p.sh_scale[lane] : p.scale[lane]);
                             ptx::cp_async4(ssc + 4 * lane,
-                                           sp + (size_t)(sh ? 0 : t.e) * ob * ib + (t.m0 >> 7) * ib + (k0 >> 7));
+                                           sp + (size_t)t.le * ob * ib + (t.m0 >> 7) * ib + (k0 >> 7));
                         }
                     } else if (nv_smem_scales) {
                         // Row r's 4 scale bytes of this stage: columns [k0, k0 + 64).
@@ -263,7 +266,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                             for (int q = 0; q < BM / 32; ++q) {
                                 const int r = lane + 32 * q, mrow = t.m0 + r;
                                 const uint8_t* src = (mrow < t.out)
-                                    ? sp + ((size_t)(sh ? 0 : t.e) * t.out + mrow) * (t.K / 16) + k0 / 16
+                                    ? sp + ((size_t)t.le * t.out + mrow) * (t.K / 16) + k0 / 16
                                     : reinterpret_cast<const uint8_t*>(p.zero4);
                                 ptx::cp_async4(ssc + (m * BM + r) * 4, src);
                             }
@@ -377,8 +380,8 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             if constexpr (GU) {
                 float s2g = 1.f, s2u = 1.f;
                 if constexpr (FMT == MOE_W_NVFP4) {
-                    s2g = sh ? p.sh_scale2[0][0] : p.scale2[0][t.e];
-                    s2u = sh ? p.sh_scale2[1][0] : p.scale2[1][t.e];
+                    s2g = sh ? p.sh_scale2[0][0] : p.scale2[0][t.le];
+                    s2u = sh ? p.sh_scale2[1][0] : p.scale2[1][t.le];
                 }
                 uint16_t* dst = reinterpret_cast<uint16_t*>(sh ? p.act_sh_out : p.act_out);
                 for (int j0 = 0; j0 < t.ntok; j0 += 16) {
@@ -407,7 +410,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                 }
             } else {
                 float s2 = 1.f;
-                if constexpr (FMT == MOE_W_NVFP4) s2 = sh ? p.sh_scale2[0][0] : p.scale2[0][t.e];
+                if constexpr (FMT == MOE_W_NVFP4) s2 = sh ? p.sh_scale2[0][0] : p.scale2[0][t.le];
                 float* dst = sh ? p.y_sh : p.y;
                 for (int j0 = 0; j0 < t.ntok; j0 += 16) {
                     float d[16];
@@ -501,7 +504,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                             s1 = e4m3x2_to_f16x2(b1 | (b1 << 8));
                         } else if (mrow < t.out && kc < t.K) {
                             const uint8_t* sc = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]) +
-                                                ((size_t)(sh ? 0 : t.e) * t.out + mrow) * (t.K / 16) + kc / 16;
+                                                ((size_t)t.le * t.out + mrow) * (t.K / 16) + kc / 16;
                             const uint32_t b0 = __ldg(sc), b1 = __ldg(sc + 1);
                             s0 = e4m3x2_to_f16x2(b0 | (b0 << 8));
                             s1 = e4m3x2_to_f16x2(b1 | (b1 << 8));
@@ -648,7 +651,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
 // out[t, h] = bf16( sum_j y[inv[t*k + j], h] (slot order) + y_sh[t, h] ).
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ ysh,
                                                       const int32_t* __restrict__ inv, int n, int H, int k,
-                                                      int has_shared, uint16_t* __restrict__ out) {
+                                                      int has_shared, int accumulate, uint16_t* __restrict__ out) {
     pdl_wait();
     const int C4 = H >> 2;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)n * C4;
@@ -664,6 +667,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         if (has_shared) {
             const float4 v = __ldg(reinterpret_cast<const float4*>(ysh + (size_t)t * H) + c);
             acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        if (accumulate) {
+            const uint2 o = reinterpret_cast<const uint2*>(out + (size_t)t * H)[c];
+            acc.x += __uint_as_float(o.x << 16); acc.y += __uint_as_float(o.x & 0xffff0000u);
+            acc.z += __uint_as_float(o.y << 16); acc.w += __uint_as_float(o.y & 0xffff0000u);
         }
         const uint32_t lo = pack_bf16(acc.x, acc.y), hi = pack_bf16(acc.z, acc.w);
         reinterpret_cast<uint2*>(out + (size_t)t * H)[c] = make_uint2(lo, hi);
@@ -683,8 +691,8 @@ cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const
 }
 
 cudaError_t launch_combine(const float* y, const float* ysh, const int32_t* inv, int n, int H, int k,
-                           int has_shared, uint16_t* out, int num_sms, cudaStream_t st) {
-    launch_pdl(combine_kernel, 2 * num_sms, 256, 0, st, y, ysh, inv, n, H, k, has_shared, out);
+                           int has_shared, int accumulate, uint16_t* out, int num_sms, cudaStream_t st) {
+    launch_pdl(combine_kernel, 2 * num_sms, 256, 0, st, y, ysh, inv, n, H, k, has_shared, accumulate, out);
     return cudaGetLastError();
 }
 
@@ -692,10 +700,19 @@ bool build_tc_maps(int fmt, bool gate_up, const moe_weights_t* w, int E, int H, 
                    int n_routes_max, const void* act_routed, const void* act_shared, TcMaps* maps) {
     // gate_up: routed weights [E*I, H], shared [S, H], B = xs [rows, H] / x(or xh) [n, H]
     // down:    routed weights [E*H, I], shared [H, S], B = as [rows, I] / ash [n, S]
+    // E is the experts the weight stacks hold.  With none (a call that holds
+    // only the shared expert, S > 0) the routed maps repeat the shared ones:
+    // no routed tile exists to use them.
     bool ok = true;
+    if (E == 0 && S == 0) return false;
     if (gate_up) {
-        ok &= weight_map(&maps->w[0], fmt, w->gate.w, E * I, H);
-        ok &= weight_map(&maps->w[1], fmt, w->up.w, E * I, H);
+        if (E > 0) {
+            ok &= weight_map(&maps->w[0], fmt, w->gate.w, E * I, H);
+            ok &= weight_map(&maps->w[1], fmt, w->up.w, E * I, H);
+        } else {
+            ok &= weight_map(&maps->w[0], fmt, w->sh_gate.w, S, H);
+            ok &= weight_map(&maps->w[1], fmt, w->sh_up.w, S, H);
+        }
         if (S > 0) {
             ok &= weight_map(&maps->ws[0], fmt, w->sh_gate.w, S, H);
             ok &= weight_map(&maps->ws[1], fmt, w->sh_up.w, S, H);
@@ -707,7 +724,8 @@ bool build_tc_maps(int fmt, bool gate_up, const moe_weights_t* w, int E, int H, 
         }
         ok &= act_map(&maps->b, fmt, act_routed, n_routes_max, H);
     } else {
-        ok &= weight_map(&maps->w[0], fmt, w->down.w, E * H, I);
+        ok &= (E > 0) ? weight_map(&maps->w[0], fmt, w->down.w, E * H, I)
+                      : weight_map(&maps->w[0], fmt, w->sh_down.w, H, S);
         maps->w[1] = maps->w[0];
         if (S > 0) {
             ok &= weight_map(&maps->ws[0], fmt, w->sh_down.w, H, S);

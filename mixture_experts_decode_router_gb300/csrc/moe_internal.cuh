@@ -33,7 +33,7 @@ constexpr int kTcTokensPerTile = 128;
 
 struct WsLayout {
     size_t ctrl, logits, sg_logit, idx, w, counts, offsets, perm, active, act, act_sh,
-        inv, segs, xs, xh, as, ash, y, ysh, total;
+        inv, segs, xs, xh, as, ash, y, ysh, xe, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -65,11 +65,12 @@ inline WsLayout ws_layout(const moe_config_t& c, int64_t n) {
     L.inv = take(sizeof(int32_t) * n * k);                       // route -> sorted position
     L.segs = take(sizeof(int32_t) * 3 * grouped_segs_bound(n, k, E));
     L.xs = take(sizeof(uint16_t) * n * k * H);                   // expert-sorted activations
-    L.xh = take(sizeof(uint16_t) * n * H);                       // f16 copy of x (NVFP4)
+    L.xh = take(sizeof(uint16_t) * n * H);                       // f16 copy of x (FP8, NVFP4)
     L.as = take(sizeof(uint16_t) * n * k * I);                   // SiLU(g)*u, sorted rows
     L.ash = take(sizeof(uint16_t) * n * (S > 0 ? S : 1));
     L.y = take(sizeof(float) * n * k * H);                       // weighted down rows
     L.ysh = take(sizeof(float) * n * H);
+    L.xe = take(sizeof(uint16_t) * n * H);                       // pre-expert RMSNorm of x
     L.total = off;
     return L;
 }
@@ -82,6 +83,7 @@ struct QMatDev {
     const void* scale;      // FP8: float blocks; NVFP4: E4M3 bytes
     const float* scale2;    // NVFP4 per-expert
     int out_dim, in_dim;
+    int e_base;             // global index of the stack's first expert (expert parallelism)
 };
 
 // ----------------------------------------------------------------------------
@@ -180,7 +182,7 @@ template <> struct WChunk<MOE_W_BF16> {
     uint4 raw;
     __device__ __forceinline__ void load(const QMatDev& m, int e, int row, int c) {
         const uint16_t* base = reinterpret_cast<const uint16_t*>(m.w) +
-                               ((size_t)e * m.out_dim + row) * m.in_dim + (size_t)c * 8;
+                               ((size_t)(e - m.e_base) * m.out_dim + row) * m.in_dim + (size_t)c * 8;
         raw = ld_stream_v4(base);
     }
     __device__ __forceinline__ float scale(const QMatDev&, int, int, int) const { return 1.0f; }
@@ -193,12 +195,12 @@ template <> struct WChunk<MOE_W_BF16> {
 template <> struct WChunk<MOE_W_FP8_B128> {
     uint2 raw;
     __device__ __forceinline__ void load(const QMatDev& m, int e, int row, int c) {
-        const uint8_t* base = m.w + ((size_t)e * m.out_dim + row) * m.in_dim + (size_t)c * 8;
+        const uint8_t* base = m.w + ((size_t)(e - m.e_base) * m.out_dim + row) * m.in_dim + (size_t)c * 8;
         raw = ld_stream_v2(base);
     }
     __device__ __forceinline__ float scale(const QMatDev& m, int e, int row, int c) const {
         const int ob = (m.out_dim + 127) >> 7, ib = (m.in_dim + 127) >> 7;
-        const float* s = reinterpret_cast<const float*>(m.scale) + (size_t)e * ob * ib;
+        const float* s = reinterpret_cast<const float*>(m.scale) + (size_t)(e - m.e_base) * ob * ib;
         return __ldg(s + (row >> 7) * ib + ((c * 8) >> 7));
     }
     __device__ __forceinline__ void decode(float (&v)[8]) const {
@@ -211,12 +213,12 @@ template <> struct WChunk<MOE_W_FP8_B128> {
 template <> struct WChunk<MOE_W_NVFP4> {
     uint32_t raw;
     __device__ __forceinline__ void load(const QMatDev& m, int e, int row, int c) {
-        const uint8_t* base = m.w + ((size_t)e * m.out_dim + row) * (m.in_dim / 2) + (size_t)c * 4;
+        const uint8_t* base = m.w + ((size_t)(e - m.e_base) * m.out_dim + row) * (m.in_dim / 2) + (size_t)c * 4;
         raw = ld_stream_u32(base);
     }
     __device__ __forceinline__ float scale(const QMatDev& m, int e, int row, int c) const {
         const uint8_t* s = reinterpret_cast<const uint8_t*>(m.scale) +
-                           ((size_t)e * m.out_dim + row) * (m.in_dim / 16);
+                           ((size_t)(e - m.e_base) * m.out_dim + row) * (m.in_dim / 16);
         return e4m3_to_float(__ldg(s + (c >> 1)));
     }
     __device__ __forceinline__ void decode(float (&v)[8]) const {
@@ -229,7 +231,7 @@ template <> struct WChunk<MOE_W_NVFP4> {
 // Per-matrix multiplier applied after the row's dot product (NVFP4 scale2).
 template <int FMT>
 __device__ __forceinline__ float matrix_scale(const QMatDev& m, int e) {
-    if constexpr (FMT == MOE_W_NVFP4) return __ldg(m.scale2 + e);
+    if constexpr (FMT == MOE_W_NVFP4) return __ldg(m.scale2 + (e - m.e_base));
     else return 1.0f;
 }
 
@@ -247,5 +249,34 @@ __device__ __forceinline__ float dot8(const float (&a)[8], const float (&b)[8]) 
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// 1 / sqrt(mean(x^2) + eps) of one BF16 row of H elements, by one warp: lane l
+// chains fmaf over its chunks l, l+32, ... in order, then a fixed butterfly.
+// (Generic pointer: the row may be in global or shared memory.)
+__device__ __forceinline__ float rms_inv_warp(const uint16_t* row, int H, float eps, int lane) {
+    float ss = 0.f;
+    for (int c = lane; c < (H >> 3); c += 32) {
+        float v[8];
+        bf16x8_to_float(reinterpret_cast<const uint4*>(row)[c], v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
+    }
+    ss = warp_sum(ss);
+    return rsqrtf(ss / (float)H + eps);
+}
+
+// One 8-element chunk of the normalised row: BF16(x * inv * w), element-wise.
+__device__ __forceinline__ uint4 rms_apply8(uint4 xr, uint4 wr, float inv) {
+    float x[8], w[8];
+    bf16x8_to_float(xr, x);
+    bf16x8_to_float(wr, w);
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn((x[2 * i] * inv) * w[2 * i], (x[2 * i + 1] * inv) * w[2 * i + 1]);
+        o[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
 
 }  // namespace moe

@@ -23,6 +23,8 @@ struct GateUpParams {
 
 struct DownParams {
     int n, H, I, S, k, E;
+    int e_begin, e_end;      // routes to experts outside [e_begin, e_end) contribute nothing
+    int accumulate;          // out = BF16(out + result)
     QMatDev down, sh_down;
     const int32_t* idx;
     const float* w;
@@ -44,6 +46,7 @@ struct TcParams {
     int out_dim, in_dim;     // routed matrix [out, in] per expert
     int sh_out, sh_in;       // shared matrix (sh_out == 0: no shared expert)
     int n, k;
+    int e_base;              // global index of the weight stacks' first expert
     const int32_t* segs;     // [n_rsegs][3] = (expert, first sorted row, tokens)
     const Ctrl* ctrl;
     const void* scale[2];    // routed scales (FP8 fp32 blocks / NVFP4 E4M3 bytes)
@@ -69,13 +72,17 @@ cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const
                           const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, int num_sms,
                           cudaStream_t st);
 cudaError_t launch_combine(const float* y, const float* ysh, const int32_t* inv, int n, int H, int k,
-                           int has_shared, uint16_t* out, int num_sms, cudaStream_t st);
+                           int has_shared, int accumulate, uint16_t* out, int num_sms, cudaStream_t st);
 
 // Fused single-token kernel (moe_fused_n1.cu).
 struct FusedParams {
     const uint16_t* x;
     int H, E, k, I, S, routing, norm;
     float scale;
+    int e_begin, e_end;       // local experts (expert parallelism)
+    int accumulate;           // out = BF16(out + result)
+    const uint16_t* norm_w;   // pre-expert RMSNorm weight or NULL
+    float eps;
     const uint16_t* router;
     const uint16_t* gw;       // shared-gate weight or NULL
     const float* bias;
@@ -90,7 +97,7 @@ struct FusedParams {
     Ctrl* ctrl;
     int rpc;                  // output columns per CTA
     uint32_t row_bytes, drow_bytes, dsh_row_bytes;
-    uint32_t off_x, off_lg, off_sc, off_sel, off_down, off_act, off_bar, smem_bytes;
+    uint32_t off_x, off_xe, off_lg, off_sc, off_sel, off_down, off_act, off_bar, smem_bytes;
 };
 
 bool fused_plan(const moe_config_t* c, int num_sms, FusedParams* p);
@@ -99,11 +106,15 @@ cudaError_t launch_fused_n1(int fmt, const FusedParams& p, int num_sms, cudaStre
 cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, int E,
                           const uint16_t* gw, float* logits, float* sg_logit, int num_sms,
                           cudaStream_t st);
+cudaError_t launch_router_nvfp4(const uint16_t* x, int n, int H, const QMatDev& wq, int E, float* logits,
+                                cudaStream_t st);
 cudaError_t launch_topk(const float* logits, int n, int E, int k, int routing, const float* bias,
                         int norm, float scale, int32_t* idx, float* w, cudaStream_t st);
-cudaError_t launch_group(const int32_t* idx, int nk, int E, int32_t* counts, int32_t* offsets,
-                         int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs, Ctrl* ctrl,
-                         cudaStream_t st);
+cudaError_t launch_group(const int32_t* idx, int nk, int E, int e_begin, int e_end, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
+                         Ctrl* ctrl, cudaStream_t st);
+cudaError_t launch_rmsnorm(const uint16_t* x, int n, int H, const uint16_t* w, float eps, uint16_t* xe,
+                           cudaStream_t st);
 cudaError_t launch_gate_up_tm(int fmt, const GateUpParams& gu, int num_sms, cudaStream_t st);
 cudaError_t launch_down_blend_tm(int fmt, const DownParams& dn, int num_sms, cudaStream_t st);
 

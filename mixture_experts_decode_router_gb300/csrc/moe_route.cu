@@ -135,6 +135,60 @@ router_tiled_kernel(const uint16_t* __restrict__ x, int n, int H,
     pdl_trigger();
 }
 
+// NVFP4 router (the gate_nvfp4 / w4a16_gemm branch of the router step on the
+// page "metrale_model_layers/layers/moe/forward.rs"): the router matrix
+// [E, H] is stored as E2M1 codes with one E4M3 scale per 16 elements and one
+// fp32 scale2, and multiplies BF16 activations.  One warp per router row and
+// RT token rows per blockIdx.y; lane l takes the 8-element chunks l, l+32, ...
+// in order, each chunk's dot product times its block scale chained with fmaf,
+// then the butterfly, then scale2 -- the expert kernels' NVFP4 row arithmetic,
+// identical for every n and grid.
+template <int RT>
+__global__ void __launch_bounds__(256)
+router_nvfp4_kernel(const uint16_t* __restrict__ x, int n, int H, const QMatDev wq, int E,
+                    float* __restrict__ logits) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * (blockDim.x >> 5) + warp;
+    if (r >= E) return;
+    pdl_wait();
+    const int t0 = blockIdx.y * RT;
+    const int C = H >> 3;
+    float acc[RT];
+#pragma unroll
+    for (int b = 0; b < RT; ++b) acc[b] = 0.f;
+#pragma unroll 2
+    for (int c = lane; c < C; c += 32) {
+        WChunk<MOE_W_NVFP4> ch;
+        ch.load(wq, 0, r, c);
+        const float cs = ch.scale(wq, 0, r, c);
+        float wv[8];
+        ch.decode(wv);
+#pragma unroll
+        for (int b = 0; b < RT; ++b) {
+            float xv[8];
+            bf16x8_to_float(__ldg(reinterpret_cast<const uint4*>(x + (size_t)min(t0 + b, n - 1) * H) + c), xv);
+            acc[b] = fmaf(dot8(wv, xv), cs, acc[b]);
+        }
+    }
+    const float s2 = matrix_scale<MOE_W_NVFP4>(wq, 0);
+#pragma unroll
+    for (int b = 0; b < RT; ++b) {
+        const float v = warp_sum(acc[b]) * s2;
+        if (lane == 0 && t0 + b < n) logits[(size_t)(t0 + b) * E + r] = v;
+    }
+    pdl_trigger();
+}
+
+cudaError_t launch_router_nvfp4(const uint16_t* x, int n, int H, const QMatDev& wq, int E, float* logits,
+                                cudaStream_t st) {
+    const int rt = n >= 8 ? 8 : (n >= 4 ? 4 : 1);
+    const dim3 grid((E + 7) / 8, (n + rt - 1) / rt);
+    if (rt == 8) launch_pdl(router_nvfp4_kernel<8>, grid, 256, 0, st, x, n, H, wq, E, logits);
+    else if (rt == 4) launch_pdl(router_nvfp4_kernel<4>, grid, 256, 0, st, x, n, H, wq, E, logits);
+    else launch_pdl(router_nvfp4_kernel<1>, grid, 256, 0, st, x, n, H, wq, E, logits);
+    return cudaGetLastError();
+}
+
 // One CTA per token row.  Selection ranks the fp32 score (softmax: the logit;
 // sigmoid: sigmoid(l) + bias, the bias only selects); every thread ranks its
 // experts against all E scores (rank = experts ahead in score-descending,
@@ -198,6 +252,32 @@ topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int rou
         }
     }
     pdl_trigger();
+}
+
+// The pre-expert RMSNorm ("pre_expert_norm" of MoeLayer::forward, page
+// "metrale_model_layers/layers/moe/forward.rs": it normalises the experts'
+// input, leaving the router's and the shared gate's input unchanged):
+// xe = BF16(x / sqrt(mean(x^2) + eps) * w), one warp per token row.
+__global__ void __launch_bounds__(256)
+rmsnorm_kernel(const uint16_t* __restrict__ x, int n, int H, const uint16_t* __restrict__ w, float eps,
+               uint16_t* __restrict__ xe) {
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+    if (t < n) {
+        const uint16_t* xr = x + (size_t)t * H;
+        const float inv = rms_inv_warp(xr, H, eps, lane);
+        for (int c = lane; c < (H >> 3); c += 32)
+            reinterpret_cast<uint4*>(xe + (size_t)t * H)[c] =
+                rms_apply8(reinterpret_cast<const uint4*>(xr)[c], __ldg(reinterpret_cast<const uint4*>(w) + c), inv);
+    }
+    pdl_trigger();
+}
+
+cudaError_t launch_rmsnorm(const uint16_t* x, int n, int H, const uint16_t* w, float eps, uint16_t* xe,
+                           cudaStream_t st) {
+    launch_pdl(rmsnorm_kernel, dim3((n + 7) / 8), dim3(256), 0, st, x, n, H, w, eps, xe);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, int E,

@@ -47,7 +47,7 @@ FMT_FP8_B128 = "fp8_b128"
 FMT_NVFP4 = "nvfp4"
 
 _TID = {"router": 1, "gate": 2, "up": 3, "down": 4, "sh_gate": 5, "sh_up": 6,
-        "sh_down": 7, "bias": 8, "shared_gate_w": 9, "x": 10, "dup": 11}
+        "sh_down": 7, "bias": 8, "shared_gate_w": 9, "x": 10, "dup": 11, "norm": 12}
 
 
 @dataclass(frozen=True)
@@ -68,6 +68,9 @@ class LayerConfig:
     bias_range: float = 0.1
     weight_std: float = 0.02
     shared_gate: bool = False
+    pre_expert_norm: bool = False      # an RMSNorm weight on the experts' input
+    router_fmt: str = FMT_BF16         # BF16 router, or NVFP4 (quantised from the same matrix)
+    rms_norm_eps: float = 1e-6
     seed: int = 0
 
     def with_(self, **kw) -> "LayerConfig":
@@ -215,11 +218,29 @@ class LayerWeights:
     sh_down: Optional[QMatT]
     correction_bias: Optional[torch.Tensor]  # fp32 [E]
     shared_gate_w: Optional[torch.Tensor]    # bf16 [H]
+    pre_expert_norm_w: Optional[torch.Tensor] = None   # bf16 [H]
+    router_q: Optional[QMatT] = None                   # NVFP4 router [1, E, H]
+
+
+def _router_fp32(cfg: LayerConfig, device) -> torch.Tensor:
+    return torch.randn(cfg.num_experts, cfg.hidden, generator=_gen(device, cfg.seed, "router"),
+                       device=device) * cfg.weight_std
 
 
 def make_router(cfg: LayerConfig, device="cpu") -> torch.Tensor:
-    return (torch.randn(cfg.num_experts, cfg.hidden, generator=_gen(device, cfg.seed, "router"),
-                        device=device) * cfg.weight_std).to(torch.bfloat16)
+    return _router_fp32(cfg, device).to(torch.bfloat16)
+
+
+def make_router_q(cfg: LayerConfig, device="cpu") -> Optional[QMatT]:
+    """The NVFP4 router (one matrix [E, H], stacked as [1, E, H]) quantised from
+    the BF16 router's fp32 draw, or None for a BF16 router."""
+    if cfg.router_fmt == FMT_BF16:
+        return None
+    if cfg.router_fmt != FMT_NVFP4:
+        raise ValueError(cfg.router_fmt)
+    q, sc, s2 = _quant_nvfp4(_router_fp32(cfg, device))
+    return QMatT(FMT_NVFP4, q[None].contiguous(), sc[None].contiguous(),
+                 torch.tensor([s2], dtype=torch.float32, device=device))
 
 
 def make_bias(cfg: LayerConfig, device="cpu") -> Optional[torch.Tensor]:
@@ -249,7 +270,27 @@ def make_weights(cfg: LayerConfig, device="cpu") -> LayerWeights:
     else:
         sh_gate = sh_up = sh_down = None
     return LayerWeights(cfg, router, gate, up, down, sh_gate, sh_up, sh_down,
-                        make_bias(cfg, device), make_shared_gate_w(cfg, device))
+                        make_bias(cfg, device), make_shared_gate_w(cfg, device),
+                        make_norm_w(cfg, device), make_router_q(cfg, device))
+
+
+def make_norm_w(cfg: LayerConfig, device="cpu") -> Optional[torch.Tensor]:
+    """RMSNorm weight, BF16 [H]: 1 + 0.1 * N(0, 1), the spread of a trained
+    norm's gains around one."""
+    if not cfg.pre_expert_norm:
+        return None
+    z = torch.randn(cfg.hidden, generator=_gen(device, cfg.seed, "norm"), device=device)
+    return (1.0 + 0.1 * z).to(torch.bfloat16)
+
+
+def expert_slice(lw: LayerWeights, begin: int, end: int) -> LayerWeights:
+    """The routed experts [begin, end) of a layer, as one expert-parallel rank
+    holds them (views of the full stacks; the shared expert and router kept)."""
+    def part(q: QMatT) -> QMatT:
+        return QMatT(q.fmt, q.w[begin:end],
+                     q.scale[begin:end] if q.scale is not None else None,
+                     q.scale2[begin:end] if q.scale2 is not None else None)
+    return replace(lw, gate=part(lw.gate), up=part(lw.up), down=part(lw.down))
 
 
 GapFn = Callable[[np.ndarray], np.ndarray]

@@ -54,14 +54,18 @@ def oracle_layer(lw: LayerWeights) -> O.OracleLayer:
         sh_up=host_qmat(lw.sh_up) if lw.sh_up is not None else None,
         sh_down=host_qmat(lw.sh_down) if lw.sh_down is not None else None,
         correction_bias=lw.correction_bias.cpu().numpy() if lw.correction_bias is not None else None,
-        shared_gate_w=bf16_bits(lw.shared_gate_w) if lw.shared_gate_w is not None else None)
+        shared_gate_w=bf16_bits(lw.shared_gate_w) if lw.shared_gate_w is not None else None,
+        pre_expert_norm_w=(bf16_bits(lw.pre_expert_norm_w) if lw.pre_expert_norm_w is not None
+                           else None),
+        rms_norm_eps=c.rms_norm_eps,
+        router_q=host_qmat(lw.router_q) if lw.router_q is not None else None)
 
 
 def gap_fn_for(layer: O.OracleLayer):
     """Per-row margin between the k-th and (k+1)-th selection score (fp64)."""
     def fn(x_bits: np.ndarray) -> np.ndarray:
         x = O.bf16_decode(x_bits)
-        lg = O.router_logits(x, layer.router_w)
+        lg = O.router_logits(x, O.router_weights(layer))
         return O.topk_gap(O.selection_scores(lg, layer.routing, layer.correction_bias),
                           layer.top_k)
     return fn

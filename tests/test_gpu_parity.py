@@ -9,6 +9,8 @@
   <= 5e-2 * RMS(oracle) for NVFP4.
 * Batch invariance: a row's output bits do not depend on which rows share the
   call (computed alone, permuted, duplicated).
+* Expert parallelism: each rank's partial against the oracle's, and the
+  partials summed (plus one shared-expert-only call) against the whole layer.
 """
 
 import numpy as np
@@ -53,7 +55,7 @@ def _check(cfg, n=None, path="auto", rows=None, x=None, lw=None):
     torch.cuda.synchronize()
     xb = bf16_bits(x)
     # Routing for every row (cheap), the layer output for `rows`.
-    lg_ref = O.router_logits(O.bf16_decode(xb), L.router_w)
+    lg_ref = O.router_logits(O.bf16_decode(xb), O.router_weights(L))
     idx_ref, w_ref = O.route(lg_ref, L.routing, L.top_k, L.norm_topk_prob,
                              L.routed_scaling_factor, L.correction_bias)
     assert np.array_equal(idx.cpu().numpy(), idx_ref), "expert indices differ"
@@ -85,6 +87,15 @@ SMALL_CASES = [
     small("all_experts", top_k=8, num_experts=8),
     small("wide_E", num_experts=1024, top_k=32, hidden=128, inter=64, shared_inter=64),
     small("E33", num_experts=33, top_k=6, routing=synth.ROUTE_SIGMOID_BIAS),
+    small("pre_norm", pre_expert_norm=True, shared_gate=True, routing=synth.ROUTE_SIGMOID_BIAS,
+          top_k=3, routed_scaling_factor=2.5),
+    small("pre_norm_fp8", expert_fmt=synth.FMT_FP8_B128, pre_expert_norm=True, rms_norm_eps=1e-5),
+    small("pre_norm_nvfp4", expert_fmt=synth.FMT_NVFP4, pre_expert_norm=True, num_experts=40,
+          top_k=5, hidden=352),
+    small("router_nvfp4", router_fmt=synth.FMT_NVFP4, routing=synth.ROUTE_SIGMOID_BIAS,
+          shared_gate=True, top_k=4, num_experts=32, routed_scaling_factor=2.5),
+    small("router_nvfp4_fp8", router_fmt=synth.FMT_NVFP4, expert_fmt=synth.FMT_FP8_B128,
+          hidden=288, num_experts=24, top_k=3),
 ]
 
 
@@ -111,16 +122,18 @@ def test_all_tokens_on_one_expert():
     _check(cfg, 33, x=x, lw=lw)
 
 
-def test_route_and_experts_entry_points():
+@pytest.mark.parametrize("norm,router", [(False, synth.FMT_BF16), (True, synth.FMT_BF16),
+                                         (False, synth.FMT_NVFP4)])
+def test_route_and_experts_entry_points(norm, router):
     cfg = small("split", routing=synth.ROUTE_SIGMOID_BIAS, top_k=3, routed_scaling_factor=2.5,
-                shared_gate=True)
+                shared_gate=True, pre_expert_norm=norm, router_fmt=router)
     lw = synth.make_weights(cfg, "cuda")
     L = oracle_layer(lw)
     x = synth.make_input(cfg, 9, "cuda", gap_fn=gap_fn_for(L))
     layer = MoeLayer(lw, 9)
     idx, w, lg = layer.route(x)
     torch.cuda.synchronize()
-    lg_ref = O.router_logits(O.bf16_decode(bf16_bits(x)), L.router_w)
+    lg_ref = O.router_logits(O.bf16_decode(bf16_bits(x)), O.router_weights(L))
     rms = np.sqrt(np.mean(lg_ref ** 2))
     assert np.max(np.abs(lg.cpu().numpy() - lg_ref)) <= 1e-4 * rms
     # moe_experts on the oracle's routing (as int32/fp32), then against the oracle output.
@@ -129,11 +142,13 @@ def test_route_and_experts_entry_points():
     out = layer.experts(x, torch.from_numpy(idx_ref.astype(np.int32)).cuda(),
                         torch.from_numpy(w_ref.astype(np.float32)).cuda())
     fwd, _, _ = layer.forward(x)
+    # On the library's own routing, moe_route + moe_experts is moe_forward bit for bit.
+    own = layer.experts(x, idx, w)
     torch.cuda.synchronize()
     ref, _, _, _ = O.moe_forward(L, bf16_bits(x))
     rms_o = np.sqrt(np.mean(ref ** 2))
     assert np.max(np.abs(out.float().cpu().numpy() - ref)) <= 2e-2 * rms_o
-    assert torch.equal(out, fwd)
+    assert torch.equal(own, fwd)
 
 
 def test_zero_tokens_is_a_noop():
@@ -146,12 +161,14 @@ def test_zero_tokens_is_a_noop():
     assert out.shape == (0, cfg.hidden)
 
 
+@pytest.mark.parametrize("norm", [False, True])
 @pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_FP8_B128, synth.FMT_NVFP4])
-def test_rows_do_not_depend_on_the_batch_token_major(fmt):
+def test_rows_do_not_depend_on_the_batch_token_major(fmt, norm):
     """The token-major kernels (forced), and one token alone: the single-token
-    kernel, which keeps the token-major arithmetic."""
+    kernel, which keeps the token-major arithmetic (the RMSNorm included)."""
     cfg = small("invariance", expert_fmt=fmt, num_experts=32, top_k=4,
-                routing=synth.ROUTE_SIGMOID_BIAS, routed_scaling_factor=2.5)
+                routing=synth.ROUTE_SIGMOID_BIAS, routed_scaling_factor=2.5,
+                pre_expert_norm=norm)
     lw = synth.make_weights(cfg, "cuda")
     L = oracle_layer(lw)
     x = synth.make_input(cfg, 12, "cuda", gap_fn=gap_fn_for(L))
@@ -167,11 +184,13 @@ def test_rows_do_not_depend_on_the_batch_token_major(fmt):
     assert torch.equal(dup[12:], full[:4])
 
 
+@pytest.mark.parametrize("norm", [False, True])
 @pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_FP8_B128, synth.FMT_NVFP4])
-def test_rows_do_not_depend_on_the_batch_grouped(fmt):
+def test_rows_do_not_depend_on_the_batch_grouped(fmt, norm):
     """N >= 4: the expert-grouped tensor-core path."""
     cfg = small("invariance_g", expert_fmt=fmt, num_experts=32, top_k=4,
-                routing=synth.ROUTE_SIGMOID_BIAS, routed_scaling_factor=2.5)
+                routing=synth.ROUTE_SIGMOID_BIAS, routed_scaling_factor=2.5,
+                pre_expert_norm=norm)
     lw = synth.make_weights(cfg, "cuda")
     L = oracle_layer(lw)
     x = synth.make_input(cfg, 40, "cuda", gap_fn=gap_fn_for(L))
@@ -187,6 +206,160 @@ def test_rows_do_not_depend_on_the_batch_grouped(fmt):
     assert torch.equal(many[-40:], full)
 
 
+# ---------------------------------------------------------------- expert parallelism
+
+def _ep_check(cfg, n, ranges, path="auto", rows=None):
+    """Each rank's partial (its experts only, no shared expert) against the
+    oracle's partial; the partials summed plus one shared-expert-only call
+    against the whole layer.  Routing is the same on every rank.
+
+    A partial is a sparse, heavy-tailed matrix (rows with no local route are
+    exactly zero), so its RMS is small next to its largest entries and the
+    BF16 rounding of the output alone (up to 2^-9 of an entry) can exceed
+    tol * RMS.  The bound is therefore tol * RMS (over the rows with a local
+    route) plus 2^-8 of each oracle entry; for the sum, plus 2^-8 of the sum of
+    the partials' magnitudes (each partial and the sum are BF16)."""
+    lw = synth.make_weights(cfg, "cuda")
+    L = oracle_layer(lw)
+    x = synth.make_input(cfg, n, "cuda", gap_fn=gap_fn_for(L))
+    xb = bf16_bits(x)
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    tol = tolerance(cfg.expert_fmt)
+    full_ref, idx_ref, _, _ = O.moe_forward(L, xb, rows=rows)
+    total = torch.zeros(n, cfg.hidden, dtype=torch.float32, device="cuda")
+    mag = np.zeros_like(full_ref)          # sum over ranks of |oracle partial|
+    idx0 = None
+    for (b, e) in ranges:
+        layer = MoeLayer(synth.expert_slice(lw, b, e), n, path, experts=(b, e),
+                         exclude_shared=True)
+        out, idx, _ = layer.forward(x)
+        torch.cuda.synchronize()
+        assert layer.device_error() == 0
+        if idx0 is None:
+            idx0 = idx.clone()
+        assert torch.equal(idx, idx0), "routing differs between ranks"
+        ref, _, _, _ = O.moe_forward(L, xb, rows=rows, experts=(b, e), include_shared=False)
+        got = out.float().cpu().numpy()[rows]
+        live = np.any(ref != 0, axis=1)                    # rows with a route to this rank
+        assert not np.any(got[~live]), f"rank [{b}, {e}): non-zeros in rows it does not serve"
+        if np.any(live):
+            rms = float(np.sqrt(np.mean(ref[live] ** 2)))
+            bound = tol * rms + 2.0 ** -8 * np.abs(ref)
+            assert np.all(np.abs(got - ref) <= bound), \
+                f"rank [{b}, {e}): max excess {float(np.max(np.abs(got - ref) - bound)):.3e}"
+        mag += np.abs(ref)
+        total += out.float()
+    assert np.array_equal(idx0.cpu().numpy()[rows], idx_ref)
+    # The all-reduce's result: the partials summed, in BF16.
+    reduced = total.to(torch.bfloat16)
+    if cfg.shared_inter > 0:
+        E = cfg.num_experts
+        none = synth.expert_slice(lw, E, E)
+        sh = MoeLayer(none, n, path, experts=(E, E))
+        out, _, _ = sh.forward(x)                  # the shared expert alone (routing computed)
+        torch.cuda.synchronize()
+        ref, _, _, _ = O.moe_forward(L, xb, rows=rows, experts=(E, E))
+        rms = float(np.sqrt(np.mean(ref ** 2)))
+        assert np.max(np.abs(out.float().cpu().numpy()[rows] - ref)) <= tol * rms, "shared only"
+        # Added once into the reduced output (routing skipped, then computed:
+        # the same bits).
+        add = MoeLayer(none, n, path, experts=(E, E), accumulate=True)
+        again = reduced.clone()
+        add.forward(x, out=reduced, routing=False)
+        add.forward(x, out=again)
+        torch.cuda.synchronize()
+        assert add.device_error() == 0
+        assert torch.equal(reduced, again)
+    rms = float(np.sqrt(np.mean(full_ref ** 2)))
+    diff = np.abs(reduced.float().cpu().numpy()[rows] - full_ref)
+    bound = tol * rms + 2.0 ** -8 * (mag + np.abs(full_ref))
+    assert np.all(diff <= bound), \
+        f"reduced partials + shared: max excess {float(np.max(diff - bound)):.3e} (RMS {rms:.3e})"
+
+
+_EP_RANGES = [[(0, 8), (8, 16), (16, 24), (24, 32)], [(0, 5), (5, 21), (21, 32)]]
+
+
+@pytest.mark.parametrize("ranges", _EP_RANGES, ids=["even4", "uneven3"])
+@pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_FP8_B128, synth.FMT_NVFP4])
+@pytest.mark.parametrize("n", [1, 3, 16, 40])
+def test_expert_parallel_partials(fmt, n, ranges):
+    cfg = small(f"ep_{fmt}", expert_fmt=fmt, num_experts=32, top_k=4,
+                routing=synth.ROUTE_SIGMOID_BIAS, routed_scaling_factor=2.5, shared_gate=True,
+                pre_expert_norm=(n == 16))
+    _ep_check(cfg, n, ranges)
+
+
+@pytest.mark.parametrize("path", ["token_major", "grouped"])
+def test_expert_parallel_forced_paths(path):
+    cfg = small("ep_paths", num_experts=32, top_k=4, routing=synth.ROUTE_SIGMOID_BIAS,
+                routed_scaling_factor=2.5)
+    for n in (1, 17):
+        _ep_check(cfg, n, _EP_RANGES[1], path=path)
+
+
+def test_expert_parallel_no_shared_expert_and_empty_rank():
+    """No shared expert: a rank that holds no expert at all writes zeros."""
+    cfg = small("ep_noshared", shared_inter=0, num_experts=16, top_k=2)
+    lw = synth.make_weights(cfg, "cuda")
+    x = synth.make_input(cfg, 20, "cuda", gap_fn=gap_fn_for(oracle_layer(lw)))
+    for n in (1, 2, 20):
+        layer = MoeLayer(synth.expert_slice(lw, 16, 16), n, experts=(16, 16))
+        out, _, _ = layer.forward(x[:n], out=torch.full((n, cfg.hidden), 3.0, dtype=torch.bfloat16,
+                                                         device="cuda"))
+        torch.cuda.synchronize()
+        assert int(out.count_nonzero()) == 0
+    _ep_check(cfg, 20, [(0, 3), (3, 16)])
+
+
+def test_accumulate_adds_into_out():
+    """accumulate = 1 on a whole layer: BF16(out + layer) on every path."""
+    cfg = small("acc", num_experts=32, top_k=4, routing=synth.ROUTE_SIGMOID_BIAS,
+                routed_scaling_factor=2.5, shared_gate=True)
+    lw = synth.make_weights(cfg, "cuda")
+    L = oracle_layer(lw)
+    x = synth.make_input(cfg, 40, "cuda", gap_fn=gap_fn_for(L))
+    for n in (1, 3, 40):
+        base = synth.make_input(cfg.with_(seed=5), n, "cuda")
+        plain, _, _ = MoeLayer(lw, n).forward(x[:n])
+        got = base.clone()
+        MoeLayer(lw, n, accumulate=True).forward(x[:n], out=got)
+        torch.cuda.synchronize()
+        ref, _, _, _ = O.moe_forward(L, bf16_bits(x[:n]))
+        ref = ref + base.float().cpu().numpy()
+        rms = float(np.sqrt(np.mean(ref ** 2)))
+        assert np.max(np.abs(got.float().cpu().numpy() - ref)) <= 2e-2 * rms
+        # Within one BF16 rounding of the two-step sum.
+        atol = float(plain.float().abs().max()) * 2 ** -8 + 1e-6
+        assert torch.allclose(got.float(), base.float() + plain.float(), rtol=2 ** -8, atol=atol)
+
+
+def test_expert_parallel_driver_single_rank():
+    """Without a process group the driver is the whole layer: the partial of
+    all experts, then the shared expert added."""
+    from mixture_experts_decode_router_gb300.ep import ExpertParallelMoe
+    cfg = small("ep_driver", num_experts=32, top_k=4, routing=synth.ROUTE_SIGMOID_BIAS,
+                routed_scaling_factor=2.5, shared_gate=True, pre_expert_norm=True)
+    lw = synth.make_weights(cfg, "cuda")
+    L = oracle_layer(lw)
+    x = synth.make_input(cfg, 16, "cuda", gap_fn=gap_fn_for(L))
+    for n in (1, 16):
+        got = ExpertParallelMoe(lw, n, 0, 1).forward(x[:n])
+        torch.cuda.synchronize()
+        ref, _, _, _ = O.moe_forward(L, bf16_bits(x[:n]))
+        part, _, _, _ = O.moe_forward(L, bf16_bits(x[:n]), include_shared=False)
+        rms = float(np.sqrt(np.mean(ref ** 2)))
+        # Two BF16 roundings: the partial, then the sum with the shared expert.
+        bound = 2e-2 * rms + 2.0 ** -8 * (np.abs(part) + np.abs(ref))
+        assert np.all(np.abs(got.float().cpu().numpy() - ref) <= bound)
+
+
+def test_expert_parallel_full_size():
+    """decode_n16 over 8 ranks of 32 experts each, with the pre-expert norm."""
+    cfg = synth.WORKLOADS["decode_n16"].with_(pre_expert_norm=True)
+    _ep_check(cfg, 16, [(32 * r, 32 * r + 32) for r in range(8)], rows=[0, 5, 11, 15])
+
+
 # ---------------------------------------------------------------- the five workloads at full size
 
 @pytest.mark.parametrize("name,rows", [
@@ -199,6 +372,16 @@ def test_rows_do_not_depend_on_the_batch_grouped(fmt):
 def test_workloads_full_size(name, rows):
     cfg = synth.WORKLOADS[name]
     _check(cfg, rows=rows)
+
+
+@pytest.mark.parametrize("name,rows", [
+    ("decode_n1", None),
+    ("decode_n16", None),
+    ("nvfp4_n256", list(range(3, 256, 16)) + [254]),
+])
+def test_nvfp4_router_full_size(name, rows):
+    """The NVFP4 router on the full-size layers (one token: token-major)."""
+    _check(synth.WORKLOADS[name].with_(router_fmt=synth.FMT_NVFP4), rows=rows)
 
 
 # ---------------------------------------------------------------- device error word
