@@ -266,7 +266,7 @@ moe_status_t moe_forward_static_ws(const moe_config_t* cfg, const moe_weights_t*
  * non-zero), so the workspace serves the next call.  Synchronises `stream`
  * (the only entry point that does).
  *   device_error (out)  0: no failure since the last check; 11-16: a bounded
- *                       wait of the single-token kernel gave up; 1-4: a bounded
+ *                       wait of the single-token kernel gave up; 1-5: a bounded
  *                       wait of the grouped tensor-core kernels gave up; 20: the
  *                       workspace control block was not zeroed before use.
  * Errors: MOE_ERR_NULL, MOE_ERR_ALIGNMENT, MOE_ERR_WORKSPACE (ws_bytes < 256),

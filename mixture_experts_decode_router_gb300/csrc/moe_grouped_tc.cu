@@ -63,7 +63,10 @@ struct TcCfg {
     static constexpr int kAccCols = kMats * NT;
     static constexpr int kTmemCols = 2 * kAccCols;
     static constexpr int kDeqWarps = kDeq ? 8 : 0;
-    static constexpr int kThreads = (6 + kDeqWarps) * 32;
+    // Dequantised tiles: a second producer warp for the token (B) tiles, after
+    // the dequant warps, so a full B ring never holds up the weight copies.
+    static constexpr int kBWarp = 6 + kDeqWarps;
+    static constexpr int kThreads = (6 + kDeqWarps + (kDeq ? 1 : 0)) * 32;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kAStages * kAStage;
     static constexpr int kOffRaw = kOffB + kBStages * kBStage;
@@ -136,16 +139,33 @@ __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
     return d;
 }
 
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-    uint32_t h2;
-    asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h2) : "r"(byte));
-    return h2;
-}
-
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
     uint32_t h2;
     asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(two));
     return h2;
+}
+
+// The four bytes of w, each a pair of E2M1 codes (the even element in the low
+// nibble), as four f16x2: byte b -> h[b], exact.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&h)[4]) {
+    asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3; }"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
+// The two 16-bit halves of w, each a pair of E4M3 codes, as two f16x2.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t (&h)[2]) {
+    asm("{ .reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi; }"
+        : "=r"(h[0]), "=r"(h[1])
+        : "r"(w));
 }
 
 __device__ __forceinline__ float2 f16x2_to_float2(uint32_t h2) {
@@ -273,17 +293,6 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                         }
                     }
                     ptx::cp_async_mbar_arrive(&raw_full[rs]);
-                    const int bs = it % C::kBStages;
-                    if (!ptx::mbar_wait_warp(&b_empty[bs], ((it / C::kBStages) & 1) ^ 1, s_abort, err, 1)) {
-                        stop = true;
-                        break;
-                    }
-                    if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(&b_full[bs], nbox * 2048);
-                        for (int j = 0; j < nbox; ++j)
-                            ptx::tma_load_2d(sB + bs * C::kBStage + j * 2048, bmap, k0, t.pos0 + 16 * j,
-                                             &b_full[bs]);
-                    }
                 } else {
                     const int as = it % C::kAStages;
                     if (!ptx::mbar_wait_warp(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 1)) {
@@ -306,17 +315,40 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         if (lane == 0 && *s_abort) {
             // Let every copy this warp issued land before the CTA exits:
             // wait (bounded) on the last phase of each ring stage it used.
-            constexpr uint32_t kRing = C::kDeq ? C::kBStages : C::kAStages;
+            constexpr uint32_t kRing = C::kDeq ? C::kRawStages : C::kAStages;
             const uint32_t na = it < kRing ? it : kRing;
             for (uint32_t q = 0; q < na; ++q) {
                 const uint32_t i2 = it - 1 - q, s2 = i2 % kRing;
-                ptx::mbar_wait_quiet(C::kDeq ? &b_full[s2] : &a_full[s2], (i2 / kRing) & 1, 100000000ull);
+                ptx::mbar_wait_quiet(C::kDeq ? &raw_full[s2] : &a_full[s2], (i2 / kRing) & 1, 100000000ull);
             }
-            if constexpr (C::kDeq) {
-                const uint32_t nr = it < (uint32_t)C::kRawStages ? it : C::kRawStages;
-                for (uint32_t q = 0; q < nr; ++q) {
-                    const uint32_t i2 = it - 1 - q, s2 = i2 % C::kRawStages;
-                    ptx::mbar_wait_quiet(&raw_full[s2], (i2 / C::kRawStages) & 1, 100000000ull);
+        }
+    } else if (C::kDeq && warp == C::kBWarp) {
+        // ------------------------------------------------------------ token-tile producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool stop = false;
+            for (int tau = blockIdx.x; tau < n_tiles && !stop && !*s_abort; tau += gridDim.x) {
+                const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
+                const int nbox = (t.ntok + 15) >> 4;
+                const CUtensorMap* bmap = t.e < 0 ? &maps.bs : &maps.b;
+                const int KB = (t.K + BK - 1) / BK;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int bs = it % C::kBStages;
+                    if (!ptx::mbar_wait(&b_empty[bs], ((it / C::kBStages) & 1) ^ 1, s_abort, err, 5)) {
+                        stop = true;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&b_full[bs], nbox * 2048);
+                    for (int j = 0; j < nbox; ++j)
+                        ptx::tma_load_2d(sB + bs * C::kBStage + j * 2048, bmap, kb * BK, t.pos0 + 16 * j,
+                                         &b_full[bs]);
+                }
+            }
+            if (*s_abort) {
+                const uint32_t nb = it < (uint32_t)C::kBStages ? it : C::kBStages;
+                for (uint32_t q = 0; q < nb; ++q) {
+                    const uint32_t i2 = it - 1 - q, s2 = i2 % C::kBStages;
+                    ptx::mbar_wait_quiet(&b_full[s2], (i2 / C::kBStages) & 1, 100000000ull);
                 }
             }
         }
@@ -438,8 +470,10 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
     } else if constexpr (C::kDeq) {
         // ------------------------------------------------------------ dequant
-        const int dt = threadIdx.x - 6 * 32;        // 0 .. 255
-        const int dwarp = dt >> 5;
+        // Each matrix of a stage is 128 rows x 64 codes = 512 chunks of 16
+        // codes; dequant thread dt takes chunks dt, dt + D, ... (D = threads).
+        constexpr int kDT = C::kDeqWarps * 32;
+        const int dt = threadIdx.x - 6 * 32;
         uint32_t it = 0;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
@@ -464,17 +498,18 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                         const __half2 s2 = __float2half2_rn(s);
                         const uint32_t s2u = *reinterpret_cast<const uint32_t*>(&s2);
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            const int qd = dt + 256 * c;           // 512 chunks of 16 codes
-                            const int r = qd >> 2, ch = qd & 3;
+                        for (int qd = dt; qd < 512; qd += kDT) {
+                            const int r = qd >> 2, ch = qd & 3;    // row, 16-byte chunk of codes
                             const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 64 + ch * 16);
                             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
                             uint32_t o[8];
                             if (f16_scale) {
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
-                                    o[2 * i] = f16x2_mul(e4m3x2_to_f16x2(w4[i] & 0xffffu), s2u);
-                                    o[2 * i + 1] = f16x2_mul(e4m3x2_to_f16x2(w4[i] >> 16), s2u);
+                                    uint32_t h[2];
+                                    e4m3x4_to_f16x2x2(w4[i], h);
+                                    o[2 * i] = f16x2_mul(h[0], s2u);
+                                    o[2 * i + 1] = f16x2_mul(h[1], s2u);
                                 }
                             } else {
 #pragma unroll
@@ -490,39 +525,37 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                             st_shared_v4(rowb + (((2 * ch + 1) ^ (r & 7)) << 4), o[4], o[5], o[6], o[7]);
                         }
                     } else {
-                        // NVFP4: 256 chunks of 32 codes (16 bytes), one per thread.
-                        const int r = dt >> 1, ch = dt & 1;
-                        const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 32 + ch * 16);
-                        const int kc = k0 + 32 * ch;
-                        const int mrow = t.m0 + r;
-                        uint32_t s0 = 0, s1 = 0;   // f16x2 of the two block scales (0 outside the matrix)
-                        if (t.K % 64 == 0) {
-                            // Fetched into shared memory with the codes (0 past the last row).
-                            const uint32_t w = reinterpret_cast<const uint32_t*>(sScale + rs * C::kScaleStage)[m * BM + r];
-                            const uint32_t b0 = (w >> (16 * ch)) & 0xffu, b1 = (w >> (16 * ch + 8)) & 0xffu;
-                            s0 = e4m3x2_to_f16x2(b0 | (b0 << 8));
-                            s1 = e4m3x2_to_f16x2(b1 | (b1 << 8));
-                        } else if (mrow < t.out && kc < t.K) {
-                            const uint8_t* sc = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]) +
-                                                ((size_t)t.le * t.out + mrow) * (t.K / 16) + kc / 16;
-                            const uint32_t b0 = __ldg(sc), b1 = __ldg(sc + 1);
-                            s0 = e4m3x2_to_f16x2(b0 | (b0 << 8));
-                            s1 = e4m3x2_to_f16x2(b1 | (b1 << 8));
+                        // NVFP4: a chunk is one 16-code scale block (8 bytes).
+#pragma unroll
+                        for (int qd = dt; qd < 512; qd += kDT) {
+                            const int r = qd >> 2, q = qd & 3;     // row, scale block of the stage
+                            const uint2 v = *reinterpret_cast<const uint2*>(raw + r * 32 + q * 8);
+                            const int kc = k0 + 16 * q;
+                            const int mrow = t.m0 + r;
+                            uint32_t sc = 0;   // f16x2 of the block scale (0 outside the matrix)
+                            if (t.K % 64 == 0) {
+                                // Fetched into shared memory with the codes (0 past the last row).
+                                const uint32_t w = reinterpret_cast<const uint32_t*>(sScale + rs * C::kScaleStage)[m * BM + r];
+                                const uint32_t b = (w >> (8 * q)) & 0xffu;
+                                sc = e4m3x2_to_f16x2(b | (b << 8));
+                            } else if (mrow < t.out && kc < t.K) {
+                                const uint8_t* sp = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]) +
+                                                    ((size_t)t.le * t.out + mrow) * (t.K / 16) + kc / 16;
+                                const uint32_t b = __ldg(sp);
+                                sc = e4m3x2_to_f16x2(b | (b << 8));
+                            }
+                            uint32_t lo[4], hi[4];
+                            e2m1x8_to_f16x2x4(v.x, lo);
+                            e2m1x8_to_f16x2x4(v.y, hi);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                lo[i] = f16x2_mul(lo[i], sc);
+                                hi[i] = f16x2_mul(hi[i], sc);
+                            }
+                            const uint32_t rowb = a_mat + r * 128;
+                            st_shared_v4(rowb + (((2 * q) ^ (r & 7)) << 4), lo[0], lo[1], lo[2], lo[3]);
+                            st_shared_v4(rowb + (((2 * q + 1) ^ (r & 7)) << 4), hi[0], hi[1], hi[2], hi[3]);
                         }
-                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                        uint32_t o[16];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint32_t sc2 = (i < 2) ? s0 : s1;
-#pragma unroll
-                            for (int b = 0; b < 4; ++b)
-                                o[4 * i + b] = f16x2_mul(e2m1x2_to_f16x2((w4[i] >> (8 * b)) & 0xffu), sc2);
-                        }
-                        const uint32_t rowb = a_mat + r * 128;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            st_shared_v4(rowb + (((4 * ch + i) ^ (r & 7)) << 4), o[4 * i], o[4 * i + 1],
-                                         o[4 * i + 2], o[4 * i + 3]);
                     }
                 }
                 ptx::fence_proxy_async_smem();
@@ -534,7 +567,6 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             }
             if (!ok) break;
         }
-        (void)dwarp;
     }
 
     pdl_trigger();
