@@ -20,14 +20,15 @@
 // The tile's M dimension is 128 weight rows and its N dimension the expert's
 // tokens (padded to a multiple of 16), so a thin token set still fills the
 // MMA.  Weights: BF16 arrive by TMA straight in the 128-byte swizzled K-major
-// layout the MMA reads; FP8 and NVFP4 arrive raw by TMA and eight dequant warps
-// rewrite them as f16 in that layout (FP8: RNE_f16(e4m3 * block scale), one
-// rounding with an 11-bit significand; NVFP4: e2m1 * e4m3 scale, exact in f16,
-// with the fp32 scale2 applied to the accumulator).  Those tiles run the f16
-// MMA with f16 activations (exact for BF16 inputs in f16's normal range,
-// saturated at +-65504).  Warp roles: 0 TMA producer, 1 MMA issuer (one
-// thread) and TMEM owner, 2-5 epilogue (TMEM -> registers -> global), 6-13
-// dequant.
+// layout the MMA reads; FP8 and NVFP4 arrive raw by TMA and dequant warps
+// (8 for FP8, 16 for NVFP4) rewrite them as f16 in that layout (FP8:
+// RNE_f16(e4m3 * block scale), one rounding with an 11-bit significand; NVFP4:
+// e2m1 * e4m3 scale, exact in f16, with the fp32 scale2 applied to the
+// accumulator).  Those tiles run the f16 MMA with f16 activations (exact for
+// BF16 inputs in f16's normal range, saturated at +-65504).  Warp roles: 0 TMA
+// producer of the weight codes (and block scales), 1 MMA issuer (one thread)
+// and TMEM owner, 2-5 epilogue (TMEM -> registers -> global), then the dequant
+// warps, then (dequantised formats) the TMA producer of the token tiles.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -62,7 +63,7 @@ struct TcCfg {
     static constexpr int kRawStages = !kDeq ? 0 : (GU ? (FMT == MOE_W_FP8_B128 ? 4 : 6) : 8);
     static constexpr int kAccCols = kMats * NT;
     static constexpr int kTmemCols = 2 * kAccCols;
-    static constexpr int kDeqWarps = kDeq ? 8 : 0;
+    static constexpr int kDeqWarps = kDeq ? (FMT == MOE_W_NVFP4 ? 16 : 8) : 0;
     // Dequantised tiles: a second producer warp for the token (B) tiles, after
     // the dequant warps, so a full B ring never holds up the weight copies.
     static constexpr int kBWarp = 6 + kDeqWarps;
@@ -473,6 +474,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         // Each matrix of a stage is 128 rows x 64 codes = 512 chunks of 16
         // codes; dequant thread dt takes chunks dt, dt + D, ... (D = threads).
         constexpr int kDT = C::kDeqWarps * 32;
+        static_assert(512 % kDT == 0, "dequant threads divide the 512 chunks");
         const int dt = threadIdx.x - 6 * 32;
         uint32_t it = 0;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
@@ -498,7 +500,8 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                         const __half2 s2 = __float2half2_rn(s);
                         const uint32_t s2u = *reinterpret_cast<const uint32_t*>(&s2);
 #pragma unroll
-                        for (int qd = dt; qd < 512; qd += kDT) {
+                        for (int c = 0; c < 512 / kDT; ++c) {
+                            const int qd = dt + c * kDT;
                             const int r = qd >> 2, ch = qd & 3;    // row, 16-byte chunk of codes
                             const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 64 + ch * 16);
                             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
@@ -527,7 +530,8 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                     } else {
                         // NVFP4: a chunk is one 16-code scale block (8 bytes).
 #pragma unroll
-                        for (int qd = dt; qd < 512; qd += kDT) {
+                        for (int c = 0; c < 512 / kDT; ++c) {
+                            const int qd = dt + c * kDT;
                             const int r = qd >> 2, q = qd & 3;     // row, scale block of the stage
                             const uint2 v = *reinterpret_cast<const uint2*>(raw + r * 32 + q * 8);
                             const int kc = k0 + 16 * q;
