@@ -355,30 +355,32 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t it = 0, acc_it = 0;
-            for (int tau = blockIdx.x; tau < n_tiles && !*s_abort; tau += gridDim.x, ++acc_it) {
-                const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
-                const int ab = acc_it & 1;
-                if (!ptx::mbar_wait(&acc_empty[ab], ((acc_it >> 1) & 1) ^ 1, s_abort, err, 2)) break;
+        // The whole warp runs the loop, so the operand descriptors are
+        // warp-uniform values; one elected lane issues the MMAs and commits.
+        uint32_t it = 0, acc_it = 0;
+        for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x, ++acc_it) {
+            const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
+            const int ab = acc_it & 1;
+            if (!ptx::mbar_wait_warp(&acc_empty[ab], ((acc_it >> 1) & 1) ^ 1, s_abort, err, 2)) break;
+            ptx::tc_fence_after();
+            const int nmma = ((t.ntok + 15) >> 4) << 4;
+            const uint32_t idesc = ptx::idesc_f16(BM, nmma, !C::kF16);
+            const uint32_t d0 = tmem + ab * C::kAccCols;
+            const int KB = (t.K + BK - 1) / BK;
+            bool ok = true;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int as = it % C::kAStages;
+                const int bs = C::kDeq ? (int)(it % C::kBStages) : as;
+                if (!ptx::mbar_wait_warp(&a_full[as], (it / C::kAStages) & 1, s_abort, err, 2)) { ok = false; break; }
+                if constexpr (C::kDeq)
+                    if (!ptx::mbar_wait_warp(&b_full[bs], (it / C::kBStages) & 1, s_abort, err, 2)) {
+                        ok = false;
+                        break;
+                    }
                 ptx::tc_fence_after();
-                const int nmma = ((t.ntok + 15) >> 4) << 4;
-                const uint32_t idesc = ptx::idesc_f16(BM, nmma, !C::kF16);
-                const uint32_t d0 = tmem + ab * C::kAccCols;
-                const int KB = (t.K + BK - 1) / BK;
-                bool ok = true;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int as = it % C::kAStages;
-                    const int bs = C::kDeq ? (int)(it % C::kBStages) : as;
-                    if (!ptx::mbar_wait(&a_full[as], (it / C::kAStages) & 1, s_abort, err, 2)) { ok = false; break; }
-                    if constexpr (C::kDeq)
-                        if (!ptx::mbar_wait(&b_full[bs], (it / C::kBStages) & 1, s_abort, err, 2)) {
-                            ok = false;
-                            break;
-                        }
-                    ptx::tc_fence_after();
-                    const uint32_t a_base = ptx::smem_u32(sA + as * C::kAStage);
-                    const uint32_t b_base = ptx::smem_u32(sB + bs * C::kBStage);
+                const uint32_t a_base = ptx::smem_u32(sA + as * C::kAStage);
+                const uint32_t b_base = ptx::smem_u32(sB + bs * C::kBStage);
+                if (ptx::elect_one()) {
 #pragma unroll
                     for (int m = 0; m < C::kMats; ++m)
 #pragma unroll
@@ -389,13 +391,18 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                     ptx::mma_commit(&a_empty[as]);
                     if constexpr (C::kDeq) ptx::mma_commit(&b_empty[bs]);
                 }
-                if (!ok) break;
-                ptx::mma_commit(&acc_full[ab]);
+                __syncwarp();
             }
-            // Every MMA issued has completed before TMEM is released.
+            if (!ok) break;
+            if (ptx::elect_one()) ptx::mma_commit(&acc_full[ab]);
+            __syncwarp();
+        }
+        // Every MMA issued has completed before TMEM is released.
+        if (ptx::elect_one()) {
             ptx::mma_commit(drain);
             ptx::mbar_wait_quiet(drain, 0, 100000000ull);
         }
+        __syncwarp();
     } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                     // TMEM lane quarter of this warp
