@@ -290,16 +290,9 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
             }
             ptx::named_bar(1, kFCompute);
             // Rank = experts ahead in (score desc, index asc): selected iff rank < k.
-            for (int e = tid; e < E; e += kFCompute) {
-                const float v = ssc[e];
-                int rank = 0;
-                for (int f = 0; f < E; ++f) {
-                    const float u = ssc[f];
-                    rank += (u > v || (u == v && f < e)) ? 1 : 0;
-                }
-                if (rank < k) ssel[rank] = e;
-            }
-            ptx::named_bar(1, kFCompute);
+            topk_rank_block(ssc, E, k, tid, kFCompute, reinterpret_cast<int*>(sm + p.off_cand),
+                            reinterpret_cast<float*>(sm + p.off_cand) + p.n_cand, ssel,
+                            [] { ptx::named_bar(1, kFCompute); });
             if (tid == 0) ptx::mbar_arrive(sel_ready);
             if (warp == 0) {
                 // Routing weights, with the top-k kernel's arithmetic.
@@ -373,8 +366,27 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
 
         if (go2 && nrows > 0) {
             // Phase 2: down rows [h0, h1) from shared memory.
-            for (int i = tid; i < k * I; i += kFCompute) sact[i] = __ldcg(p.act + i);
-            for (int i = tid; i < S; i += kFCompute) sact[k * I + i] = __ldcg(p.act_sh + i);
+            // SiLU(g) * u of every route, then of the shared expert, contiguous in
+            // shared memory; each thread issues its loads before storing any.
+            {
+                const int n4 = (k * I) >> 2, t4 = n4 + (S >> 2);
+                const float4* a4 = reinterpret_cast<const float4*>(p.act);
+                const float4* s4 = reinterpret_cast<const float4*>(p.act_sh);
+                constexpr int kB = 4;
+                for (int i0 = tid; i0 < t4; i0 += kB * kFCompute) {
+                    float4 v[kB];
+#pragma unroll
+                    for (int b = 0; b < kB; ++b) {
+                        const int i = i0 + b * kFCompute;
+                        if (i < t4) v[b] = __ldcg(i < n4 ? a4 + i : s4 + (i - n4));
+                    }
+#pragma unroll
+                    for (int b = 0; b < kB; ++b) {
+                        const int i = i0 + b * kFCompute;
+                        if (i < t4) reinterpret_cast<float4*>(sact)[i] = v[b];
+                    }
+                }
+            }
             ptx::named_bar(1, kFCompute);
             const bool ok_d = ptx::mbar_wait_warp(dfull, 0, abort_f, err, 16) &&
                               ptx::mbar_wait_warp(dshfull, 0, abort_f, err, 16);
@@ -433,6 +445,8 @@ bool fused_plan(const moe_config_t* c, int num_sms, FusedParams* p) {
     p->off_lg = take((size_t)E * 4, 16);
     p->off_sc = take((size_t)E * 4, 16);
     p->off_sel = take(256 + 16, 16);   // 32 experts, 32 weights, the inverse RMS
+    p->n_cand = (E + 31) / 32 * k;     // top-k candidates (expert, score)
+    p->off_cand = take((size_t)p->n_cand * 8, 16);
     p->off_down = take((size_t)(k + 1) * p->rpc * p->drow_bytes, 128);
     p->off_act = take(((size_t)k * I + (S > 0 ? S : 0)) * 4, 16);
     // dfull, dshfull, sel_ready, abort + phase flags

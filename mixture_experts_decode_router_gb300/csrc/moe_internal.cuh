@@ -250,6 +250,55 @@ __device__ __forceinline__ float dot8(const float (&a)[8], const float (&b)[8]) 
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// Block-wide top-k by exact ranking: ssel[j] = the expert of rank j for j < k,
+// where an expert's rank is the number of experts ahead of it in (score
+// descending, index ascending) order.  Two levels: first each group of 32
+// consecutive experts ranks its members by shuffles and keeps its first k as
+// candidates; then each candidate is ranked among all candidates.  An expert
+// of global rank < k is among its group's first k, and so is every expert
+// ahead of it, so its rank among the candidates is its global rank; any other
+// candidate has the k true top experts ahead of it.  The selection is
+// therefore the one a full ranking gives, for any thread count.
+//   sc      scores [E] (shared memory; NaN already replaced by -inf)
+//   cand_e, cand_v   ceil(E/32) * k slots each (shared memory)
+//   sync    the block's barrier (all nthr threads call this function)
+template <typename Sync>
+__device__ __forceinline__ void topk_rank_block(const float* sc, int E, int k, int tid, int nthr, int* cand_e,
+                                                float* cand_v, int* ssel, Sync sync) {
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+    const int ngroups = (E + 31) >> 5;
+    for (int g = warp; g < ngroups; g += nwarps) {
+        const int e = 32 * g + lane;
+        const int nvalid = min(32, E - 32 * g);
+        const float v = lane < nvalid ? sc[e] : 0.f;
+        int rank = 0;
+        for (int j = 0; j < nvalid; ++j) {
+            const float u = __shfl_sync(0xffffffffu, v, j);
+            rank += (u > v || (u == v && j < lane)) ? 1 : 0;
+        }
+        if (lane < nvalid && rank < k) {
+            cand_e[g * k + rank] = e;
+            cand_v[g * k + rank] = v;
+        }
+        if (lane < k && lane >= nvalid) cand_e[g * k + lane] = -1;   // slots no member fills
+    }
+    sync();
+    const int nc = ngroups * k;
+    for (int c = tid; c < nc; c += nthr) {
+        const int e = cand_e[c];
+        if (e < 0) continue;
+        const float v = cand_v[c];
+        int rank = 0;
+        for (int c2 = 0; c2 < nc; ++c2) {
+            const int e2 = cand_e[c2];
+            const float u = cand_v[c2];
+            rank += (e2 >= 0 && (u > v || (u == v && e2 < e))) ? 1 : 0;
+        }
+        if (rank < k) ssel[rank] = e;
+    }
+    sync();
+}
+
 // 1 / sqrt(mean(x^2) + eps) of one BF16 row of H elements, by one warp: lane l
 // chains fmaf over its chunks l, l+32, ... in order, then a fixed butterfly.
 // (Generic pointer: the row may be in global or shared memory.)

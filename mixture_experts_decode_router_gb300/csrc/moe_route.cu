@@ -190,10 +190,10 @@ cudaError_t launch_router_nvfp4(const uint16_t* x, int n, int H, const QMatDev& 
 }
 
 // One CTA per token row.  Selection ranks the fp32 score (softmax: the logit;
-// sigmoid: sigmoid(l) + bias, the bias only selects); every thread ranks its
-// experts against all E scores (rank = experts ahead in score-descending,
-// index-ascending order; selected iff rank < k), which needs no serial shuffle
-// chain, and slot j holds the expert of rank j.  Warp 0 forms the weights:
+// sigmoid: sigmoid(l) + bias, the bias only selects); the experts are ranked
+// exactly (rank = experts ahead in score-descending, index-ascending order;
+// selected iff rank < k) in two levels (topk_rank_block), and slot j holds the
+// expert of rank j.  Warp 0 forms the weights:
 // softmax p = exp(l - max) / sum over all experts (lane l summing experts
 // l, l+32, ... in order, then a butterfly), sigmoid p = sigmoid(l);
 // renormalised over the k selected when norm != 0; multiplied by `scale`.
@@ -206,6 +206,8 @@ topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int rou
     float* slg = smf;          // [E]
     float* ssc = smf + E;      // [E]
     __shared__ int ssel[kMaxTopK];
+    __shared__ int cand_e[kMaxExperts / 32 * kMaxTopK];
+    __shared__ float cand_v[kMaxExperts / 32 * kMaxTopK];
     const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
     const float* lrow = logits + (size_t)t * E;
     pdl_wait();
@@ -219,16 +221,7 @@ topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int rou
         ssc[e] = sc;
     }
     __syncthreads();
-    for (int e = tid; e < E; e += blockDim.x) {
-        const float v = ssc[e];
-        int rank = 0;
-        for (int f = 0; f < E; ++f) {
-            const float u = ssc[f];
-            rank += (u > v || (u == v && f < e)) ? 1 : 0;
-        }
-        if (rank < k) ssel[rank] = e;
-    }
-    __syncthreads();
+    topk_rank_block(ssc, E, k, tid, blockDim.x, cand_e, cand_v, ssel, [] { __syncthreads(); });
     if (tid < 32) {
         const int sel_e = lane < k ? ssel[lane] : -1;
         const float sel_l = lane < k ? slg[sel_e] : 0.f;
