@@ -47,6 +47,9 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="decode_n1")
     p.add_argument("--path", default="auto", choices=["auto", "token_major", "grouped"])
     p.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
+    p.add_argument("--experts", type=int, default=0,
+                   help="override the workload's expert count (a smaller layer of the same kernels, "
+                        "for profiler captures)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--oracle-budget", type=float, default=15.0,
                    help="seconds of oracle work for the CPU baseline sample")
@@ -180,7 +183,7 @@ def _oracle_child(args):
     from oracle import moe_oracle as O
 
     torch.set_num_threads(1)
-    cfg = synth.WORKLOADS[args.workload]
+    cfg = workload_config(args)
     n_pool = max(cfg.n_tokens, 8)
     x = synth.make_input(cfg, n_pool, "cpu", dup_frac=0.0, stream=7)
     xb = x.view(torch.int16).numpy().view(np.uint16)
@@ -248,13 +251,26 @@ def _oracle_child(args):
     print(json.dumps({"tokens": done, "seconds": el, "tokens_per_s": done / el}))
 
 
+def workload_config(args):
+    """The workload's layer, with the --tokens / --experts overrides applied."""
+    from mixture_experts_decode_router_gb300 import synth
+    cfg = synth.WORKLOADS[args.workload]
+    if args.tokens > 0:
+        cfg = cfg.with_(n_tokens=args.tokens, name=f"{cfg.name}@n{args.tokens}")
+    if args.experts > 0:
+        cfg = cfg.with_(num_experts=args.experts, top_k=min(cfg.top_k, args.experts),
+                        name=f"{cfg.name}@e{args.experts}")
+    return cfg
+
+
 def cpu_baseline(args, budget: float, tokens: int = 0):
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[v] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", args.workload,
-           "--oracle-budget", str(budget), "--oracle-tokens", str(tokens)]
+           "--oracle-budget", str(budget), "--oracle-tokens", str(tokens),
+           "--tokens", str(args.tokens), "--experts", str(args.experts)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=budget * 4 + 600)
     if r.returncode != 0:
         raise RuntimeError(f"oracle child failed:\n{r.stderr[-2000:]}")
@@ -282,9 +298,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     B.load()
 
-    cfg = synth.WORKLOADS[args.workload]
-    if args.tokens > 0:
-        cfg = cfg.with_(n_tokens=args.tokens, name=f"{cfg.name}@n{args.tokens}")
+    cfg = workload_config(args)
     n = cfg.n_tokens
     lw = synth.make_weights(cfg, dev)
     x = synth.make_input(cfg, device=dev)
@@ -464,8 +478,7 @@ def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
         return
-    from mixture_experts_decode_router_gb300 import synth
-    cfg = synth.WORKLOADS[args.workload]
+    cfg = workload_config(args)
     # One step = one token through the oracle; the run is bounded to ~2 minutes.
     budget = 120.0
     cpu = cpu_baseline(args, budget, tokens=max(1, args.steps))

@@ -18,8 +18,11 @@
 //           down rows into shared memory.
 //           Grid barrier 2: all SiLU(g)*u values are written.
 //  phase 2  every CTA computes its output columns from the down rows already
-//           in shared memory: down projection, routing-weighted sum and the
-//           shared expert, written as BF16.
+//           in shared memory: first each lane's partial dot product of every
+//           (expert slot, row) pair -- a warp per slot, its activation chunks
+//           held in registers across the rows -- then per row the partials
+//           weighted in slot order, the gated shared expert, the butterfly
+//           and the BF16 write.
 //
 // The arithmetic of every dot product, the top-k weights and the blend is the
 // same, operation for operation, as the token-major kernels' for one token,
@@ -59,26 +62,6 @@ __device__ __forceinline__ const uint8_t* row_ptr(const QMatDev& m, int e, int r
     return m.w + ((size_t)(e - m.e_base) * m.out_dim + row) * row_bytes_of(FMT, m.in_dim);
 }
 
-// Lane partial of one down-projection row against an activation vector, with
-// the token-major kernel's chunk order and per-chunk scale.
-template <int FMT>
-__device__ __forceinline__ float row_partial_smem(const uint8_t* drow, const float* a, const QMatDev& M, int e,
-                                                  int h, int K, int lane) {
-    float acc2 = 0.f;
-    for (int c = lane; c < (K >> 3); c += 32) {
-        float wv[8], av[8];
-        decode_at<FMT>(drow, c, wv);
-        WChunk<FMT> sch;
-        const float cs = sch.scale(M, e, h, c);
-        const float4 a0 = reinterpret_cast<const float4*>(a)[2 * c];
-        const float4 a1 = reinterpret_cast<const float4*>(a)[2 * c + 1];
-        av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
-        av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
-        acc2 = fmaf(dot8(wv, av), cs, acc2);
-    }
-    return acc2;
-}
-
 template <int FMT>
 __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParams p) {
     extern __shared__ __align__(128) uint8_t sm[];
@@ -102,16 +85,17 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
     Ctrl* ctrl = p.ctrl;
     int32_t* err = &ctrl->err;
 
+    // The barrier word must be below G at the start of a call (zeroed once,
+    // returned to zero by every call); anything else is a workspace that was
+    // not initialised (or a call that failed): refuse before writing anything.
+    // The word is read early and tested after x is staged, so its latency and
+    // x's overlap.
+    uint32_t gbar0 = 0;
     if (tid == 0) {
+        gbar0 = ptx::ld_relaxed_gpu(&ctrl->gbar);
         ptx::mbar_init(dfull, 1);
         ptx::mbar_init(dshfull, 1);
         ptx::mbar_init(sel_ready, 1);
-        // The barrier word must be below G at the start of a call (zeroed once,
-        // returned to zero by every call); anything else is a workspace that
-        // was not initialised (or a call that failed): refuse before touching it.
-        const bool clean = ptx::ld_acquire_gpu(&ctrl->gbar) < (uint32_t)G;
-        if (!clean) atomicExch(err, 20);
-        *abort_f = clean ? 0 : 2;
         ptx::fence_mbar_init();
     }
     // Router row of this warp (r == E: the shared-gate row): its first chunks
@@ -130,6 +114,11 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
     }
     for (int i = tid; i < H / 8; i += kFThreads)
         reinterpret_cast<uint4*>(sx)[i] = __ldg(reinterpret_cast<const uint4*>(p.x) + i);
+    if (tid == 0) {
+        const bool clean = gbar0 < (uint32_t)G;
+        if (!clean) atomicExch(err, 20);
+        *abort_f = clean ? 0 : 2;
+    }
     __syncthreads();
     const bool refused = *abort_f == 2;
     // The experts' input: x, or its pre-expert RMSNorm (the norm kernel's
@@ -289,38 +278,18 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                 ssc[e] = sc;
             }
             ptx::named_bar(1, kFCompute);
-            // Rank = experts ahead in (score desc, index asc): selected iff rank < k.
-            topk_rank_block(ssc, E, k, tid, kFCompute, reinterpret_cast<int*>(sm + p.off_cand),
-                            reinterpret_cast<float*>(sm + p.off_cand) + p.n_cand, ssel,
-                            [] { ptx::named_bar(1, kFCompute); });
-            if (tid == 0) ptx::mbar_arrive(sel_ready);
-            if (warp == 0) {
-                // Routing weights, with the top-k kernel's arithmetic.
-                const int sel_e = lane < k ? ssel[lane] : -1;
-                const float sel_l = lane < k ? slg[sel_e] : 0.f;
-                float pr;
-                if (p.routing == MOE_ROUTE_SOFTMAX) {
-                    const float mx = __shfl_sync(0xffffffffu, sel_l, 0);
-                    float z = 0.f;
-                    for (int i = 0; lane + 32 * i < E; ++i) z += expf(slg[lane + 32 * i] - mx);
-                    z = warp_sum(z);
-                    pr = (lane < k) ? expf(sel_l - mx) / z : 0.f;
-                } else {
-                    pr = (lane < k) ? 1.0f / (1.0f + expf(-sel_l)) : 0.f;
-                }
-                if (p.norm) {
-                    const float tot = warp_sum(pr);
-                    pr = pr / tot;
-                }
-                if (lane < k) {
-                    sselw[lane] = pr * p.scale;
-                    if (cta == 0) {
-                        p.idx_out[lane] = sel_e;
-                        p.w_out[lane] = pr * p.scale;
-                    }
-                }
+            // Selection and weights, with the top-k kernel's arithmetic; the copy
+            // producer starts on the routed down rows as soon as ssel is known.
+            int* cand_e = reinterpret_cast<int*>(sm + p.off_cand);
+            float* cand_v = reinterpret_cast<float*>(cand_e + p.n_cand);
+            float* gmax = cand_v + p.n_cand;
+            route_block(slg, ssc, E, k, p.routing, p.norm, p.scale, tid, kFCompute, cand_e, cand_v, gmax,
+                        gmax + 32, ssel, sselw, [] { ptx::named_bar(1, kFCompute); },
+                        [&] { if (tid == 0) ptx::mbar_arrive(sel_ready); });
+            if (cta == 0 && tid < k) {
+                p.idx_out[tid] = ssel[tid];
+                p.w_out[tid] = sselw[tid];
             }
-            ptx::named_bar(1, kFCompute);
 
             // Phase 1b: the routed gate/up rows of this CTA.
             // Items continue the shared ones' warp rotation, so the CTA's warps
@@ -388,28 +357,74 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                 }
             }
             ptx::named_bar(1, kFCompute);
-            const bool ok_d = ptx::mbar_wait_warp(dfull, 0, abort_f, err, 16) &&
+            const bool ok_w = ptx::mbar_wait_warp(dfull, 0, abort_f, err, 16) &&
                               ptx::mbar_wait_warp(dshfull, 0, abort_f, err, 16);
-            if (ok_d) {
+            if (!ok_w) *s_go = 0;              // one decision for every compute warp
+            ptx::named_bar(1, kFCompute);
+            if (*s_go != 0) {
+                // Phase 2a: each lane's partial dot product of every (slot, row) of
+                // this CTA -- slot j < k a routed expert, slot k the shared one --
+                // with the token-major kernel's chunk order.  A warp keeps one
+                // slot's activation chunk in registers across its rows.
+                float* spart = reinterpret_cast<float*>(sm + p.off_part);   // [J][rpc][32]
+                const int J = k + (S > 0 ? 1 : 0);
+                const int R = J >= kFComputeWarps ? 1 : kFComputeWarps / J;   // warps per slot
+                constexpr int kPR = 16;                                      // rows per pass
+                for (int w = warp; w < J * R; w += kFComputeWarps) {
+                    const int j = w % J, sub = w / J;
+                    const bool shj = S > 0 && j == k;
+                    const int e = shj ? 0 : ssel[j];
+                    if (!shj && !local(e)) continue;
+                    const QMatDev& M = shj ? p.sh_down : p.down;
+                    const int K = shj ? S : I;
+                    const float* a = sact + (size_t)j * I;
+                    const uint8_t* base = sdown + (size_t)j * rpc * p.drow_bytes;
+                    const uint32_t rb = shj ? p.dsh_row_bytes : p.drow_bytes;
+                    for (int r0 = sub; r0 < nrows; r0 += R * kPR) {
+                        float part[kPR];
+#pragma unroll
+                        for (int i = 0; i < kPR; ++i) part[i] = 0.f;
+                        for (int c = lane; c < (K >> 3); c += 32) {
+                            float av[8];
+                            const float4 a0 = reinterpret_cast<const float4*>(a)[2 * c];
+                            const float4 a1 = reinterpret_cast<const float4*>(a)[2 * c + 1];
+                            av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
+                            av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
+#pragma unroll
+                            for (int i = 0; i < kPR; ++i) {
+                                const int r = r0 + i * R;
+                                if (r < nrows) {
+                                    float wv[8];
+                                    decode_at<FMT>(base + (size_t)r * rb, c, wv);
+                                    WChunk<FMT> sch;
+                                    const float cs = sch.scale(M, e, h0 + r, c);
+                                    part[i] = fmaf(dot8(wv, av), cs, part[i]);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < kPR; ++i) {
+                            const int r = r0 + i * R;
+                            if (r < nrows) spart[((size_t)j * rpc + r) * 32 + lane] = part[i];
+                        }
+                    }
+                }
+                ptx::named_bar(1, kFCompute);
+                // Phase 2b: per output row, the slots' partials weighted in slot
+                // order, the gated shared expert last, then the butterfly.
                 float gs = 1.0f;
                 if (p.gw) gs = 1.0f / (1.0f + expf(-__ldcg(p.sg_logit)));
                 if (S > 0) gs *= matrix_scale<FMT>(p.sh_down, 0);
                 for (int h = h0 + warp; h < h1; h += kFComputeWarps) {
+                    const int r = h - h0;
                     float acc = 0.f;
                     for (int j = 0; j < k; ++j) {
                         const int e = ssel[j];
                         if (!local(e)) continue;
                         const float wt = sselw[j] * matrix_scale<FMT>(p.down, e);
-                        const uint8_t* drow = sdown + ((size_t)j * rpc + (h - h0)) * p.drow_bytes;
-                        acc = fmaf(row_partial_smem<FMT>(drow, sact + (size_t)j * I, p.down, e, h, I, lane), wt,
-                                   acc);
+                        acc = fmaf(spart[((size_t)j * rpc + r) * 32 + lane], wt, acc);
                     }
-                    if (S > 0) {
-                        const uint8_t* drow =
-                            sdown + (size_t)k * rpc * p.drow_bytes + (size_t)(h - h0) * p.dsh_row_bytes;
-                        acc = fmaf(row_partial_smem<FMT>(drow, sact + (size_t)k * I, p.sh_down, 0, h, S, lane), gs,
-                                   acc);
-                    }
+                    if (S > 0) acc = fmaf(spart[((size_t)k * rpc + r) * 32 + lane], gs, acc);
                     float s = warp_sum(acc);
                     if (lane == 0) {
                         if (p.accumulate) s += __uint_as_float((uint32_t)p.out[h] << 16);
@@ -445,10 +460,11 @@ bool fused_plan(const moe_config_t* c, int num_sms, FusedParams* p) {
     p->off_lg = take((size_t)E * 4, 16);
     p->off_sc = take((size_t)E * 4, 16);
     p->off_sel = take(256 + 16, 16);   // 32 experts, 32 weights, the inverse RMS
-    p->n_cand = (E + 31) / 32 * k;     // top-k candidates (expert, score)
-    p->off_cand = take((size_t)p->n_cand * 8, 16);
+    p->n_cand = (E + 31) / 32 * k;     // top-k candidates (expert, score), group maxima and sums
+    p->off_cand = take((size_t)p->n_cand * 8 + 2 * 32 * 4, 16);
     p->off_down = take((size_t)(k + 1) * p->rpc * p->drow_bytes, 128);
     p->off_act = take(((size_t)k * I + (S > 0 ? S : 0)) * 4, 16);
+    p->off_part = take((size_t)(k + (S > 0 ? 1 : 0)) * p->rpc * 32 * 4, 16);   // phase-2 lane partials
     // dfull, dshfull, sel_ready, abort + phase flags
     p->off_bar = take(3 * 8 + 16, 8);
     p->smem_bytes = (uint32_t)off;

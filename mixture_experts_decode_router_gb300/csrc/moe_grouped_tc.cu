@@ -8,10 +8,10 @@
 // as a dense GEMM on the 5th-generation tensor cores.
 //
 //   gather     xs[p, :] = x[token(perm[p]), :]   (expert-sorted activations)
-//   gate_up    per (expert, 128 rows of I, <=128 tokens) tile:
+//   gate_up    per (expert, 128 rows of I, <=64 tokens) tile:
 //              G = Wg x^T, U = Wu x^T on tcgen05 (TMEM accumulators),
 //              a = SiLU(G) * U  -> as[p, i]
-//   down       per (expert, 128 rows of H, <=128 tokens) tile:
+//   down       per (expert, 128 rows of H, <=64 tokens) tile:
 //              D = Wd a^T;  y[p, h] = w(route p) * D      (fp32)
 //   combine    out[t, h] = sum over t's slots, in slot order, of y[., h]
 //              + the gated shared expert; BF16.  No atomics, so every row's
@@ -56,7 +56,7 @@ struct TcCfg {
     static constexpr int kRawRow = FMT == MOE_W_FP8_B128 ? BK : (FMT == MOE_W_NVFP4 ? BK / 2 : 0);
     static constexpr int kRawMat = BM * kRawRow;
     static constexpr int kRawStage = kMats * kRawMat;
-    static constexpr int kAStages = kDeq ? (GU ? 3 : 4) : (GU ? 4 : 6);
+    static constexpr int kAStages = kDeq ? (GU ? 4 : 7) : (GU ? 5 : 8);
     // Dequantised tiles: the token (B) tiles have a ring of their own, so they
     // are fetched ahead instead of after the MMA frees an A slot.
     static constexpr int kBStages = kDeq ? (GU ? 4 : 6) : kAStages;
@@ -378,16 +378,17 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                         break;
                     }
                 ptx::tc_fence_after();
-                const uint32_t a_base = ptx::smem_u32(sA + as * C::kAStage);
-                const uint32_t b_base = ptx::smem_u32(sB + bs * C::kBStage);
+                // Descriptors of the stage's first K step; a later step (or the
+                // second matrix) only moves the start address field (16-byte units).
+                const uint64_t a_desc = ptx::sw128_desc(ptx::smem_u32(sA + as * C::kAStage));
+                const uint64_t b_desc = ptx::sw128_desc(ptx::smem_u32(sB + bs * C::kBStage));
                 if (ptx::elect_one()) {
 #pragma unroll
                     for (int m = 0; m < C::kMats; ++m)
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            ptx::mma_f16(d0 + m * NT, ptx::sw128_desc(a_base + m * C::kAMat + kk * 32),
-                                         ptx::sw128_desc(b_base + kk * 32), idesc,
-                                         (kb > 0 || kk > 0) ? 1u : 0u);
+                            ptx::mma_f16(d0 + m * NT, a_desc + (uint64_t)((m * C::kAMat + kk * 32) >> 4),
+                                         b_desc + (uint64_t)((kk * 32) >> 4), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
                     ptx::mma_commit(&a_empty[as]);
                     if constexpr (C::kDeq) ptx::mma_commit(&b_empty[bs]);
                 }

@@ -29,7 +29,7 @@ struct Ctrl {
 };
 
 // Tokens per tile of the grouped tensor-core path (its MMA N is at most this).
-constexpr int kTcTokensPerTile = 128;
+constexpr int kTcTokensPerTile = 64;
 
 struct WsLayout {
     size_t ctrl, logits, sg_logit, idx, w, counts, offsets, perm, active, act, act_sh,
@@ -250,23 +250,42 @@ __device__ __forceinline__ float dot8(const float (&a)[8], const float (&b)[8]) 
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
-// Block-wide top-k by exact ranking: ssel[j] = the expert of rank j for j < k,
-// where an expert's rank is the number of experts ahead of it in (score
-// descending, index ascending) order.  Two levels: first each group of 32
+// Routing of one token by one thread block: the top-k experts and their
+// weights from the router logits.
+//
+// Selection ranks the score sc[e] (softmax: the logit; sigmoid: sigmoid(l) +
+// bias, the bias only selects): the rank of e is the number of experts ahead
+// of it in (score descending, index ascending) order, and ssel[j] is the
+// expert of rank j < k.  The ranks are exact, in two levels: each group of 32
 // consecutive experts ranks its members by shuffles and keeps its first k as
-// candidates; then each candidate is ranked among all candidates.  An expert
-// of global rank < k is among its group's first k, and so is every expert
-// ahead of it, so its rank among the candidates is its global rank; any other
-// candidate has the k true top experts ahead of it.  The selection is
-// therefore the one a full ranking gives, for any thread count.
-//   sc      scores [E] (shared memory; NaN already replaced by -inf)
-//   cand_e, cand_v   ceil(E/32) * k slots each (shared memory)
-//   sync    the block's barrier (all nthr threads call this function)
-template <typename Sync>
-__device__ __forceinline__ void topk_rank_block(const float* sc, int E, int k, int tid, int nthr, int* cand_e,
-                                                float* cand_v, int* ssel, Sync sync) {
+// candidates; then each candidate is ranked among all candidates (one warp per
+// candidate, by ballots).  An expert of global rank < k is among its group's
+// first k, and so is every expert ahead of it, so its rank among the
+// candidates is its global rank; any other candidate has the k true top
+// experts ahead of it.
+//
+// Weights: softmax p = exp(l - m) / z with m the largest logit and z the sum
+// of exp(l - m) over all E experts, taken as a fixed butterfly within each
+// group of 32 and then over the groups in order; sigmoid p = sigmoid(l).
+// Renormalised over the k selected when norm != 0 (a fixed butterfly), then
+// multiplied by `scale`: sselw[j] is the weight of ssel[j].
+//
+// The result depends on E, k and the logits only (not on the thread count),
+// so every kernel that routes with this function routes alike.
+//   slg, sc            logits and scores [E] (shared memory; NaN scores as -inf)
+//   cand_e, cand_v     ceil(E/32) * k slots each (shared memory)
+//   gmax, zg           ceil(E/32) floats each (shared memory)
+//   on_selected        called by every thread once ssel is complete
+//   sync               the block's barrier (all nthr threads call this function)
+template <typename Sync, typename OnSelected>
+__device__ __forceinline__ void route_block(const float* slg, const float* sc, int E, int k, int routing,
+                                            int norm, float scale, int tid, int nthr, int* cand_e,
+                                            float* cand_v, float* gmax, float* zg, int* ssel, float* sselw,
+                                            Sync sync, OnSelected on_selected) {
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
     const int ngroups = (E + 31) >> 5;
+    const bool softmax = routing == MOE_ROUTE_SOFTMAX;
+    // Level 1, and each group's largest logit.
     for (int g = warp; g < ngroups; g += nwarps) {
         const int e = 32 * g + lane;
         const int nvalid = min(32, E - 32 * g);
@@ -281,20 +300,64 @@ __device__ __forceinline__ void topk_rank_block(const float* sc, int E, int k, i
             cand_v[g * k + rank] = v;
         }
         if (lane < k && lane >= nvalid) cand_e[g * k + lane] = -1;   // slots no member fills
+        if (softmax) {
+            float m = lane < nvalid ? slg[e] : -INFINITY;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) gmax[g] = m;
+        }
     }
     sync();
+    // Level 2: one warp per candidate.
     const int nc = ngroups * k;
-    for (int c = tid; c < nc; c += nthr) {
+    for (int c = warp; c < nc; c += nwarps) {
         const int e = cand_e[c];
         if (e < 0) continue;
         const float v = cand_v[c];
-        int rank = 0;
-        for (int c2 = 0; c2 < nc; ++c2) {
-            const int e2 = cand_e[c2];
-            const float u = cand_v[c2];
-            rank += (e2 >= 0 && (u > v || (u == v && e2 < e))) ? 1 : 0;
+        int cnt = 0;
+        for (int c0 = 0; c0 < nc; c0 += 32) {
+            const int c2 = c0 + lane;
+            bool ahead = false;
+            if (c2 < nc) {
+                const int e2 = cand_e[c2];
+                const float u = cand_v[c2];
+                ahead = e2 >= 0 && (u > v || (u == v && e2 < e));
+            }
+            cnt += __popc(__ballot_sync(0xffffffffu, ahead));
         }
-        if (rank < k) ssel[rank] = e;
+        if (lane == 0 && cnt < k) ssel[cnt] = e;
+    }
+    // The softmax normaliser, one group per warp.
+    float mx = 0.f;
+    if (softmax) {
+        mx = lane < ngroups ? gmax[lane] : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        for (int g = warp; g < ngroups; g += nwarps) {
+            const int e = 32 * g + lane;
+            float z = e < E ? expf(slg[e] - mx) : 0.f;
+            z = warp_sum(z);
+            if (lane == 0) zg[g] = z;
+        }
+    }
+    sync();
+    on_selected();
+    if (warp == 0) {
+        const int sel_e = lane < k ? ssel[lane] : -1;
+        const float sel_l = lane < k ? slg[sel_e] : 0.f;
+        float p;
+        if (softmax) {
+            float z = 0.f;
+            for (int g = 0; g < ngroups; ++g) z += zg[g];
+            p = lane < k ? expf(sel_l - mx) / z : 0.f;
+        } else {
+            p = lane < k ? 1.0f / (1.0f + expf(-sel_l)) : 0.f;
+        }
+        if (norm) {
+            const float tot = warp_sum(p);
+            p = p / tot;
+        }
+        if (lane < k) sselw[lane] = p * scale;
     }
     sync();
 }

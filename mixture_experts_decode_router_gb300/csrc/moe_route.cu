@@ -189,15 +189,8 @@ cudaError_t launch_router_nvfp4(const uint16_t* x, int n, int H, const QMatDev& 
     return cudaGetLastError();
 }
 
-// One CTA per token row.  Selection ranks the fp32 score (softmax: the logit;
-// sigmoid: sigmoid(l) + bias, the bias only selects); the experts are ranked
-// exactly (rank = experts ahead in score-descending, index-ascending order;
-// selected iff rank < k) in two levels (topk_rank_block), and slot j holds the
-// expert of rank j.  Warp 0 forms the weights:
-// softmax p = exp(l - max) / sum over all experts (lane l summing experts
-// l, l+32, ... in order, then a butterfly), sigmoid p = sigmoid(l);
-// renormalised over the k selected when norm != 0; multiplied by `scale`.
-// The single-token kernel repeats this arithmetic exactly.
+// One CTA per token row: selection and weights by route_block (exact ranks,
+// fixed-order softmax normaliser), which the single-token kernel also uses.
 __global__ void __launch_bounds__(256)
 topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int routing,
                   const float* __restrict__ bias, int norm, float scale,
@@ -206,9 +199,11 @@ topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int rou
     float* slg = smf;          // [E]
     float* ssc = smf + E;      // [E]
     __shared__ int ssel[kMaxTopK];
+    __shared__ float sselw[kMaxTopK];
     __shared__ int cand_e[kMaxExperts / 32 * kMaxTopK];
     __shared__ float cand_v[kMaxExperts / 32 * kMaxTopK];
-    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+    __shared__ float gmax[kMaxExperts / 32], zg[kMaxExperts / 32];
+    const int t = blockIdx.x, tid = threadIdx.x;
     const float* lrow = logits + (size_t)t * E;
     pdl_wait();
     for (int e = tid; e < E; e += blockDim.x) {
@@ -221,28 +216,11 @@ topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int rou
         ssc[e] = sc;
     }
     __syncthreads();
-    topk_rank_block(ssc, E, k, tid, blockDim.x, cand_e, cand_v, ssel, [] { __syncthreads(); });
-    if (tid < 32) {
-        const int sel_e = lane < k ? ssel[lane] : -1;
-        const float sel_l = lane < k ? slg[sel_e] : 0.f;
-        float p;
-        if (routing == MOE_ROUTE_SOFTMAX) {
-            const float mx = __shfl_sync(0xffffffffu, sel_l, 0);
-            float z = 0.f;
-            for (int i = 0; lane + 32 * i < E; ++i) z += expf(slg[lane + 32 * i] - mx);
-            z = warp_sum(z);
-            p = (lane < k) ? expf(sel_l - mx) / z : 0.f;
-        } else {
-            p = (lane < k) ? 1.0f / (1.0f + expf(-sel_l)) : 0.f;
-        }
-        if (norm) {
-            const float tot = warp_sum(p);
-            p = p / tot;
-        }
-        if (lane < k) {
-            idx_out[(size_t)t * k + lane] = sel_e;
-            w_out[(size_t)t * k + lane] = p * scale;
-        }
+    route_block(slg, ssc, E, k, routing, norm, scale, tid, blockDim.x, cand_e, cand_v, gmax, zg, ssel, sselw,
+                [] { __syncthreads(); }, [] {});
+    if (tid < k) {
+        idx_out[(size_t)t * k + tid] = ssel[tid];
+        w_out[(size_t)t * k + tid] = sselw[tid];
     }
     pdl_trigger();
 }
