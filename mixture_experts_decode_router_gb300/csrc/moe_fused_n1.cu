@@ -19,8 +19,9 @@
 //           Grid barrier 2: all SiLU(g)*u values are written.
 //  phase 2  every CTA computes its output columns from the down rows already
 //           in shared memory: first each lane's partial dot product of every
-//           (expert slot, row) pair -- a warp per slot, its activation chunks
-//           held in registers across the rows -- then per row the partials
+//           (expert slot, row) pair -- the pairs split evenly over the warps in
+//           slot-major order, a warp's activation chunk held in registers across
+//           its rows of a slot -- then per row the partials
 //           weighted in slot order, the gated shared expert, the butterfly
 //           and the BF16 write.
 //
@@ -71,7 +72,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
 
     uint16_t* sx = reinterpret_cast<uint16_t*>(sm + p.off_x);
     float* slg = reinterpret_cast<float*>(sm + p.off_lg);
-    float* ssc = reinterpret_cast<float*>(sm + p.off_sc);
+    unsigned long long* skey = reinterpret_cast<unsigned long long*>(sm + p.off_sc);   // [E + 32]
     int* ssel = reinterpret_cast<int*>(sm + p.off_sel);
     float* sselw = reinterpret_cast<float*>(sm + p.off_sel + 128);
     uint8_t* sdown = sm + p.off_down;
@@ -268,28 +269,28 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
 
         if (go1) {
             // Phase 1a: routing, computed by every CTA for itself.
-            for (int e = tid; e < E; e += kFCompute) {
-                const float l = __ldcg(p.logits + e);
-                float sc;
-                if (p.routing == MOE_ROUTE_SOFTMAX) sc = l;
-                else sc = 1.0f / (1.0f + expf(-l)) + p.bias[e];
-                if (sc != sc) sc = -INFINITY;
-                slg[e] = l;
-                ssc[e] = sc;
+            for (int e = tid; e < E + 32; e += kFCompute) {
+                if (e < E) {
+                    const float l = __ldcg(p.logits + e);
+                    float sc;
+                    if (p.routing == MOE_ROUTE_SOFTMAX) sc = l;
+                    else sc = 1.0f / (1.0f + expf(-l)) + p.bias[e];
+                    if (sc != sc) sc = -INFINITY;
+                    slg[e] = l;
+                    skey[e] = route_key(sc, e);
+                } else {
+                    skey[e] = 0ull;
+                }
             }
             ptx::named_bar(1, kFCompute);
-            // Selection and weights, with the top-k kernel's arithmetic; the copy
-            // producer starts on the routed down rows as soon as ssel is known.
-            int* cand_e = reinterpret_cast<int*>(sm + p.off_cand);
-            float* cand_v = reinterpret_cast<float*>(cand_e + p.n_cand);
-            float* gmax = cand_v + p.n_cand;
-            route_block(slg, ssc, E, k, p.routing, p.norm, p.scale, tid, kFCompute, cand_e, cand_v, gmax,
-                        gmax + 32, ssel, sselw, [] { ptx::named_bar(1, kFCompute); },
-                        [&] { if (tid == 0) ptx::mbar_arrive(sel_ready); });
-            if (cta == 0 && tid < k) {
-                p.idx_out[tid] = ssel[tid];
-                p.w_out[tid] = sselw[tid];
-            }
+            // Selection, with the top-k kernel's arithmetic; the copy producer
+            // starts on the routed down rows as soon as it is known.  The
+            // weights are formed later, while grid barrier 2 fills.
+            unsigned long long* cand_k = reinterpret_cast<unsigned long long*>(sm + p.off_cand);
+            float* gmax = reinterpret_cast<float*>(cand_k + p.n_cand);
+            route_select_block(slg, skey, E, k, p.routing, tid, kFCompute, cand_k, gmax, ssel,
+                               [] { ptx::named_bar(1, kFCompute); });
+            if (tid == 0) ptx::mbar_arrive(sel_ready);
 
             // Phase 1b: the routed gate/up rows of this CTA.
             // Items continue the shared ones' warp rotation, so the CTA's warps
@@ -304,14 +305,27 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
             }
         }
 
-        // Grid barrier 2: every SiLU(g) * u is written.
+        // Grid barrier 2: every SiLU(g) * u is written.  The routing weights
+        // (needed from phase 2 on) are formed between the arrival and the wait.
         ptx::named_bar(1, kFCompute);
+        uint32_t old2 = 0;
+        const bool arrived2 = tid == 0 && !*abort_f;
+        if (arrived2) old2 = ptx::atom_add_acq_rel_gpu(&ctrl->gbar, 1u);
+        if (go1) {
+            float* gmax = reinterpret_cast<float*>(reinterpret_cast<unsigned long long*>(sm + p.off_cand) + p.n_cand);
+            route_weights_block(slg, E, k, p.routing, p.norm, p.scale, tid, kFCompute, gmax, gmax + 32, ssel,
+                                sselw, [] { ptx::named_bar(1, kFCompute); });
+            if (cta == 0 && tid < k) {
+                p.idx_out[tid] = ssel[tid];
+                p.w_out[tid] = sselw[tid];
+            }
+        }
         if (tid == 0) {
-            if (!*abort_f) {
+            if (arrived2) {
                 // The last CTA to arrive returns the word to zero for the next
                 // call; the others stop waiting at 2G or at that zero (the word
                 // cannot be zero again before this call ends).
-                const uint32_t old = ptx::atom_add_acq_rel_gpu(&ctrl->gbar, 1u);
+                const uint32_t old = old2;
                 if (old == 2u * G - 1) {
                     ptx::st_relaxed_gpu(&ctrl->gbar, 0u);
                 } else {
@@ -364,14 +378,18 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
             if (*s_go != 0) {
                 // Phase 2a: each lane's partial dot product of every (slot, row) of
                 // this CTA -- slot j < k a routed expert, slot k the shared one --
-                // with the token-major kernel's chunk order.  A warp keeps one
-                // slot's activation chunk in registers across its rows.
+                // with the token-major kernel's chunk order.  The (slot, row) pairs
+                // are split evenly over the warps in slot-major order; a warp keeps
+                // a slot's activation chunk in registers across its rows.
                 float* spart = reinterpret_cast<float*>(sm + p.off_part);   // [J][rpc][32]
                 const int J = k + (S > 0 ? 1 : 0);
-                const int R = J >= kFComputeWarps ? 1 : kFComputeWarps / J;   // warps per slot
+                const int P = J * nrows;
+                const int q1 = (int)((int64_t)P * (warp + 1) / kFComputeWarps);
                 constexpr int kPR = 16;                                      // rows per pass
-                for (int w = warp; w < J * R; w += kFComputeWarps) {
-                    const int j = w % J, sub = w / J;
+                for (int q = (int)((int64_t)P * warp / kFComputeWarps); q < q1;) {
+                    const int j = q / nrows, rb0 = q - j * nrows;
+                    const int nr = min(q1 - q, nrows - rb0);   // this warp's rows of slot j
+                    q += nr;
                     const bool shj = S > 0 && j == k;
                     const int e = shj ? 0 : ssel[j];
                     if (!shj && !local(e)) continue;
@@ -380,10 +398,12 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                     const float* a = sact + (size_t)j * I;
                     const uint8_t* base = sdown + (size_t)j * rpc * p.drow_bytes;
                     const uint32_t rb = shj ? p.dsh_row_bytes : p.drow_bytes;
-                    for (int r0 = sub; r0 < nrows; r0 += R * kPR) {
+                    for (int r0 = rb0; r0 < rb0 + nr; r0 += kPR) {
+                        const int rn = min(kPR, rb0 + nr - r0);
                         float part[kPR];
 #pragma unroll
                         for (int i = 0; i < kPR; ++i) part[i] = 0.f;
+#pragma unroll 2
                         for (int c = lane; c < (K >> 3); c += 32) {
                             float av[8];
                             const float4 a0 = reinterpret_cast<const float4*>(a)[2 * c];
@@ -392,8 +412,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                             av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
 #pragma unroll
                             for (int i = 0; i < kPR; ++i) {
-                                const int r = r0 + i * R;
-                                if (r < nrows) {
+                                if (i < rn) {
+                                    const int r = r0 + i;
                                     float wv[8];
                                     decode_at<FMT>(base + (size_t)r * rb, c, wv);
                                     WChunk<FMT> sch;
@@ -403,10 +423,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                             }
                         }
 #pragma unroll
-                        for (int i = 0; i < kPR; ++i) {
-                            const int r = r0 + i * R;
-                            if (r < nrows) spart[((size_t)j * rpc + r) * 32 + lane] = part[i];
-                        }
+                        for (int i = 0; i < kPR; ++i)
+                            if (i < rn) spart[((size_t)j * rpc + r0 + i) * 32 + lane] = part[i];
                     }
                 }
                 ptx::named_bar(1, kFCompute);
@@ -418,11 +436,21 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                 for (int h = h0 + warp; h < h1; h += kFComputeWarps) {
                     const int r = h - h0;
                     float acc = 0.f;
-                    for (int j = 0; j < k; ++j) {
-                        const int e = ssel[j];
-                        if (!local(e)) continue;
-                        const float wt = sselw[j] * matrix_scale<FMT>(p.down, e);
-                        acc = fmaf(spart[((size_t)j * rpc + r) * 32 + lane], wt, acc);
+                    for (int j0 = 0; j0 < k; j0 += 8) {
+                        // Eight slots' loads first, then their terms in slot order.
+                        float pv[8], wv[8];
+                        bool lv[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int j = j0 + u;
+                            const int e = j < k ? ssel[j] : -1;
+                            lv[u] = j < k && local(e);
+                            pv[u] = lv[u] ? spart[((size_t)j * rpc + r) * 32 + lane] : 0.f;
+                            wv[u] = lv[u] ? sselw[j] * matrix_scale<FMT>(p.down, e) : 0.f;
+                        }
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            if (lv[u]) acc = fmaf(pv[u], wv[u], acc);
                     }
                     if (S > 0) acc = fmaf(spart[((size_t)k * rpc + r) * 32 + lane], gs, acc);
                     float s = warp_sum(acc);
@@ -458,9 +486,9 @@ bool fused_plan(const moe_config_t* c, int num_sms, FusedParams* p) {
     p->off_x = take((size_t)H * 2, 128);
     p->off_xe = take((size_t)H * 2, 128);
     p->off_lg = take((size_t)E * 4, 16);
-    p->off_sc = take((size_t)E * 4, 16);
+    p->off_sc = take((size_t)(E + 32) * 8, 16);   // selection keys, zero-padded
     p->off_sel = take(256 + 16, 16);   // 32 experts, 32 weights, the inverse RMS
-    p->n_cand = (E + 31) / 32 * k;     // top-k candidates (expert, score), group maxima and sums
+    p->n_cand = (E + 31) / 32 * k;     // top-k candidate keys, group maxima and sums
     p->off_cand = take((size_t)p->n_cand * 8 + 2 * 32 * 4, 16);
     p->off_down = take((size_t)(k + 1) * p->rpc * p->drow_bytes, 128);
     p->off_act = take(((size_t)k * I + (S > 0 ? S : 0)) * 4, 16);

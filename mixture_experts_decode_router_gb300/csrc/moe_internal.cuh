@@ -250,19 +250,21 @@ __device__ __forceinline__ float dot8(const float (&a)[8], const float (&b)[8]) 
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
-// Routing of one token by one thread block: the top-k experts and their
-// weights from the router logits.
+// Routing of one token by one thread block, in two calls: route_select_block
+// (the top-k experts) and route_weights_block (their weights).
 //
-// Selection ranks the score sc[e] (softmax: the logit; sigmoid: sigmoid(l) +
+// Selection ranks the score s[e] (softmax: the logit; sigmoid: sigmoid(l) +
 // bias, the bias only selects): the rank of e is the number of experts ahead
 // of it in (score descending, index ascending) order, and ssel[j] is the
-// expert of rank j < k.  The ranks are exact, in two levels: each group of 32
-// consecutive experts ranks its members by shuffles and keeps its first k as
-// candidates; then each candidate is ranked among all candidates (one warp per
-// candidate, by ballots).  An expert of global rank < k is among its group's
-// first k, and so is every expert ahead of it, so its rank among the
-// candidates is its global rank; any other candidate has the k true top
-// experts ahead of it.
+// expert of rank j < k.  Each expert carries that order as one 64-bit key
+// (route_key: the score's bits made order-preserving above the complemented
+// index), so "ahead" is one integer comparison.  The ranks are exact, in two
+// levels: each group of 32 consecutive experts ranks its members and keeps
+// its first k as candidates; then each candidate is ranked among all
+// candidates (eight threads per candidate, their counts summed by shuffles).
+// An expert of global rank < k is among its group's first k, and so is every
+// expert ahead of it, so its rank among the candidates is its global rank;
+// any other candidate has the k true top experts ahead of it.
 //
 // Weights: softmax p = exp(l - m) / z with m the largest logit and z the sum
 // of exp(l - m) over all E experts, taken as a fixed butterfly within each
@@ -270,64 +272,77 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 // Renormalised over the k selected when norm != 0 (a fixed butterfly), then
 // multiplied by `scale`: sselw[j] is the weight of ssel[j].
 //
-// The result depends on E, k and the logits only (not on the thread count),
-// so every kernel that routes with this function routes alike.
-//   slg, sc            logits and scores [E] (shared memory; NaN scores as -inf)
-//   cand_e, cand_v     ceil(E/32) * k slots each (shared memory)
-//   gmax, zg           ceil(E/32) floats each (shared memory)
-//   on_selected        called by every thread once ssel is complete
-//   sync               the block's barrier (all nthr threads call this function)
-template <typename Sync, typename OnSelected>
-__device__ __forceinline__ void route_block(const float* slg, const float* sc, int E, int k, int routing,
-                                            int norm, float scale, int tid, int nthr, int* cand_e,
-                                            float* cand_v, float* gmax, float* zg, int* ssel, float* sselw,
-                                            Sync sync, OnSelected on_selected) {
+// The results depend on E, k and the logits only (not on the thread count),
+// so every kernel that routes with these functions routes alike.  All nthr
+// threads of the block call each function; `sync` is the block's barrier.
+//   slg            logits [E] (shared memory)
+//   skey           keys [E + 32] (shared memory, 16-byte aligned; entries E..E+31 zero)
+//   cand_k         ceil(E/32) * k slots (shared memory, 16-byte aligned)
+//   gmax, zg       ceil(E/32) floats each (shared memory)
+
+// The selection key of expert e with score s (NaN already replaced by -inf):
+// larger key = ahead.  -0 counts as +0, as equal scores must tie.
+__device__ __forceinline__ unsigned long long route_key(float s, int e) {
+    uint32_t b = __float_as_uint(s + 0.0f);
+    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)b << 32) | (uint32_t)~(uint32_t)e;
+}
+
+template <typename Sync>
+__device__ __forceinline__ void route_select_block(const float* slg, const unsigned long long* skey, int E, int k,
+                                                   int routing, int tid, int nthr, unsigned long long* cand_k,
+                                                   float* gmax, int* ssel, Sync sync) {
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
     const int ngroups = (E + 31) >> 5;
-    const bool softmax = routing == MOE_ROUTE_SOFTMAX;
-    // Level 1, and each group's largest logit.
+    // Level 1, and (softmax) each group's largest logit.  Every real key is
+    // above zero, the padding's.
     for (int g = warp; g < ngroups; g += nwarps) {
         const int e = 32 * g + lane;
-        const int nvalid = min(32, E - 32 * g);
-        const float v = lane < nvalid ? sc[e] : 0.f;
+        const unsigned long long kv = skey[e];
+        const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(skey + 32 * g);
         int rank = 0;
-        for (int j = 0; j < nvalid; ++j) {
-            const float u = __shfl_sync(0xffffffffu, v, j);
-            rank += (u > v || (u == v && j < lane)) ? 1 : 0;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const ulonglong2 u = k2[q];
+            rank += (u.x > kv ? 1 : 0) + (u.y > kv ? 1 : 0);
         }
-        if (lane < nvalid && rank < k) {
-            cand_e[g * k + rank] = e;
-            cand_v[g * k + rank] = v;
-        }
-        if (lane < k && lane >= nvalid) cand_e[g * k + lane] = -1;   // slots no member fills
-        if (softmax) {
-            float m = lane < nvalid ? slg[e] : -INFINITY;
+        const bool valid = e < E;
+        if (valid && rank < k) cand_k[g * k + rank] = kv;
+        const int nvalid = min(32, E - 32 * g);
+        if (lane < k && lane >= nvalid) cand_k[g * k + lane] = 0ull;   // slots no member fills
+        if (routing == MOE_ROUTE_SOFTMAX) {
+            float m = valid ? slg[e] : -INFINITY;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
             if (lane == 0) gmax[g] = m;
         }
     }
     sync();
-    // Level 2: one warp per candidate.
+    // Level 2: 4 candidates per warp per pass, 8 lanes each.
     const int nc = ngroups * k;
-    for (int c = warp; c < nc; c += nwarps) {
-        const int e = cand_e[c];
-        if (e < 0) continue;
-        const float v = cand_v[c];
+    for (int q0 = warp * 4; q0 < nc; q0 += nwarps * 4) {
+        const int c = q0 + (lane >> 3), part = lane & 7;
+        const unsigned long long kv = c < nc ? cand_k[c] : 0ull;
         int cnt = 0;
-        for (int c0 = 0; c0 < nc; c0 += 32) {
-            const int c2 = c0 + lane;
-            bool ahead = false;
-            if (c2 < nc) {
-                const int e2 = cand_e[c2];
-                const float u = cand_v[c2];
-                ahead = e2 >= 0 && (u > v || (u == v && e2 < e));
-            }
-            cnt += __popc(__ballot_sync(0xffffffffu, ahead));
+        if (kv != 0ull) {
+#pragma unroll 4
+            for (int c2 = part; c2 < nc; c2 += 8) cnt += cand_k[c2] > kv ? 1 : 0;
         }
-        if (lane == 0 && cnt < k) ssel[cnt] = e;
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, 4);
+        if (kv != 0ull && part == 0 && cnt < k) ssel[cnt] = (int)~(uint32_t)kv;
     }
-    // The softmax normaliser, one group per warp.
+    sync();
+}
+
+template <typename Sync>
+__device__ __forceinline__ void route_weights_block(const float* slg, int E, int k, int routing, int norm,
+                                                    float scale, int tid, int nthr, const float* gmax, float* zg,
+                                                    const int* ssel, float* sselw, Sync sync) {
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+    const int ngroups = (E + 31) >> 5;
+    const bool softmax = routing == MOE_ROUTE_SOFTMAX;
     float mx = 0.f;
     if (softmax) {
         mx = lane < ngroups ? gmax[lane] : -INFINITY;
@@ -339,9 +354,8 @@ __device__ __forceinline__ void route_block(const float* slg, const float* sc, i
             z = warp_sum(z);
             if (lane == 0) zg[g] = z;
         }
+        sync();
     }
-    sync();
-    on_selected();
     if (warp == 0) {
         const int sel_e = lane < k ? ssel[lane] : -1;
         const float sel_l = lane < k ? slg[sel_e] : 0.f;

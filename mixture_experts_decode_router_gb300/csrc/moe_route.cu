@@ -189,35 +189,41 @@ cudaError_t launch_router_nvfp4(const uint16_t* x, int n, int H, const QMatDev& 
     return cudaGetLastError();
 }
 
-// One CTA per token row: selection and weights by route_block (exact ranks,
-// fixed-order softmax normaliser), which the single-token kernel also uses.
+// One CTA per token row: selection and weights by route_select_block and
+// route_weights_block (exact ranks, fixed-order softmax normaliser), which the
+// single-token kernel also uses.
 __global__ void __launch_bounds__(256)
 topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int routing,
                   const float* __restrict__ bias, int norm, float scale,
                   int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
     extern __shared__ float smf[];
-    float* slg = smf;          // [E]
-    float* ssc = smf + E;      // [E]
+    float* slg = smf;                                                    // [E]
+    unsigned long long* skey =
+        reinterpret_cast<unsigned long long*>(smf + ((E + 3) & ~3));     // [E + 32], 16-byte aligned
     __shared__ int ssel[kMaxTopK];
     __shared__ float sselw[kMaxTopK];
-    __shared__ int cand_e[kMaxExperts / 32 * kMaxTopK];
-    __shared__ float cand_v[kMaxExperts / 32 * kMaxTopK];
+    __shared__ __align__(16) unsigned long long cand_k[kMaxExperts / 32 * kMaxTopK];
     __shared__ float gmax[kMaxExperts / 32], zg[kMaxExperts / 32];
     const int t = blockIdx.x, tid = threadIdx.x;
     const float* lrow = logits + (size_t)t * E;
     pdl_wait();
-    for (int e = tid; e < E; e += blockDim.x) {
-        const float l = lrow[e];
-        float sc;
-        if (routing == MOE_ROUTE_SOFTMAX) sc = l;
-        else sc = 1.0f / (1.0f + expf(-l)) + bias[e];
-        if (sc != sc) sc = -INFINITY;
-        slg[e] = l;
-        ssc[e] = sc;
+    for (int e = tid; e < E + 32; e += blockDim.x) {
+        if (e < E) {
+            const float l = lrow[e];
+            float sc;
+            if (routing == MOE_ROUTE_SOFTMAX) sc = l;
+            else sc = 1.0f / (1.0f + expf(-l)) + bias[e];
+            if (sc != sc) sc = -INFINITY;
+            slg[e] = l;
+            skey[e] = route_key(sc, e);
+        } else {
+            skey[e] = 0ull;
+        }
     }
     __syncthreads();
-    route_block(slg, ssc, E, k, routing, norm, scale, tid, blockDim.x, cand_e, cand_v, gmax, zg, ssel, sselw,
-                [] { __syncthreads(); }, [] {});
+    route_select_block(slg, skey, E, k, routing, tid, blockDim.x, cand_k, gmax, ssel, [] { __syncthreads(); });
+    route_weights_block(slg, E, k, routing, norm, scale, tid, blockDim.x, gmax, zg, ssel, sselw,
+                        [] { __syncthreads(); });
     if (tid < k) {
         idx_out[(size_t)t * k + tid] = ssel[tid];
         w_out[(size_t)t * k + tid] = sselw[tid];
@@ -282,9 +288,9 @@ cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, i
 
 cudaError_t launch_topk(const float* logits, int n, int E, int k, int routing, const float* bias,
                         int norm, float scale, int32_t* idx, float* w, cudaStream_t st) {
-    // 2 E floats of shared memory (<= 8 KB for E <= 1024).
-    launch_pdl(topk_block_kernel, n, 256, 2 * E * sizeof(float), st, logits, n, E, k, routing, bias, norm, scale, idx,
-                                                             w);
+    // Logits and keys: ~12 E + 272 bytes of shared memory (<= 13 KB for E <= 1024).
+    const size_t smem = (size_t)((E + 3) & ~3) * sizeof(float) + (size_t)(E + 32) * sizeof(unsigned long long);
+    launch_pdl(topk_block_kernel, n, 256, smem, st, logits, n, E, k, routing, bias, norm, scale, idx, w);
     return cudaGetLastError();
 }
 
