@@ -53,6 +53,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` (it resumes as soon
+// as the phase completes), so a long wait costs few issue slots.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with `parity` to complete.  Returns false (after setting
 // *err and *abort) when the wait outlives kWaitLimitNs or another role of the
 // CTA has aborted.
@@ -61,8 +73,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 63) {
+        if (mbar_try_wait_hint(bar, parity, 100000u)) return true;   // up to 0.1 ms asleep
+        if ((i & 3) == 3) {
             if (*abort) return false;
             if (globaltimer() - t0 > kWaitLimitNs) {
                 atomicExch(err, code);
