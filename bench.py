@@ -78,9 +78,9 @@ def _src_hash(files) -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic(kernel: str, workload: str):
-    """dram bytes per launch of `kernel` from the committed ncu summary, or None
-    when the kernel's source changed since it was captured."""
+def _ncu_entry(kernel: str, workload: str):
+    """The committed ncu figures of `kernel` on `workload`, or None when the
+    kernel's source changed since they were captured."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     try:
         with open(path) as f:
@@ -95,7 +95,20 @@ def _traffic(kernel: str, workload: str):
             return None
     except OSError:
         return None
-    return float(ent["dram_bytes_per_launch"])
+    return ent
+
+
+def _traffic(kernel: str, workload: str):
+    """dram bytes per launch of `kernel` from the committed ncu summary, or None."""
+    ent = _ncu_entry(kernel, workload)
+    return float(ent["dram_bytes_per_launch"]) if ent else None
+
+
+def _tensor_pipe(kernel: str, workload: str):
+    """Tensor-pipe active % of `kernel` from the committed ncu summary, or None."""
+    ent = _ncu_entry(kernel, workload)
+    v = ent.get("tensor_pipe_active_pct") if ent else None
+    return float(v) if v is not None else None
 
 
 class ClockSampler:
@@ -459,6 +472,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": _traffic(dom, cfg.name),
+                         "tensor_pipe_active_pct": _tensor_pipe(dom, cfg.name),
                          "alg_bytes_per_launch": int(alg[dom]),
                          "avg_launch_us": round(dom_ms * 1e3, 3)},
             "e2e": {"value": round(whole_job_tokens_per_s(world, n, Ke, e2e_ms), 2), "unit": "tokens/s",
