@@ -56,7 +56,11 @@ struct TcCfg {
     static constexpr int kRawRow = FMT == MOE_W_FP8_B128 ? BK : (FMT == MOE_W_NVFP4 ? BK / 2 : 0);
     static constexpr int kRawMat = BM * kRawRow;
     static constexpr int kRawStage = kMats * kRawMat;
-    static constexpr int kAStages = kDeq ? (GU ? 4 : 7) : (GU ? 5 : 8);
+    static constexpr int kAStages = kDeq ? (GU ? 4 : 6) : (GU ? 5 : 8);
+    // Dequantised tiles hand operand stages to the MMA warp in groups of two
+    // (one barrier round trip per 128 K instead of per 64).
+    static constexpr int kGrp = kDeq ? 2 : 1;
+    static constexpr int kAGroups = kAStages / kGrp;
     // Dequantised tiles: the token (B) tiles have a ring of their own, so they
     // are fetched ahead instead of after the MMA frees an A slot.
     static constexpr int kBStages = kDeq ? (GU ? 4 : 6) : kAStages;
@@ -83,6 +87,7 @@ struct TcCfg {
     static constexpr int kSmem = kOffMisc + 16 + 1024;   // + alignment slack
     static_assert(kSmem <= 232448, "shared memory budget");
     static_assert(kTmemCols <= 512, "TMEM budget");
+    static_assert(kAStages % kGrp == 0, "operand stages come in whole groups");
 };
 
 struct Tile {
@@ -209,7 +214,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kAStages; ++s) {
+        for (int s = 0; s < C::kAGroups; ++s) {
             ptx::mbar_init(&a_full[s], C::kDeq ? C::kDeqWarps : 1);
             ptx::mbar_init(&a_empty[s], 1);
         }
@@ -295,7 +300,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                     }
                     ptx::cp_async_mbar_arrive(&raw_full[rs]);
                 } else {
-                    const int as = it % C::kAStages;
+                    const int as = it % C::kAStages;   // kGrp == 1: a group is a stage
                     if (!ptx::mbar_wait_warp(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 1)) {
                         stop = true;
                         break;
@@ -357,7 +362,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp runs the loop, so the operand descriptors are
         // warp-uniform values; one elected lane issues the MMAs and commits.
-        uint32_t it = 0, acc_it = 0;
+        uint32_t it = 0, git = 0, acc_it = 0;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x, ++acc_it) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
             const int ab = acc_it & 1;
@@ -368,30 +373,36 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             const uint32_t d0 = tmem + ab * C::kAccCols;
             const int KB = (t.K + BK - 1) / BK;
             bool ok = true;
-            for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int as = it % C::kAStages;
-                const int bs = C::kDeq ? (int)(it % C::kBStages) : as;
-                if (!ptx::mbar_wait_warp(&a_full[as], (it / C::kAStages) & 1, s_abort, err, 2)) { ok = false; break; }
-                if constexpr (C::kDeq)
-                    if (!ptx::mbar_wait_warp(&b_full[bs], (it / C::kBStages) & 1, s_abort, err, 2)) {
-                        ok = false;
-                        break;
+            for (int kb = 0; kb < KB && ok; ++git) {
+                // One group of operand stages: one a_full wait, one a_empty commit.
+                const int g = git % C::kAGroups;
+                if (!ptx::mbar_wait_warp(&a_full[g], (git / C::kAGroups) & 1, s_abort, err, 2)) { ok = false; break; }
+                const int n = min(C::kGrp, KB - kb);
+                for (int u = 0; u < n; ++u, ++kb, ++it) {
+                const int as = g * C::kGrp + u;
+                    const int bs = C::kDeq ? (int)(it % C::kBStages) : as;
+                    if constexpr (C::kDeq)
+                        if (!ptx::mbar_wait_warp(&b_full[bs], (it / C::kBStages) & 1, s_abort, err, 2)) {
+                            ok = false;
+                            break;
+                        }
+                    ptx::tc_fence_after();
+                    // Descriptors of the stage's first K step; a later step (or the
+                    // second matrix) only moves the start address field (16-byte units).
+                    const uint64_t a_desc = ptx::sw128_desc(ptx::smem_u32(sA + as * C::kAStage));
+                    const uint64_t b_desc = ptx::sw128_desc(ptx::smem_u32(sB + bs * C::kBStage));
+                    if (ptx::elect_one()) {
+    #pragma unroll
+                        for (int m = 0; m < C::kMats; ++m)
+    #pragma unroll
+                            for (int kk = 0; kk < BK / 16; ++kk)
+                                ptx::mma_f16(d0 + m * NT, a_desc + (uint64_t)((m * C::kAMat + kk * 32) >> 4),
+                                             b_desc + (uint64_t)((kk * 32) >> 4), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        if constexpr (C::kDeq) ptx::mma_commit(&b_empty[bs]);
                     }
-                ptx::tc_fence_after();
-                // Descriptors of the stage's first K step; a later step (or the
-                // second matrix) only moves the start address field (16-byte units).
-                const uint64_t a_desc = ptx::sw128_desc(ptx::smem_u32(sA + as * C::kAStage));
-                const uint64_t b_desc = ptx::sw128_desc(ptx::smem_u32(sB + bs * C::kBStage));
-                if (ptx::elect_one()) {
-#pragma unroll
-                    for (int m = 0; m < C::kMats; ++m)
-#pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            ptx::mma_f16(d0 + m * NT, a_desc + (uint64_t)((m * C::kAMat + kk * 32) >> 4),
-                                         b_desc + (uint64_t)((kk * 32) >> 4), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                    ptx::mma_commit(&a_empty[as]);
-                    if constexpr (C::kDeq) ptx::mma_commit(&b_empty[bs]);
+                    __syncwarp();
                 }
+                if (ptx::elect_one()) ptx::mma_commit(&a_empty[g]);   // after the group's MMAs
                 __syncwarp();
             }
             if (!ok) break;
@@ -484,97 +495,103 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         constexpr int kDT = C::kDeqWarps * 32;
         static_assert(512 % kDT == 0, "dequant threads divide the 512 chunks");
         const int dt = threadIdx.x - 6 * 32;
-        uint32_t it = 0;
+        uint32_t it = 0, git = 0;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
             const bool sh = t.e < 0;
             const int KB = (t.K + BK - 1) / BK;
             bool ok = true;
-            for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int rs = it % C::kRawStages, as = it % C::kAStages;
-                if (!ptx::mbar_wait_warp(&raw_full[rs], (it / C::kRawStages) & 1, s_abort, err, 4)) { ok = false; break; }
-                if (!ptx::mbar_wait_warp(&a_empty[as], ((it / C::kAStages) & 1) ^ 1, s_abort, err, 4)) { ok = false; break; }
-                const int k0 = kb * BK;
-                for (int m = 0; m < C::kMats; ++m) {
-                    const uint8_t* raw = sRaw + rs * C::kRawStage + m * C::kRawMat;
-                    const uint32_t a_mat = ptx::smem_u32(sA + as * C::kAStage + m * C::kAMat);
-                    if constexpr (FMT == MOE_W_FP8_B128) {
-                        // One fp32 scale per 128x128 block: uniform over this stage
-                        // (fetched into shared memory with the codes).
-                        const float s = reinterpret_cast<const float*>(sScale + rs * C::kScaleStage)[m];
-                        // In f16's normal range the product is formed in f16x2 (the
-                        // scale and the product each rounded once to f16); else in fp32.
-                        const bool f16_scale = s >= 6.2e-5f && s <= 128.0f;
-                        const __half2 s2 = __float2half2_rn(s);
-                        const uint32_t s2u = *reinterpret_cast<const uint32_t*>(&s2);
-#pragma unroll
-                        for (int c = 0; c < 512 / kDT; ++c) {
-                            const int qd = dt + c * kDT;
-                            const int r = qd >> 2, ch = qd & 3;    // row, 16-byte chunk of codes
-                            const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 64 + ch * 16);
-                            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                            uint32_t o[8];
-                            if (f16_scale) {
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    uint32_t h[2];
-                                    e4m3x4_to_f16x2x2(w4[i], h);
-                                    o[2 * i] = f16x2_mul(h[0], s2u);
-                                    o[2 * i + 1] = f16x2_mul(h[1], s2u);
+            for (int kb = 0; kb < KB && ok; ++git) {
+                // A group of kGrp operand stages (fewer at the end of the tile).
+                const int g = git % C::kAGroups;
+                if (!ptx::mbar_wait_warp(&a_empty[g], ((git / C::kAGroups) & 1) ^ 1, s_abort, err, 4)) { ok = false; break; }
+                const int n = min(C::kGrp, KB - kb);
+                for (int u = 0; u < n; ++u, ++kb, ++it) {
+                const int rs = it % C::kRawStages, as = g * C::kGrp + u;
+                    if (!ptx::mbar_wait_warp(&raw_full[rs], (it / C::kRawStages) & 1, s_abort, err, 4)) { ok = false; break; }
+                    const int k0 = kb * BK;
+                    for (int m = 0; m < C::kMats; ++m) {
+                        const uint8_t* raw = sRaw + rs * C::kRawStage + m * C::kRawMat;
+                        const uint32_t a_mat = ptx::smem_u32(sA + as * C::kAStage + m * C::kAMat);
+                        if constexpr (FMT == MOE_W_FP8_B128) {
+                            // One fp32 scale per 128x128 block: uniform over this stage
+                            // (fetched into shared memory with the codes).
+                            const float s = reinterpret_cast<const float*>(sScale + rs * C::kScaleStage)[m];
+                            // In f16's normal range the product is formed in f16x2 (the
+                            // scale and the product each rounded once to f16); else in fp32.
+                            const bool f16_scale = s >= 6.2e-5f && s <= 128.0f;
+                            const __half2 s2 = __float2half2_rn(s);
+                            const uint32_t s2u = *reinterpret_cast<const uint32_t*>(&s2);
+    #pragma unroll
+                            for (int c = 0; c < 512 / kDT; ++c) {
+                                const int qd = dt + c * kDT;
+                                const int r = qd >> 2, ch = qd & 3;    // row, 16-byte chunk of codes
+                                const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 64 + ch * 16);
+                                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                                uint32_t o[8];
+                                if (f16_scale) {
+    #pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        uint32_t h[2];
+                                        e4m3x4_to_f16x2x2(w4[i], h);
+                                        o[2 * i] = f16x2_mul(h[0], s2u);
+                                        o[2 * i + 1] = f16x2_mul(h[1], s2u);
+                                    }
+                                } else {
+    #pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        const float2 lo = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] & 0xffffu));
+                                        const float2 hi = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] >> 16));
+                                        o[2 * i] = pack_f16(lo.x * s, lo.y * s);
+                                        o[2 * i + 1] = pack_f16(hi.x * s, hi.y * s);
+                                    }
                                 }
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const float2 lo = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] & 0xffffu));
-                                    const float2 hi = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] >> 16));
-                                    o[2 * i] = pack_f16(lo.x * s, lo.y * s);
-                                    o[2 * i + 1] = pack_f16(hi.x * s, hi.y * s);
+                                const uint32_t rowb = a_mat + r * 128;
+                                st_shared_v4(rowb + (((2 * ch) ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
+                                st_shared_v4(rowb + (((2 * ch + 1) ^ (r & 7)) << 4), o[4], o[5], o[6], o[7]);
+                            }
+                        } else {
+                            // NVFP4: a chunk is one 16-code scale block (8 bytes).
+    #pragma unroll
+                            for (int c = 0; c < 512 / kDT; ++c) {
+                                const int qd = dt + c * kDT;
+                                const int r = qd >> 2, q = qd & 3;     // row, scale block of the stage
+                                const uint2 v = *reinterpret_cast<const uint2*>(raw + r * 32 + q * 8);
+                                const int kc = k0 + 16 * q;
+                                const int mrow = t.m0 + r;
+                                uint32_t sc = 0;   // f16x2 of the block scale (0 outside the matrix)
+                                if (t.K % 64 == 0) {
+                                    // Fetched into shared memory with the codes (0 past the last row).
+                                    const uint32_t w = reinterpret_cast<const uint32_t*>(sScale + rs * C::kScaleStage)[m * BM + r];
+                                    const uint32_t b = (w >> (8 * q)) & 0xffu;
+                                    sc = e4m3x2_to_f16x2(b | (b << 8));
+                                } else if (mrow < t.out && kc < t.K) {
+                                    const uint8_t* sp = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]) +
+                                                        ((size_t)t.le * t.out + mrow) * (t.K / 16) + kc / 16;
+                                    const uint32_t b = __ldg(sp);
+                                    sc = e4m3x2_to_f16x2(b | (b << 8));
                                 }
+                                uint32_t lo[4], hi[4];
+                                e2m1x8_to_f16x2x4(v.x, lo);
+                                e2m1x8_to_f16x2x4(v.y, hi);
+    #pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    lo[i] = f16x2_mul(lo[i], sc);
+                                    hi[i] = f16x2_mul(hi[i], sc);
+                                }
+                                const uint32_t rowb = a_mat + r * 128;
+                                st_shared_v4(rowb + (((2 * q) ^ (r & 7)) << 4), lo[0], lo[1], lo[2], lo[3]);
+                                st_shared_v4(rowb + (((2 * q + 1) ^ (r & 7)) << 4), hi[0], hi[1], hi[2], hi[3]);
                             }
-                            const uint32_t rowb = a_mat + r * 128;
-                            st_shared_v4(rowb + (((2 * ch) ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
-                            st_shared_v4(rowb + (((2 * ch + 1) ^ (r & 7)) << 4), o[4], o[5], o[6], o[7]);
-                        }
-                    } else {
-                        // NVFP4: a chunk is one 16-code scale block (8 bytes).
-#pragma unroll
-                        for (int c = 0; c < 512 / kDT; ++c) {
-                            const int qd = dt + c * kDT;
-                            const int r = qd >> 2, q = qd & 3;     // row, scale block of the stage
-                            const uint2 v = *reinterpret_cast<const uint2*>(raw + r * 32 + q * 8);
-                            const int kc = k0 + 16 * q;
-                            const int mrow = t.m0 + r;
-                            uint32_t sc = 0;   // f16x2 of the block scale (0 outside the matrix)
-                            if (t.K % 64 == 0) {
-                                // Fetched into shared memory with the codes (0 past the last row).
-                                const uint32_t w = reinterpret_cast<const uint32_t*>(sScale + rs * C::kScaleStage)[m * BM + r];
-                                const uint32_t b = (w >> (8 * q)) & 0xffu;
-                                sc = e4m3x2_to_f16x2(b | (b << 8));
-                            } else if (mrow < t.out && kc < t.K) {
-                                const uint8_t* sp = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]) +
-                                                    ((size_t)t.le * t.out + mrow) * (t.K / 16) + kc / 16;
-                                const uint32_t b = __ldg(sp);
-                                sc = e4m3x2_to_f16x2(b | (b << 8));
-                            }
-                            uint32_t lo[4], hi[4];
-                            e2m1x8_to_f16x2x4(v.x, lo);
-                            e2m1x8_to_f16x2x4(v.y, hi);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                lo[i] = f16x2_mul(lo[i], sc);
-                                hi[i] = f16x2_mul(hi[i], sc);
-                            }
-                            const uint32_t rowb = a_mat + r * 128;
-                            st_shared_v4(rowb + (((2 * q) ^ (r & 7)) << 4), lo[0], lo[1], lo[2], lo[3]);
-                            st_shared_v4(rowb + (((2 * q + 1) ^ (r & 7)) << 4), hi[0], hi[1], hi[2], hi[3]);
                         }
                     }
                 }
+                if (!ok) break;
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    ptx::mbar_arrive(&raw_empty[rs]);
-                    ptx::mbar_arrive(&a_full[as]);
+                    for (int u = 0; u < n; ++u) ptx::mbar_arrive(&raw_empty[(it - n + u) % C::kRawStages]);
+                    ptx::mbar_arrive(&a_full[g]);
                 }
             }
             if (!ok) break;
