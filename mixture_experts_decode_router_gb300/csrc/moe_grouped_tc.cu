@@ -379,7 +379,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                 if (!ptx::mbar_wait_warp(&a_full[g], (git / C::kAGroups) & 1, s_abort, err, 2)) { ok = false; break; }
                 const int n = min(C::kGrp, KB - kb);
                 for (int u = 0; u < n; ++u, ++kb, ++it) {
-                const int as = g * C::kGrp + u;
+                    const int as = g * C::kGrp + u;
                     const int bs = C::kDeq ? (int)(it % C::kBStages) : as;
                     if constexpr (C::kDeq)
                         if (!ptx::mbar_wait_warp(&b_full[bs], (it / C::kBStages) & 1, s_abort, err, 2)) {
@@ -507,7 +507,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                 if (!ptx::mbar_wait_warp(&a_empty[g], ((git / C::kAGroups) & 1) ^ 1, s_abort, err, 4)) { ok = false; break; }
                 const int n = min(C::kGrp, KB - kb);
                 for (int u = 0; u < n; ++u, ++kb, ++it) {
-                const int rs = it % C::kRawStages, as = g * C::kGrp + u;
+                    const int rs = it % C::kRawStages, as = g * C::kGrp + u;
                     if (!ptx::mbar_wait_warp(&raw_full[rs], (it / C::kRawStages) & 1, s_abort, err, 4)) { ok = false; break; }
                     const int k0 = kb * BK;
                     for (int m = 0; m < C::kMats; ++m) {
