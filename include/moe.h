@@ -265,7 +265,7 @@ moe_status_t moe_forward_static_ws(const moe_config_t* cfg, const moe_weights_t*
  * single-token kernel's barrier word (which a call that ended early leaves
  * non-zero), so the workspace serves the next call.  Synchronises `stream`
  * (the only entry point that does).
- *   device_error (out)  0: no failure since the last check; 11-16: a bounded
+ *   device_error (out)  0: no failure since the last check; 11-17: a bounded
  *                       wait of the single-token kernel gave up; 1-5: a bounded
  *                       wait of the grouped tensor-core kernels gave up; 20: the
  *                       workspace control block was not zeroed before use.

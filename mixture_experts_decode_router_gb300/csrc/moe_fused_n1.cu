@@ -81,7 +81,8 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
     uint64_t* dfull = bars;
     uint64_t* dshfull = bars + 1;
     uint64_t* sel_ready = bars + 2;
-    volatile int* abort_f = reinterpret_cast<volatile int*>(bars + 3);
+    uint64_t* shgu_full = bars + 3;
+    volatile int* abort_f = reinterpret_cast<volatile int*>(bars + 4);
     volatile int* s_go = abort_f + 1;   // phase decision, written by tid 0 before a barrier
     Ctrl* ctrl = p.ctrl;
     int32_t* err = &ctrl->err;
@@ -97,6 +98,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
         ptx::mbar_init(dfull, 1);
         ptx::mbar_init(dshfull, 1);
         ptx::mbar_init(sel_ready, 1);
+        ptx::mbar_init(shgu_full, 1);
         ptx::fence_mbar_init();
     }
     // Router row of this warp (r == E: the shared-gate row): its first chunks
@@ -156,7 +158,17 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
         // ------------------------------------------------------------ copy producer
         if (lane == 0) {
             bool ok = true;
-            // Shared down slice (routing-independent), then the routed ones.
+            // The CTA's shared gate/up rows (needed first), the shared down
+            // slice (routing-independent), then the routed down slices.
+            uint8_t* sshgu = sm + p.off_shgu;
+            if (S > 0 && n_sh > 0) {
+                const uint32_t bytes = (uint32_t)n_sh * p.row_bytes;
+                ptx::mbar_arrive_expect_tx(shgu_full, 2 * bytes);
+                ptx::bulk_load(sshgu, row_ptr<FMT>(p.sh_gate, 0, sh_b), bytes, shgu_full);
+                ptx::bulk_load(sshgu + bytes, row_ptr<FMT>(p.sh_up, 0, sh_b), bytes, shgu_full);
+            } else {
+                ptx::mbar_arrive(shgu_full);
+            }
             if (S > 0 && nrows > 0) {
                 ptx::mbar_arrive_expect_tx(dshfull, nrows * p.dsh_row_bytes);
                 ptx::bulk_load(sdown + (size_t)k * rpc * p.drow_bytes, row_ptr<FMT>(p.sh_down, 0, h0),
@@ -178,6 +190,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                 ptx::mbar_arrive(dfull);
             } else {
                 // Let the copies issued land before the CTA exits.
+                ptx::mbar_wait_quiet(shgu_full, 0, 100000000ull);
                 ptx::mbar_wait_quiet(dshfull, 0, 100000000ull);
             }
         }
@@ -244,11 +257,38 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
             if (lane == 0) *dst = silu(g) * u;
         };
 
-        // Phase 0b: the shared expert's gate/up rows of this CTA.
+        // Phase 0b: the shared expert's gate/up rows of this CTA, from the copy
+        // the producer started at kernel entry (the same arithmetic as consume).
         const float msg_sh = S > 0 ? matrix_scale<FMT>(p.sh_gate, 0) : 1.f;
         const float msu_sh = S > 0 ? matrix_scale<FMT>(p.sh_up, 0) : 1.f;
-        for (int s = warp; s < n_sh; s += kFComputeWarps)
-            consume(p.sh_gate, p.sh_up, 0, sh_b + s, msg_sh, msu_sh, p.act_sh + sh_b + s);
+        if (warp < n_sh && ptx::mbar_wait_warp(shgu_full, 0, abort_f, err, 17)) {
+            const uint8_t* sshgu = sm + p.off_shgu;
+            for (int s = warp; s < n_sh; s += kFComputeWarps) {
+                const uint8_t* grow = sshgu + (size_t)s * p.row_bytes;
+                const uint8_t* urow = sshgu + (size_t)(n_sh + s) * p.row_bytes;
+                const int row = sh_b + s;
+                float ag = 0.f, au = 0.f;
+                for (int c0 = lane; c0 < C; c0 += 32 * kSeg) {
+#pragma unroll
+                    for (int i = 0; i < kSeg; ++i) {
+                        const int c = c0 + 32 * i;
+                        if (c < C) {
+                            float wg[8], wu[8], xv[8];
+                            decode_at<FMT>(grow, c, wg);
+                            decode_at<FMT>(urow, c, wu);
+                            WChunk<FMT> sch;
+                            const float sg = sch.scale(p.sh_gate, 0, row, c), su = sch.scale(p.sh_up, 0, row, c);
+                            bf16x8_to_float(reinterpret_cast<const uint4*>(sxe)[c], xv);
+                            ag = fmaf(dot8(wg, xv), sg, ag);
+                            au = fmaf(dot8(wu, xv), su, au);
+                        }
+                    }
+                }
+                const float g = warp_sum(ag) * msg_sh;
+                const float u = warp_sum(au) * msu_sh;
+                if (lane == 0) p.act_sh[row] = silu(g) * u;
+            }
+        }
 
         // Grid barrier 1: every logit is written.
         ptx::named_bar(1, kFCompute);
@@ -493,8 +533,10 @@ bool fused_plan(const moe_config_t* c, int num_sms, FusedParams* p) {
     p->off_down = take((size_t)(k + 1) * p->rpc * p->drow_bytes, 128);
     p->off_act = take(((size_t)k * I + (S > 0 ? S : 0)) * 4, 16);
     p->off_part = take((size_t)(k + (S > 0 ? 1 : 0)) * p->rpc * 32 * 4, 16);   // phase-2 lane partials
-    // dfull, dshfull, sel_ready, abort + phase flags
-    p->off_bar = take(3 * 8 + 16, 8);
+    // The CTA's shared gate and up rows: at most ceil(S / #SM) of each.
+    p->off_shgu = take((size_t)2 * ((S + num_sms - 1) / num_sms) * p->row_bytes, 128);
+    // dfull, dshfull, sel_ready, shgu_full, abort + phase flags
+    p->off_bar = take(4 * 8 + 16, 8);
     p->smem_bytes = (uint32_t)off;
     return off <= 227 * 1024 && k <= 32 && (size_t)k * p->rpc * p->drow_bytes < (1u << 20);
 }

@@ -97,7 +97,8 @@ struct FusedParams {
     Ctrl* ctrl;
     int rpc;                  // output columns per CTA
     uint32_t row_bytes, drow_bytes, dsh_row_bytes;
-    uint32_t off_x, off_xe, off_lg, off_sc, off_sel, off_cand, off_down, off_act, off_part, off_bar, smem_bytes;
+    uint32_t off_x, off_xe, off_lg, off_sc, off_sel, off_cand, off_down, off_act, off_part, off_shgu, off_bar,
+        smem_bytes;
     int n_cand;
 };
 
