@@ -98,26 +98,40 @@ router_tiled_kernel(const uint16_t* __restrict__ x, int n, int H,
     for (int a = 0; a < RE; ++a)
 #pragma unroll
         for (int b = 0; b < RT; ++b) acc[a][b] = 0.f;
-#pragma unroll 2
-    for (int c = lane; c < C; c += 32) {
-        uint4 wv4[RE], xv4[RT];
+    // The router chunks of KB consecutive steps (lane, lane+32, ...) are all
+    // requested before any is used, so a warp has RE*KB 16-byte loads of its
+    // rows in flight; the token rows come from L1/L2.
+    constexpr int KB = RE >= 4 ? 2 : 8 / RE;
+    for (int c0 = lane; c0 < C; c0 += 32 * KB) {
+        uint4 wv4[RE][KB];
 #pragma unroll
-        for (int a = 0; a < RE; ++a) wv4[a] = __ldg(reinterpret_cast<const uint4*>(wrow[a]) + c);
+        for (int q = 0; q < KB; ++q) {
+            const int c = c0 + 32 * q;
 #pragma unroll
-        for (int b = 0; b < RT; ++b)
-            xv4[b] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)min(t0 + b, n - 1) * H) + c);
+            for (int a = 0; a < RE; ++a)
+                wv4[a][q] = c < C ? __ldg(reinterpret_cast<const uint4*>(wrow[a]) + c) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-        for (int b = 0; b < RT; ++b) {
-            float xv[8];
-            bf16x8_to_float(xv4[b], xv);
+        for (int q = 0; q < KB; ++q) {
+            const int c = c0 + 32 * q;
+            if (c >= C) break;
+            uint4 xv4[RT];
 #pragma unroll
-            for (int a = 0; a < RE; ++a) {
-                float wv[8];
-                bf16x8_to_float(wv4[a], wv);
-                float s = acc[a][b];
+            for (int b = 0; b < RT; ++b)
+                xv4[b] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)min(t0 + b, n - 1) * H) + c);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) s = fmaf(wv[i], xv[i], s);
-                acc[a][b] = s;
+            for (int b = 0; b < RT; ++b) {
+                float xv[8];
+                bf16x8_to_float(xv4[b], xv);
+#pragma unroll
+                for (int a = 0; a < RE; ++a) {
+                    float wv[8];
+                    bf16x8_to_float(wv4[a][q], wv);
+                    float s = acc[a][b];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) s = fmaf(wv[i], xv[i], s);
+                    acc[a][b] = s;
+                }
             }
         }
     }
