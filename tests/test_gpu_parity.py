@@ -13,6 +13,8 @@
   partials summed (plus one shared-expert-only call) against the whole layer.
 """
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -149,6 +151,44 @@ def test_route_and_experts_entry_points(norm, router):
     rms_o = np.sqrt(np.mean(ref ** 2))
     assert np.max(np.abs(out.float().cpu().numpy() - ref)) <= 2e-2 * rms_o
     assert torch.equal(own, fwd)
+
+
+@pytest.mark.parametrize("routing", [synth.ROUTE_SOFTMAX, synth.ROUTE_SIGMOID_BIAS])
+@pytest.mark.parametrize("n", [1, 3, 16])
+def test_exact_ties_go_to_the_lower_index(routing, n):
+    """Two experts with identical, dominant router rows (and equal biases) tie
+    exactly on every token: the lower index takes the single slot (k = 1) on
+    every path.  An all-zero router ties all experts: slots 0..k-1 in order."""
+    cfg = small("ties", num_experts=16, top_k=1, routing=routing,
+                routed_scaling_factor=1.0 if routing == synth.ROUTE_SOFTMAX else 2.5)
+    lw = synth.make_weights(cfg, "cuda")
+    for lo, hi in ((0, 1), (2, 5), (9, 14)):
+        router = lw.router_w.clone()
+        router[hi] = router[lo] = (lw.router_w[lo].float() * 40).to(torch.bfloat16)
+        bias = lw.correction_bias.clone() if lw.correction_bias is not None else None
+        if bias is not None:
+            bias[hi] = bias[lo]
+        tied = dataclasses.replace(lw, router_w=router, correction_bias=bias)
+        x = synth.make_input(cfg, n, "cuda")
+        # Make the tied experts dominate: x along their (shared) router row.
+        x = (x.float() * 0.1 + router[lo].float() / router[lo].float().norm()).to(torch.bfloat16)
+        out, idx, w = MoeLayer(tied, n).forward(x)
+        torch.cuda.synchronize()
+        assert torch.all(idx == lo), (lo, hi, idx.flatten().tolist())
+        L = oracle_layer(tied)
+        _, idx_ref, _, _ = O.moe_forward(L, bf16_bits(x))
+        assert np.all(idx_ref == lo)
+    zero = dataclasses.replace(lw, router_w=torch.zeros_like(lw.router_w),
+                               correction_bias=(torch.zeros_like(lw.correction_bias)
+                                                if lw.correction_bias is not None else None))
+    for k in (1, 3):
+        zk = dataclasses.replace(zero, cfg=zero.cfg.with_(top_k=k))
+        x = synth.make_input(cfg, n, "cuda")
+        _, idx, w = MoeLayer(zk, n).forward(x)
+        torch.cuda.synchronize()
+        assert torch.equal(idx.cpu(), torch.arange(k, dtype=torch.int32).repeat(n, 1))
+        expect = (1.0 / k) * (1.0 if routing == synth.ROUTE_SOFTMAX else 2.5)
+        assert torch.allclose(w.cpu(), torch.full((n, k), expect), rtol=1e-6)
 
 
 def test_zero_tokens_is_a_noop():
