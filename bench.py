@@ -33,8 +33,8 @@ METRIC = "MoE layer µs/call, tokens/s and HBM GB/s (frac of ~8 TB/s) at N=1–2
 # Kernel sequence of each expert path, by the number of stage markers a call records.
 STAGES_BY_MARKS = {
     2: ["fused"],
-    6: ["router", "topk", "group", "gate_up", "down_blend"],
-    8: ["router", "topk", "group", "gather", "gate_up", "down", "combine"],
+    5: ["router", "topk_group", "gate_up", "down_blend"],
+    7: ["router", "topk_group", "gather", "gate_up", "down", "combine"],
 }
 
 
@@ -396,11 +396,12 @@ def run_ours(args):
     alg = {
         "fused": touched,
         "router": E * H * 2 + n * H * 2 + n * E * 4,
-        "topk": n * E * 4 + nk * 8 + (4 * E if lw.correction_bias is not None else 0),
-        "group": nk * 4 + 4 * (3 * E + 1) + nk * 4,
+        # top-k (logits in, routes out) + grouping (routes in, counts/offsets/permutation out)
+        "topk_group": n * E * 4 + nk * 8 + (4 * E if lw.correction_bias is not None else 0)
+        + nk * 4 + 4 * (3 * E + 1) + nk * 4,
         # token-major: fp32 activations; grouped: 16-bit activations
-        "gate_up": w_gu + n * H * 2 + (4 if nm == 6 else 2) * (nk * I + n * S)
-        + (2 * (nk * H + (n * H if fmt != "bf16" else 0)) if nm == 8 else 0),
+        "gate_up": w_gu + n * H * 2 + (4 if nm == 5 else 2) * (nk * I + n * S)
+        + (2 * (nk * H + (n * H if fmt != "bf16" else 0)) if nm == 7 else 0),
         "down_blend": w_dn + 4 * (nk * I + n * S) + n * H * 2 + nk * 8,
         "gather": 2 * 2 * (nk * H + (n * H if fmt != "bf16" else 0)),
         "down": w_dn + 2 * (nk * I + n * S) + 4 * (nk * H + (n * H if S else 0)),

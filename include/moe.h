@@ -228,9 +228,10 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* wts,
  *   n_marks   (out, optional) markers the call reached
  * Markers: 0 before the first kernel, then one after each stage, in launch
  * order.  One token on the single-token kernel: 2 markers (before, after).
- * Token-major kernels: 6 (router, top-k, grouping, gate+up, down+blend).
- * Grouped tensor-core path: 8 (router, top-k, grouping, gather, gate+up, down,
- * combine).  The pre-expert RMSNorm, when present, runs in the grouping stage.
+ * Token-major kernels: 5 (router, top-k + grouping, gate+up, down+blend).
+ * Grouped tensor-core path: 7 (router, top-k + grouping, gather, gate+up, down,
+ * combine).  The pre-expert RMSNorm, when present, runs at the start of the
+ * stage after top-k + grouping.
  * Errors: as moe_forward, plus MOE_ERR_NULL for events == NULL with n_events > 0. */
 moe_status_t moe_forward_timed(const moe_config_t* cfg, const moe_weights_t* wts,
                                const void* x, int32_t n, void* out,

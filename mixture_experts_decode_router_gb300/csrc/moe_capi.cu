@@ -159,10 +159,12 @@ static QMatDev qdev(const moe_qmat_t& q, int out_dim, int in_dim, int e_base) {
     return d;
 }
 
-// Enqueue router + top-k.  Arguments already validated.
+// Enqueue router + top-k.  Arguments already validated.  `with_group`: the
+// top-k launch also groups the routes by expert (the fused top-k + grouping
+// kernel), so the expert stage that follows skips its grouping launch.
 static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w, const void* x,
                                   int32_t n, int32_t* idx, float* wt, float* logits, void* ws,
-                                  const WsLayout& L, cudaStream_t st, Marks& mk) {
+                                  const WsLayout& L, bool with_group, cudaStream_t st, Marks& mk) {
     const int sms = device_sm_count();
     float* lg = logits ? logits : at<float>(ws, L.logits);
     cudaError_t e;
@@ -181,8 +183,15 @@ static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w,
     }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     mk.mark(st);
-    e = launch_topk(lg, n, c->num_experts, c->top_k, c->routing, w->correction_bias,
-                    c->norm_topk_prob, c->routed_scaling_factor, idx, wt, st);
+    if (with_group)
+        e = launch_topk_group(lg, n, c->num_experts, c->top_k, c->routing, w->correction_bias, c->norm_topk_prob,
+                              c->routed_scaling_factor, idx, wt, c->expert_begin, c->expert_end,
+                              at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm),
+                              at<int32_t>(ws, L.inv), at<int32_t>(ws, L.active), at<int32_t>(ws, L.segs),
+                              at<Ctrl>(ws, L.ctrl), st);
+    else
+        e = launch_topk(lg, n, c->num_experts, c->top_k, c->routing, w->correction_bias,
+                        c->norm_topk_prob, c->routed_scaling_factor, idx, wt, st);
     mk.mark(st);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -260,11 +269,12 @@ static moe_status_t enqueue_grouped(const moe_config_t* c, const moe_weights_t* 
 }
 
 // Enqueue grouping + experts + blend.  `sg_from_ws`: the shared-gate logit was
-// written to the workspace by enqueue_route of the same call.
+// written to the workspace by enqueue_route of the same call.  `grouped`: so
+// were the routes' grouping by expert (enqueue_route with_group).
 static moe_status_t enqueue_experts(const moe_config_t* c, const moe_weights_t* w, const void* x,
                                     int32_t n, const int32_t* idx, const float* wt, void* out,
-                                    void* ws, const WsLayout& L, bool sg_from_ws, cudaStream_t st,
-                                    Marks& mk) {
+                                    void* ws, const WsLayout& L, bool sg_from_ws, bool grouped,
+                                    cudaStream_t st, Marks& mk) {
     const int sms = device_sm_count();
     const int H = c->hidden, I = c->inter, S = c->shared_inter, k = c->top_k, E = c->num_experts;
     float* sg_logit = at<float>(ws, L.sg_logit);
@@ -287,11 +297,13 @@ static moe_status_t enqueue_experts(const moe_config_t* c, const moe_weights_t* 
         if (e != cudaSuccess) return MOE_ERR_CUDA;
         xin = xe;
     }
-    e = launch_group(idx, n * k, E, c->expert_begin, c->expert_end, at<int32_t>(ws, L.counts),
-                     at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv),
-                     at<int32_t>(ws, L.active), at<int32_t>(ws, L.segs), at<Ctrl>(ws, L.ctrl), st);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    mk.mark(st);
+    if (!grouped) {
+        e = launch_group(idx, n * k, E, c->expert_begin, c->expert_end, at<int32_t>(ws, L.counts),
+                         at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm), at<int32_t>(ws, L.inv),
+                         at<int32_t>(ws, L.active), at<int32_t>(ws, L.segs), at<Ctrl>(ws, L.ctrl), st);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        mk.mark(st);
+    }
 
     const int path = (c->path == MOE_PATH_AUTO) ? (n <= kTokenMajorMaxN ? MOE_PATH_TOKEN_MAJOR
                                                                         : MOE_PATH_GROUPED)
@@ -373,7 +385,7 @@ moe_status_t moe_route(const moe_config_t* cfg_in, const moe_weights_t* wts, con
     WsLayout L;
     if ((s = check_ws(cfg, n, ws, ws_bytes, &L)) != MOE_OK) return s;
     Marks mk;
-    return enqueue_route(cfg, wts, x, n, idx, w, logits, ws, L, reinterpret_cast<cudaStream_t>(stream),
+    return enqueue_route(cfg, wts, x, n, idx, w, logits, ws, L, false, reinterpret_cast<cudaStream_t>(stream),
                          mk);
 }
 
@@ -393,7 +405,7 @@ moe_status_t moe_experts(const moe_config_t* cfg_in, const moe_weights_t* wts, c
     WsLayout L;
     if ((s = check_ws(cfg, n, ws, ws_bytes, &L)) != MOE_OK) return s;
     Marks mk;
-    return enqueue_experts(cfg, wts, x, n, idx, w, out, ws, L, false,
+    return enqueue_experts(cfg, wts, x, n, idx, w, out, ws, L, false, false,
                            reinterpret_cast<cudaStream_t>(stream), mk);
 }
 
@@ -470,11 +482,10 @@ static moe_status_t forward_impl(const moe_config_t* cfg_in, const moe_weights_t
             if (e != cudaSuccess) return MOE_ERR_CUDA;
         }
         mk.mark(st);
-        mk.mark(st);
-    } else if ((s = enqueue_route(cfg, wts, x, n, idx_p, w_p, nullptr, ws, L, st, mk)) != MOE_OK) {
-        return s;
+        return enqueue_experts(cfg, wts, x, n, idx_p, w_p, out, ws, L, true, false, st, mk);
     }
-    return enqueue_experts(cfg, wts, x, n, idx_p, w_p, out, ws, L, true, st, mk);
+    if ((s = enqueue_route(cfg, wts, x, n, idx_p, w_p, nullptr, ws, L, true, st, mk)) != MOE_OK) return s;
+    return enqueue_experts(cfg, wts, x, n, idx_p, w_p, out, ws, L, true, true, st, mk);
 }
 
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* wts, const void* x, int32_t n,

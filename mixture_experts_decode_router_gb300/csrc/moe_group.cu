@@ -17,6 +17,8 @@
 //   segs[s]     (expert, first sorted position, routes) for runs of at most
 //               kTcTokensPerTile routes of one expert, ascending expert;
 //               ctrl->n_rsegs of them (the tiles of the grouped path)
+#include <mutex>
+
 #include "moe_launch.cuh"
 
 namespace moe {
@@ -24,17 +26,17 @@ namespace moe {
 constexpr int kGroupThreads = 1024;
 constexpr int kSegWarps = 8;   // warps that own contiguous route segments
 
-__global__ void __launch_bounds__(kGroupThreads)
-group_kernel(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_end,
-             int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-             int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ active,
-             int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl) {
-    extern __shared__ int32_t sm[];
+// The grouping of all n*k routes by one block of kGroupThreads threads.
+// sm: (kSegWarps + 1) * E ints of shared memory.
+__device__ __forceinline__ void group_block(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_end,
+                                            int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                            int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                                            int32_t* __restrict__ active, int32_t* __restrict__ segs,
+                                            Ctrl* __restrict__ ctrl, int32_t* sm) {
     int32_t* cnt = sm;                           // [kSegWarps][E]
     int32_t* tot = sm + kSegWarps * E;           // [E]
     __shared__ int32_t warp_sums[3][32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    pdl_wait();
 
     for (int i = tid; i < kSegWarps * E; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
@@ -43,7 +45,7 @@ group_kernel(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_
     if (warp < kSegWarps) {
         const int b = warp * seg, e_ = min(nk, b + seg);
         for (int r = b + lane; r < e_; r += 32) {
-            const int e = idx[r];
+            const int e = __ldcg(idx + r);   // L2: the fused kernel's other blocks wrote idx
             if (e >= e_begin && e < e_end) atomicAdd(&cnt[warp * E + e], 1);   // not held here: dropped
         }
     }
@@ -122,7 +124,7 @@ group_kernel(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_
         for (int r0 = b; r0 < e_; r0 += 32) {
             const int r = r0 + lane;
             const bool valid = r < e_;
-            const int e = valid ? idx[r] : -1;
+            const int e = valid ? __ldcg(idx + r) : -1;
             const bool in_range = valid && e >= e_begin && e < e_end;
             if (valid && !in_range) inv[r] = -1;
             const unsigned vmask = __ballot_sync(0xffffffffu, in_range);
@@ -138,6 +140,60 @@ group_kernel(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_
             __syncwarp();
         }
     }
+}
+
+__global__ void __launch_bounds__(kGroupThreads)
+group_kernel(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_end,
+             int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+             int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ active,
+             int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl) {
+    extern __shared__ int32_t sm[];
+    pdl_wait();
+    group_block(idx, nk, E, e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, sm);
+    pdl_trigger();
+}
+
+// Top-k routing of every token (one CTA per token, the top-k kernel's
+// arithmetic) and then, in the CTA that finishes last, the grouping of all
+// routes: one launch instead of two.  The last CTA is found with a counter in
+// the control block (release fence before the increment, acquire fence after
+// it), which that CTA returns to zero.
+__global__ void __launch_bounds__(kGroupThreads)
+topk_group_kernel(const float* __restrict__ logits, int n, int E, int k, int routing,
+                  const float* __restrict__ bias, int norm, float scale, int32_t* idx_out,
+                  float* __restrict__ w_out, int e_begin, int e_end, int32_t* __restrict__ counts,
+                  int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                  int32_t* __restrict__ active, int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl) {
+    extern __shared__ __align__(16) float smf[];
+    float* slg = smf;                                                    // [E]
+    unsigned long long* skey =
+        reinterpret_cast<unsigned long long*>(smf + ((E + 3) & ~3));     // [E + 32]
+    int32_t* gsm = reinterpret_cast<int32_t*>(skey + E + 32);           // grouping scratch
+    __shared__ int ssel[kMaxTopK];
+    __shared__ float sselw[kMaxTopK];
+    __shared__ __align__(16) unsigned long long cand_k[kMaxExperts / 32 * kMaxTopK];
+    __shared__ float gmax[kMaxExperts / 32], zg[kMaxExperts / 32];
+    __shared__ int s_last;
+    const int t = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();
+    route_token_block(logits + (size_t)t * E, E, k, routing, bias, norm, scale, slg, skey, cand_k, gmax, zg, ssel,
+                      sselw);
+    if (tid < k) {
+        idx_out[(size_t)t * k + tid] = ssel[tid];
+        w_out[(size_t)t * k + tid] = sselw[tid];
+        __threadfence();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const int done = atomicAdd(&ctrl->routed, 1);
+        s_last = done == n - 1;
+        __threadfence();
+    }
+    __syncthreads();
+    if (s_last) {
+        group_block(idx_out, n * k, E, e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, gsm);
+        if (tid == 0) ctrl->routed = 0;
+    }
     pdl_trigger();
 }
 
@@ -148,6 +204,30 @@ cudaError_t launch_group(const int32_t* idx, int nk, int E, int e_begin, int e_e
     // (kSegWarps + 1) * E ints <= 36 KB for E <= 1024: under the 48 KB default.
     launch_pdl(group_kernel, 1, kGroupThreads, smem, st, idx, nk, E, e_begin, e_end, counts, offsets, perm, inv, active, segs,
                                                   ctrl);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk_group(const float* logits, int n, int E, int k, int routing, const float* bias, int norm,
+                              float scale, int32_t* idx, float* w, int e_begin, int e_end, int32_t* counts,
+                              int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
+                              Ctrl* ctrl, cudaStream_t st) {
+    const size_t smem = (size_t)((E + 3) & ~3) * sizeof(float) + (size_t)(E + 32) * sizeof(unsigned long long) +
+                        sizeof(int32_t) * (size_t)(kSegWarps + 1) * E;
+    static std::mutex mu;
+    static size_t configured[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (configured[dev] < smem) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(topk_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            configured[dev] = smem;
+        }
+    }
+    launch_pdl(topk_group_kernel, n, kGroupThreads, smem, st, logits, n, E, k, routing, bias, norm, scale, idx, w,
+               e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl);
     return cudaGetLastError();
 }
 

@@ -25,7 +25,8 @@ struct Ctrl {
     int32_t n_rsegs;       // routed token segments of <= kTcTokensPerTile (group kernel)
     int32_t err;           // sticky device error code (bounded waits that gave up); 0 = none
     uint32_t gbar;         // grid-barrier arrivals of the single-token kernel (0 between calls)
-    int32_t pad[60];
+    int32_t routed;        // tokens routed so far by the fused top-k + grouping kernel (0 between calls)
+    int32_t pad[59];
 };
 
 // Tokens per tile of the grouped tensor-core path (its MMA N is at most this).
@@ -374,6 +375,35 @@ __device__ __forceinline__ void route_weights_block(const float* slg, int E, int
         if (lane < k) sselw[lane] = p * scale;
     }
     sync();
+}
+
+// One token's routing by one thread block from its logit row: the selection
+// keys (sigmoid routing: sigmoid(l) + bias selects; NaN scores rank last),
+// then route_select_block and route_weights_block.  ssel / sselw receive the
+// k experts and weights.  slg [E] and skey [E + 32] as above.
+__device__ __forceinline__ void route_token_block(const float* __restrict__ lrow, int E, int k, int routing,
+                                                  const float* __restrict__ bias, int norm, float scale,
+                                                  float* slg, unsigned long long* skey,
+                                                  unsigned long long* cand_k, float* gmax, float* zg, int* ssel,
+                                                  float* sselw) {
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    for (int e = tid; e < E + 32; e += nthr) {
+        if (e < E) {
+            const float l = lrow[e];
+            float sc;
+            if (routing == MOE_ROUTE_SOFTMAX) sc = l;
+            else sc = 1.0f / (1.0f + expf(-l)) + bias[e];
+            if (sc != sc) sc = -INFINITY;
+            slg[e] = l;
+            skey[e] = route_key(sc, e);
+        } else {
+            skey[e] = 0ull;
+        }
+    }
+    __syncthreads();
+    route_select_block(slg, skey, E, k, routing, tid, nthr, cand_k, gmax, ssel, [] { __syncthreads(); });
+    route_weights_block(slg, E, k, routing, norm, scale, tid, nthr, gmax, zg, ssel, sselw,
+                        [] { __syncthreads(); });
 }
 
 // 1 / sqrt(mean(x^2) + eps) of one BF16 row of H elements, by one warp: lane l

@@ -219,25 +219,9 @@ topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int rou
     __shared__ __align__(16) unsigned long long cand_k[kMaxExperts / 32 * kMaxTopK];
     __shared__ float gmax[kMaxExperts / 32], zg[kMaxExperts / 32];
     const int t = blockIdx.x, tid = threadIdx.x;
-    const float* lrow = logits + (size_t)t * E;
     pdl_wait();
-    for (int e = tid; e < E + 32; e += blockDim.x) {
-        if (e < E) {
-            const float l = lrow[e];
-            float sc;
-            if (routing == MOE_ROUTE_SOFTMAX) sc = l;
-            else sc = 1.0f / (1.0f + expf(-l)) + bias[e];
-            if (sc != sc) sc = -INFINITY;
-            slg[e] = l;
-            skey[e] = route_key(sc, e);
-        } else {
-            skey[e] = 0ull;
-        }
-    }
-    __syncthreads();
-    route_select_block(slg, skey, E, k, routing, tid, blockDim.x, cand_k, gmax, ssel, [] { __syncthreads(); });
-    route_weights_block(slg, E, k, routing, norm, scale, tid, blockDim.x, gmax, zg, ssel, sselw,
-                        [] { __syncthreads(); });
+    route_token_block(logits + (size_t)t * E, E, k, routing, bias, norm, scale, slg, skey, cand_k, gmax, zg, ssel,
+                      sselw);
     if (tid < k) {
         idx_out[(size_t)t * k + tid] = ssel[tid];
         w_out[(size_t)t * k + tid] = sselw[tid];

@@ -116,12 +116,18 @@ def test_forced_paths(path, fmt):
         _check(cfg, n, path=path)
 
 
-def test_all_tokens_on_one_expert():
-    cfg = small("one_expert", num_experts=16, top_k=2)
+@pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_FP8_B128, synth.FMT_NVFP4])
+@pytest.mark.parametrize("n", [33, 150])
+def test_all_tokens_on_one_expert(fmt, n):
+    """Every route on the same two experts: at 150 tokens each expert's tokens
+    span three tensor-core token segments (64 + 64 + 22)."""
+    cfg = small("one_expert", num_experts=16, top_k=2, expert_fmt=fmt)
     lw = synth.make_weights(cfg, "cuda")
     x1 = synth.make_input(cfg, 1, "cuda", gap_fn=gap_fn_for(oracle_layer(lw)))
-    x = x1.repeat(33, 1)      # 33 copies: every route lands on the same two experts
-    _check(cfg, 33, x=x, lw=lw)
+    x = x1.repeat(n, 1)
+    rows = sorted({r for r in (0, 31, 63, 64, 127, 128, n - 1) if r < n})
+    _, _, _, _, _, layer = _check(cfg, n, x=x, lw=lw, rows=rows)
+    assert layer.device_error() == 0
 
 
 @pytest.mark.parametrize("norm,router", [(False, synth.FMT_BF16), (True, synth.FMT_BF16),
