@@ -56,7 +56,23 @@ struct TcCfg {
     static constexpr int kRawRow = FMT == MOE_W_FP8_B128 ? BK : (FMT == MOE_W_NVFP4 ? BK / 2 : 0);
     static constexpr int kRawMat = BM * kRawRow;
     static constexpr int kRawStage = kMats * kRawMat;
-    static constexpr int kAStages = kDeq ? (GU ? 4 : 6) : (GU ? 5 : 8);
+    // BF16 tiles: operand stages in shared memory (TMA, 128-byte swizzle).
+    // FP8 / NVFP4 tiles: the dequant warps write the f16 operand stages into
+    // tensor memory (tcgen05.st), where tcgen05.mma reads A; shared memory
+    // holds only the raw codes and the token tiles, so the raw ring is deep.
+    // Tensor memory: kAccBufs accumulators of kMats x NT fp32 columns (two, so
+    // a tile's epilogue overlaps the next tile's MMAs; one for dequantised
+    // gate/up, whose 32+ K stages per tile hide the epilogue, so that the
+    // operand ring gets the columns), then (dequantised tiles) the operand
+    // stages, kMats x BK/2 columns each (two f16 per 32-bit column, row i of
+    // the tile in lane i).
+    static constexpr int kAccBufs = (kDeq && GU) ? 1 : 2;
+    static constexpr int kAccCols = kMats * NT;
+    static constexpr int kACols = kMats * BK / 2;
+    static constexpr int kAColBase = kAccBufs * kAccCols;
+    static constexpr int kTmemCols = kDeq ? 512 : kAccBufs * kAccCols;
+    static constexpr int kAStages = kDeq ? (512 - kAColBase) / kACols : (GU ? 5 : 8);
+    static constexpr int kASmemStages = kDeq ? 0 : kAStages;
     // Dequantised tiles hand operand stages to the MMA warp in groups of two
     // (one barrier round trip per 128 K instead of per 64).
     static constexpr int kGrp = kDeq ? 2 : 1;
@@ -64,16 +80,18 @@ struct TcCfg {
     // Dequantised tiles: the token (B) tiles have a ring of their own, so they
     // are fetched ahead instead of after the MMA frees an A slot.
     static constexpr int kBStages = kDeq ? (GU ? 4 : 6) : kAStages;
-    static constexpr int kRawStages = !kDeq ? 0 : (GU ? (FMT == MOE_W_FP8_B128 ? 4 : 6) : 8);
-    static constexpr int kAccCols = kMats * NT;
-    static constexpr int kTmemCols = 2 * kAccCols;
+    static constexpr int kRawStages = !kDeq ? 0 : (GU ? (FMT == MOE_W_FP8_B128 ? 10 : 16) : (FMT == MOE_W_FP8_B128 ? 16 : 24));
     static constexpr int kDeqWarps = kDeq ? (FMT == MOE_W_NVFP4 ? 16 : 8) : 0;
+    // Dequant work split: warp 6 + dw serves TMEM lane quarter (6 + dw) & 3 (the
+    // quarter a warp may access) and part dw >> 2 of each row's kMats x BK codes.
+    static constexpr int kParts = kDeqWarps / 4;
+    static constexpr int kPartElems = kDeq ? kMats * BK / kParts : 0;
     // Dequantised tiles: a second producer warp for the token (B) tiles, after
     // the dequant warps, so a full B ring never holds up the weight copies.
     static constexpr int kBWarp = 6 + kDeqWarps;
     static constexpr int kThreads = (6 + kDeqWarps + (kDeq ? 1 : 0)) * 32;
     static constexpr int kOffA = 0;
-    static constexpr int kOffB = kOffA + kAStages * kAStage;
+    static constexpr int kOffB = kOffA + kASmemStages * kAStage;
     static constexpr int kOffRaw = kOffB + kBStages * kBStage;
     // Block scales of each raw stage, fetched by the producer warp with the
     // raw codes: FP8 one fp32 per matrix; NVFP4 4 E4M3 bytes per row per matrix.
@@ -87,7 +105,11 @@ struct TcCfg {
     static constexpr int kSmem = kOffMisc + 16 + 1024;   // + alignment slack
     static_assert(kSmem <= 232448, "shared memory budget");
     static_assert(kTmemCols <= 512, "TMEM budget");
+    static_assert(!kDeq || kAColBase + kAStages * kACols <= kTmemCols, "TMEM operand stages");
     static_assert(kAStages % kGrp == 0, "operand stages come in whole groups");
+    static_assert(kOffRaw % 1024 == 0 && kRawMat % 1024 == 0, "swizzled raw stages sit on 1024-byte boundaries");
+    static_assert(!kDeq || (kPartElems % 16 == 0 && BK % (kDeq ? kPartElems : 1) == 0),
+                  "a dequant part is whole 16-code blocks of one matrix");
 };
 
 struct Tile {
@@ -181,11 +203,15 @@ __device__ __forceinline__ float2 f16x2_to_float2(uint32_t h2) {
     return __half22float2(__half2(raw));
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
+// Byte offset of 16-byte chunk c of row r in a raw stage.  The TMA writes the
+// raw codes swizzled, the row's chunk index XORed with address bits 7 and up
+// (FP8, 64-byte rows, 64-byte swizzle: c ^ ((r >> 1) & 3); NVFP4, 32-byte
+// rows, 32-byte swizzle: c ^ ((r >> 2) & 1)), so that 32 lanes reading one
+// chunk of 32 consecutive rows spread over all banks.
+template <int FMT>
+__device__ __forceinline__ int raw_chunk(int r, int c) {
+    if constexpr (FMT == MOE_W_FP8_B128) return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+    else return r * 32 + ((c ^ ((r >> 2) & 1)) << 4);
 }
 
 template <int FMT, bool GU>
@@ -365,8 +391,8 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         uint32_t it = 0, git = 0, acc_it = 0;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x, ++acc_it) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
-            const int ab = acc_it & 1;
-            if (!ptx::mbar_wait_warp(&acc_empty[ab], ((acc_it >> 1) & 1) ^ 1, s_abort, err, 2)) break;
+            const int ab = acc_it % C::kAccBufs;
+            if (!ptx::mbar_wait_warp(&acc_empty[ab], ((acc_it / C::kAccBufs) & 1) ^ 1, s_abort, err, 2)) break;
             ptx::tc_fence_after();
             const int nmma = ((t.ntok + 15) >> 4) << 4;
             const uint32_t idesc = ptx::idesc_f16(BM, nmma, !C::kF16);
@@ -389,16 +415,31 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                     ptx::tc_fence_after();
                     // Descriptors of the stage's first K step; a later step (or the
                     // second matrix) only moves the start address field (16-byte units).
-                    const uint64_t a_desc = ptx::sw128_desc(ptx::smem_u32(sA + as * C::kAStage));
                     const uint64_t b_desc = ptx::sw128_desc(ptx::smem_u32(sB + bs * C::kBStage));
-                    if (ptx::elect_one()) {
+                    if constexpr (C::kDeq) {
+                        // A in tensor memory: K step kk of matrix m is 8 columns on.
+                        const uint32_t a_t = tmem + C::kAColBase + as * C::kACols;
+                        if (ptx::elect_one()) {
     #pragma unroll
-                        for (int m = 0; m < C::kMats; ++m)
+                            for (int m = 0; m < C::kMats; ++m)
     #pragma unroll
-                            for (int kk = 0; kk < BK / 16; ++kk)
-                                ptx::mma_f16(d0 + m * NT, a_desc + (uint64_t)((m * C::kAMat + kk * 32) >> 4),
-                                             b_desc + (uint64_t)((kk * 32) >> 4), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                        if constexpr (C::kDeq) ptx::mma_commit(&b_empty[bs]);
+                                for (int kk = 0; kk < BK / 16; ++kk)
+                                    ptx::mma_f16_ts(d0 + m * NT, a_t + m * (BK / 2) + kk * 8,
+                                                    b_desc + (uint64_t)((kk * 32) >> 4), idesc,
+                                                    (kb > 0 || kk > 0) ? 1u : 0u);
+                            ptx::mma_commit(&b_empty[bs]);
+                        }
+                    } else {
+                        const uint64_t a_desc = ptx::sw128_desc(ptx::smem_u32(sA + as * C::kAStage));
+                        if (ptx::elect_one()) {
+    #pragma unroll
+                            for (int m = 0; m < C::kMats; ++m)
+    #pragma unroll
+                                for (int kk = 0; kk < BK / 16; ++kk)
+                                    ptx::mma_f16(d0 + m * NT, a_desc + (uint64_t)((m * C::kAMat + kk * 32) >> 4),
+                                                 b_desc + (uint64_t)((kk * 32) >> 4), idesc,
+                                                 (kb > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     __syncwarp();
                 }
@@ -422,8 +463,8 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         uint32_t acc_it = 0;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x, ++acc_it) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
-            const int ab = acc_it & 1;
-            if (!ptx::mbar_wait_warp(&acc_full[ab], (acc_it >> 1) & 1, s_abort, err, 3)) break;
+            const int ab = acc_it % C::kAccBufs;
+            if (!ptx::mbar_wait_warp(&acc_full[ab], (acc_it / C::kAccBufs) & 1, s_abort, err, 3)) break;
             ptx::tc_fence_after();
             const int m = t.m0 + row;
             const bool valid = m < t.out;
@@ -490,109 +531,107 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
     } else if constexpr (C::kDeq) {
         // ------------------------------------------------------------ dequant
-        // Each matrix of a stage is 128 rows x 64 codes = 512 chunks of 16
-        // codes; dequant thread dt takes chunks dt, dt + D, ... (D = threads).
-        constexpr int kDT = C::kDeqWarps * 32;
-        static_assert(512 % kDT == 0, "dequant threads divide the 512 chunks");
-        const int dt = threadIdx.x - 6 * 32;
+        // Thread `lane` of a dequant warp converts row r = 32 qd + lane of its
+        // part of every stage: kPartElems codes of matrix pm from column pk0 of
+        // the stage, kPartElems / 2 f16x2 words written to that row's lane of
+        // the stage's TMEM operand columns.
+        constexpr int PE = C::kPartElems, NC = PE / 2;
+        const int qd = warp & 3, part = (warp - 6) >> 2;
+        const int r = 32 * qd + lane;
+        const int pm = (part * PE) / BK, pk0 = (part * PE) % BK;
+        const uint32_t t_row = tmem + ((uint32_t)(32 * qd) << 16) + C::kAColBase + pm * (BK / 2) + pk0 / 2;
         uint32_t it = 0, git = 0;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
             const bool sh = t.e < 0;
             const int KB = (t.K + BK - 1) / BK;
+            const int mrow = t.m0 + r;
             bool ok = true;
             for (int kb = 0; kb < KB && ok; ++git) {
                 // A group of kGrp operand stages (fewer at the end of the tile).
                 const int g = git % C::kAGroups;
                 if (!ptx::mbar_wait_warp(&a_empty[g], ((git / C::kAGroups) & 1) ^ 1, s_abort, err, 4)) { ok = false; break; }
+                ptx::tc_fence_after();   // the MMAs that read these columns are complete
                 const int n = min(C::kGrp, KB - kb);
                 for (int u = 0; u < n; ++u, ++kb, ++it) {
                     const int rs = it % C::kRawStages, as = g * C::kGrp + u;
                     if (!ptx::mbar_wait_warp(&raw_full[rs], (it / C::kRawStages) & 1, s_abort, err, 4)) { ok = false; break; }
                     const int k0 = kb * BK;
-                    for (int m = 0; m < C::kMats; ++m) {
-                        const uint8_t* raw = sRaw + rs * C::kRawStage + m * C::kRawMat;
-                        const uint32_t a_mat = ptx::smem_u32(sA + as * C::kAStage + m * C::kAMat);
-                        if constexpr (FMT == MOE_W_FP8_B128) {
-                            // One fp32 scale per 128x128 block: uniform over this stage
-                            // (fetched into shared memory with the codes).
-                            const float s = reinterpret_cast<const float*>(sScale + rs * C::kScaleStage)[m];
-                            // In f16's normal range the product is formed in f16x2 (the
-                            // scale and the product each rounded once to f16); else in fp32.
-                            const bool f16_scale = s >= 6.2e-5f && s <= 128.0f;
-                            const __half2 s2 = __float2half2_rn(s);
-                            const uint32_t s2u = *reinterpret_cast<const uint32_t*>(&s2);
+                    const uint8_t* raw = sRaw + rs * C::kRawStage + pm * C::kRawMat;
+                    uint32_t o[NC];
+                    if constexpr (FMT == MOE_W_FP8_B128) {
+                        // One fp32 scale per 128x128 block: uniform over this stage
+                        // (fetched into shared memory with the codes).
+                        const float s = reinterpret_cast<const float*>(sScale + rs * C::kScaleStage)[pm];
+                        // In f16's normal range the product is formed in f16x2 (the
+                        // scale and the product each rounded once to f16); else in fp32.
+                        const bool f16_scale = s >= 6.2e-5f && s <= 128.0f;
+                        const __half2 s2 = __float2half2_rn(s);
+                        const uint32_t s2u = *reinterpret_cast<const uint32_t*>(&s2);
     #pragma unroll
-                            for (int c = 0; c < 512 / kDT; ++c) {
-                                const int qd = dt + c * kDT;
-                                const int r = qd >> 2, ch = qd & 3;    // row, 16-byte chunk of codes
-                                const uint4 v = *reinterpret_cast<const uint4*>(raw + r * 64 + ch * 16);
-                                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                                uint32_t o[8];
-                                if (f16_scale) {
-    #pragma unroll
-                                    for (int i = 0; i < 4; ++i) {
-                                        uint32_t h[2];
-                                        e4m3x4_to_f16x2x2(w4[i], h);
-                                        o[2 * i] = f16x2_mul(h[0], s2u);
-                                        o[2 * i + 1] = f16x2_mul(h[1], s2u);
-                                    }
-                                } else {
-    #pragma unroll
-                                    for (int i = 0; i < 4; ++i) {
-                                        const float2 lo = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] & 0xffffu));
-                                        const float2 hi = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] >> 16));
-                                        o[2 * i] = pack_f16(lo.x * s, lo.y * s);
-                                        o[2 * i + 1] = pack_f16(hi.x * s, hi.y * s);
-                                    }
-                                }
-                                const uint32_t rowb = a_mat + r * 128;
-                                st_shared_v4(rowb + (((2 * ch) ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
-                                st_shared_v4(rowb + (((2 * ch + 1) ^ (r & 7)) << 4), o[4], o[5], o[6], o[7]);
-                            }
-                        } else {
-                            // NVFP4: a chunk is one 16-code scale block (8 bytes).
-    #pragma unroll
-                            for (int c = 0; c < 512 / kDT; ++c) {
-                                const int qd = dt + c * kDT;
-                                const int r = qd >> 2, q = qd & 3;     // row, scale block of the stage
-                                const uint2 v = *reinterpret_cast<const uint2*>(raw + r * 32 + q * 8);
-                                const int kc = k0 + 16 * q;
-                                const int mrow = t.m0 + r;
-                                uint32_t sc = 0;   // f16x2 of the block scale (0 outside the matrix)
-                                if (t.K % 64 == 0) {
-                                    // Fetched into shared memory with the codes (0 past the last row).
-                                    const uint32_t w = reinterpret_cast<const uint32_t*>(sScale + rs * C::kScaleStage)[m * BM + r];
-                                    const uint32_t b = (w >> (8 * q)) & 0xffu;
-                                    sc = e4m3x2_to_f16x2(b | (b << 8));
-                                } else if (mrow < t.out && kc < t.K) {
-                                    const uint8_t* sp = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]) +
-                                                        ((size_t)t.le * t.out + mrow) * (t.K / 16) + kc / 16;
-                                    const uint32_t b = __ldg(sp);
-                                    sc = e4m3x2_to_f16x2(b | (b << 8));
-                                }
-                                uint32_t lo[4], hi[4];
-                                e2m1x8_to_f16x2x4(v.x, lo);
-                                e2m1x8_to_f16x2x4(v.y, hi);
+                        for (int c = 0; c < PE / 16; ++c) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(raw + raw_chunk<FMT>(r, pk0 / 16 + c));
+                            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                            if (f16_scale) {
     #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
-                                    lo[i] = f16x2_mul(lo[i], sc);
-                                    hi[i] = f16x2_mul(hi[i], sc);
+                                    uint32_t h[2];
+                                    e4m3x4_to_f16x2x2(w4[i], h);
+                                    o[8 * c + 2 * i] = f16x2_mul(h[0], s2u);
+                                    o[8 * c + 2 * i + 1] = f16x2_mul(h[1], s2u);
                                 }
-                                const uint32_t rowb = a_mat + r * 128;
-                                st_shared_v4(rowb + (((2 * q) ^ (r & 7)) << 4), lo[0], lo[1], lo[2], lo[3]);
-                                st_shared_v4(rowb + (((2 * q + 1) ^ (r & 7)) << 4), hi[0], hi[1], hi[2], hi[3]);
+                            } else {
+    #pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float2 lo = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] & 0xffffu));
+                                    const float2 hi = f16x2_to_float2(e4m3x2_to_f16x2(w4[i] >> 16));
+                                    o[8 * c + 2 * i] = pack_f16(lo.x * s, lo.y * s);
+                                    o[8 * c + 2 * i + 1] = pack_f16(hi.x * s, hi.y * s);
+                                }
+                            }
+                        }
+                    } else {
+                        // NVFP4: 16 codes (8 bytes) per E4M3 block scale.
+    #pragma unroll
+                        for (int b = 0; b < PE / 16; ++b) {
+                            const int qb = pk0 / 16 + b;   // scale block of the stage
+                            const uint2 v = *reinterpret_cast<const uint2*>(raw + raw_chunk<FMT>(r, qb >> 1) + 8 * (qb & 1));
+                            const int kc = k0 + 16 * qb;
+                            uint32_t sc = 0;   // f16x2 of the block scale (0 outside the matrix)
+                            if (t.K % 64 == 0) {
+                                // Fetched into shared memory with the codes (0 past the last row).
+                                const uint32_t w = reinterpret_cast<const uint32_t*>(sScale + rs * C::kScaleStage)[pm * BM + r];
+                                const uint32_t bb = (w >> (8 * qb)) & 0xffu;
+                                sc = e4m3x2_to_f16x2(bb | (bb << 8));
+                            } else if (mrow < t.out && kc < t.K) {
+                                const uint8_t* sp = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[pm] : p.scale[pm]) +
+                                                    ((size_t)t.le * t.out + mrow) * (t.K / 16) + kc / 16;
+                                const uint32_t bb = __ldg(sp);
+                                sc = e4m3x2_to_f16x2(bb | (bb << 8));
+                            }
+                            uint32_t lo[4], hi[4];
+                            e2m1x8_to_f16x2x4(v.x, lo);
+                            e2m1x8_to_f16x2x4(v.y, hi);
+    #pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                o[8 * b + i] = f16x2_mul(lo[i], sc);
+                                o[8 * b + 4 + i] = f16x2_mul(hi[i], sc);
                             }
                         }
                     }
+                    const uint32_t ta = t_row + as * C::kACols;
+                    if constexpr (NC == 8) ptx::tmem_st8(ta, o);
+                    else if constexpr (NC == 16) ptx::tmem_st16(ta, o);
+                    else ptx::tmem_st32(ta, o);
+                    // The codes are in registers: the raw stage may be refilled.
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&raw_empty[rs]);
                 }
                 if (!ok) break;
-                ptx::fence_proxy_async_smem();
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    for (int u = 0; u < n; ++u) ptx::mbar_arrive(&raw_empty[(it - n + u) % C::kRawStages]);
-                    ptx::mbar_arrive(&a_full[g]);
-                }
+                if (lane == 0) ptx::mbar_arrive(&a_full[g]);
             }
             if (!ok) break;
         }
@@ -629,7 +668,7 @@ EncodeTiledFn encode_fn() {
 
 // 2-D map over a row-major [rows, cols] matrix of `esize`-byte elements.
 bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t cols,
-              uint64_t rows, uint32_t box_cols, uint32_t box_rows, bool swizzle) {
+              uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
@@ -637,22 +676,27 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              swizzle,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Weight map: raw codes (FP8 / NVFP4, unswizzled) or BF16 (swizzled, MMA layout).
+// Weight map: BF16 (128-byte swizzle, the MMA operand layout) or raw codes
+// (FP8: 64-byte rows, 64-byte swizzle; NVFP4: 32-byte rows, 32-byte swizzle;
+// the layout raw_chunk reads).
 bool weight_map(CUtensorMap* m, int fmt, const void* w, int rows_total, int in_dim) {
     if (fmt == MOE_W_BF16)
-        return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, in_dim, rows_total, BK, BM, true);
+        return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, in_dim, rows_total, BK, BM,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (fmt == MOE_W_FP8_B128)
-        return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim, rows_total, BK, BM, false);
-    return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim / 2, rows_total, BK / 2, BM, false);
+        return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim, rows_total, BK, BM,
+                        CU_TENSOR_MAP_SWIZZLE_64B);
+    return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim / 2, rows_total, BK / 2, BM,
+                    CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
 bool act_map(CUtensorMap* m, int fmt, const void* a, int rows, int cols) {
     return make_map(m, a, fmt != MOE_W_BF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                    2, cols, rows > 0 ? rows : 1, BK, 16, true);
+                    2, cols, rows > 0 ? rows : 1, BK, 16, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int FMT, bool GU>
