@@ -12,6 +12,8 @@
 //
 // Top-k: the "topk" step (moe_topk_softmax_batched / moe_topk_sigmoid_batched
 // on the same pages): one CTA per token row.
+#include <mutex>
+
 #include "moe_launch.cuh"
 
 namespace moe {
@@ -74,19 +76,34 @@ router_kernel(const uint16_t* __restrict__ x, int n, int H,
 // For every (token, expert) pair the arithmetic is the one above -- lane l
 // chains fmaf over its chunks l, l+32, ... in order, then the same butterfly
 // -- so tiling changes nothing but how often each chunk is loaded.
-template <int RE, int RT>
+// XS: the block first copies its RT token rows into shared memory (every
+// thread's loads issued together: one round of latency instead of one per
+// chunk step); otherwise each warp reads them from L1/L2 as it goes.
+template <int RE, int RT, bool XS>
 __global__ void __launch_bounds__(256)
 router_tiled_kernel(const uint16_t* __restrict__ x, int n, int H,
                     const uint16_t* __restrict__ wr, int E,
                     const uint16_t* __restrict__ gw,
                     float* __restrict__ logits, float* __restrict__ sg_logit) {
+    extern __shared__ uint4 sxt[];   // XS: [RT][H / 8] chunks of the block's token rows
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows = E + (gw ? 1 : 0);
     const int r0 = (blockIdx.x * (blockDim.x >> 5) + warp) * RE;
-    if (r0 >= rows) return;
+    if (!XS && r0 >= rows) return;
     pdl_wait();
     const int t0 = blockIdx.y * RT;
     const int C = H >> 3;
+    if constexpr (XS) {
+        for (int i = threadIdx.x; i < RT * C; i += blockDim.x) {
+            const int b = i / C, c = i - b * C;
+            sxt[i] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)min(t0 + b, n - 1) * H) + c);
+        }
+        __syncthreads();
+        if (r0 >= rows) {
+            pdl_trigger();
+            return;
+        }
+    }
     const uint16_t* wrow[RE];
 #pragma unroll
     for (int a = 0; a < RE; ++a) {
@@ -118,7 +135,8 @@ router_tiled_kernel(const uint16_t* __restrict__ x, int n, int H,
             uint4 xv4[RT];
 #pragma unroll
             for (int b = 0; b < RT; ++b)
-                xv4[b] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)min(t0 + b, n - 1) * H) + c);
+                xv4[b] = XS ? sxt[b * C + c]
+                            : __ldg(reinterpret_cast<const uint4*>(x + (size_t)min(t0 + b, n - 1) * H) + c);
 #pragma unroll
             for (int b = 0; b < RT; ++b) {
                 float xv[8];
@@ -267,19 +285,43 @@ cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, i
         return cudaGetLastError();
     }
     // RT tokens x RE router rows per warp, 8 warps per CTA; RE as large as keeps
-    // at least one CTA per SM.
-    const int rt = n >= 8 ? 8 : 4;
+    // at least one CTA per SM.  The token rows are staged in shared memory when
+    // RT of them fit in kRouterXsMax bytes (8 tokens, else 4).
+    constexpr size_t kRouterXsMax = 64 * 1024;
+    int rt = n >= 8 ? 8 : 4;
+    if (rt == 8 && (size_t)8 * H * 2 > kRouterXsMax) rt = 4;
+    const size_t xs_bytes = (size_t)rt * H * 2;
+    const bool xs = xs_bytes <= kRouterXsMax;
     const int gy = (n + rt - 1) / rt;
     int re = 4;
     while (re > 1 && (long)((rows + 8 * re - 1) / (8 * re)) * gy < num_sms) re >>= 1;
     dim3 grid((rows + 8 * re - 1) / (8 * re), gy);
-#define MOE_ROUTER_CASE(RE_, RT_)                                                                    \
+    static std::mutex mu;
+    static bool configured[128][6] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+#define MOE_ROUTER_CASE(RE_, RT_, SLOT_)                                                             \
     if (re == RE_ && rt == RT_) {                                                                    \
-        launch_pdl(router_tiled_kernel<RE_, RT_>, grid, 256, 0, st, x, n, H, wr, E, gw, logits, sg_logit);   \
+        if (xs) {                                                                                    \
+            {                                                                                        \
+                std::lock_guard<std::mutex> lock(mu);                                                \
+                if (!configured[dev][SLOT_]) {                                                       \
+                    const cudaError_t e = cudaFuncSetAttribute(router_tiled_kernel<RE_, RT_, true>,  \
+                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRouterXsMax);             \
+                    if (e != cudaSuccess) return e;                                                  \
+                    configured[dev][SLOT_] = true;                                                   \
+                }                                                                                    \
+            }                                                                                        \
+            launch_pdl(router_tiled_kernel<RE_, RT_, true>, grid, 256, xs_bytes, st, x, n, H, wr, E, gw, \
+                       logits, sg_logit);                                                            \
+        } else {                                                                                     \
+            launch_pdl(router_tiled_kernel<RE_, RT_, false>, grid, 256, 0, st, x, n, H, wr, E, gw,  \
+                       logits, sg_logit);                                                            \
+        }                                                                                            \
         return cudaGetLastError();                                                                   \
     }
-    MOE_ROUTER_CASE(4, 8) MOE_ROUTER_CASE(2, 8) MOE_ROUTER_CASE(1, 8)
-    MOE_ROUTER_CASE(4, 4) MOE_ROUTER_CASE(2, 4) MOE_ROUTER_CASE(1, 4)
+    MOE_ROUTER_CASE(4, 8, 0) MOE_ROUTER_CASE(2, 8, 1) MOE_ROUTER_CASE(1, 8, 2)
+    MOE_ROUTER_CASE(4, 4, 3) MOE_ROUTER_CASE(2, 4, 4) MOE_ROUTER_CASE(1, 4, 5)
 #undef MOE_ROUTER_CASE
     return cudaErrorInvalidValue;
 }
