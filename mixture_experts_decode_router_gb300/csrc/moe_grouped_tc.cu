@@ -458,24 +458,40 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         __syncwarp();
     } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue
+        // The tile's global operands (NVFP4 scale2; per token the routing
+        // weight or the shared-expert gate) are loaded before the accumulator
+        // wait, lane l holding token l and l + 32, and broadcast by shuffles.
         const int q = warp & 3;                     // TMEM lane quarter of this warp
         const int row = 32 * q + lane;
         uint32_t acc_it = 0;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x, ++acc_it) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
             const int ab = acc_it % C::kAccBufs;
-            if (!ptx::mbar_wait_warp(&acc_full[ab], (acc_it / C::kAccBufs) & 1, s_abort, err, 3)) break;
-            ptx::tc_fence_after();
             const int m = t.m0 + row;
             const bool valid = m < t.out;
             const bool sh = t.e < 0;
+            float s2g = 1.f, s2u = 1.f;
+            if constexpr (FMT == MOE_W_NVFP4) {
+                s2g = sh ? p.sh_scale2[0][0] : p.scale2[0][t.le];
+                if constexpr (GU) s2u = sh ? p.sh_scale2[1][0] : p.scale2[1][t.le];
+            }
+            float tw[2] = {0.f, 0.f};   // down: weight of token lane, lane + 32 (times scale2)
+            if constexpr (!GU) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int j = lane + 32 * h;
+                    if (j < t.ntok) {
+                        float wgt;
+                        if (sh) wgt = p.sg_logit ? 1.0f / (1.0f + expf(-p.sg_logit[t.pos0 + j])) : 1.0f;
+                        else wgt = p.route_w[p.perm[t.pos0 + j]];
+                        tw[h] = wgt * s2g;
+                    }
+                }
+            }
+            if (!ptx::mbar_wait_warp(&acc_full[ab], (acc_it / C::kAccBufs) & 1, s_abort, err, 3)) break;
+            ptx::tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + ab * C::kAccCols;
             if constexpr (GU) {
-                float s2g = 1.f, s2u = 1.f;
-                if constexpr (FMT == MOE_W_NVFP4) {
-                    s2g = sh ? p.sh_scale2[0][0] : p.scale2[0][t.le];
-                    s2u = sh ? p.sh_scale2[1][0] : p.scale2[1][t.le];
-                }
                 uint16_t* dst = reinterpret_cast<uint16_t*>(sh ? p.act_sh_out : p.act_out);
                 for (int j0 = 0; j0 < t.ntok; j0 += 16) {
                     float g[16], u[16];
@@ -502,25 +518,21 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                     }
                 }
             } else {
-                float s2 = 1.f;
-                if constexpr (FMT == MOE_W_NVFP4) s2 = sh ? p.sh_scale2[0][0] : p.scale2[0][t.le];
                 float* dst = sh ? p.y_sh : p.y;
                 for (int j0 = 0; j0 < t.ntok; j0 += 16) {
                     float d[16];
                     ptx::tmem_ld16(tb + j0, d);
+                    float wj[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = j0 + jj;
+                        wj[jj] = __shfl_sync(0xffffffffu, j < 32 ? tw[0] : tw[1], j & 31);
+                    }
                     if (valid) {
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) {
                             const int j = j0 + jj;
-                            if (j < t.ntok) {
-                                float wgt;
-                                if (sh) {
-                                    wgt = p.sg_logit ? 1.0f / (1.0f + expf(-p.sg_logit[t.pos0 + j])) : 1.0f;
-                                } else {
-                                    wgt = p.route_w[p.perm[t.pos0 + j]];
-                                }
-                                dst[(size_t)(t.pos0 + j) * t.out + m] = d[jj] * (wgt * s2);
-                            }
+                            if (j < t.ntok) dst[(size_t)(t.pos0 + j) * t.out + m] = d[jj] * wj[jj];
                         }
                     }
                 }
