@@ -29,6 +29,13 @@
  *    current device; the caller owns every buffer (weights, input, outputs,
  *    workspace).  The library never allocates, frees or synchronises: each call
  *    only enqueues kernels on `stream` and returns.
+ *  - The layer input x and output out of moe_forward and moe_experts may
+ *    instead be pinned (page-locked) host memory mapped into the device's
+ *    address space (cudaHostAlloc, or any pinned allocation under unified
+ *    addressing).  The kernels then read x and write out over the host link
+ *    (NVLink-C2C on Grace systems) with plain loads and stores, and no copy is
+ *    needed before or after the call.  idx, w, logits, the weights and the
+ *    workspace stay in device memory.
  *  - Device pointers must be 16-byte aligned (MOE_ERR_ALIGNMENT otherwise),
  *    except the scale and scale2 arrays of moe_qmat_t, which need 4 bytes (so
  *    that one rank's slice of a stacked scale array can be passed as it is).

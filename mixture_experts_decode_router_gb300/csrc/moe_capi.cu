@@ -212,7 +212,6 @@ static moe_status_t enqueue_grouped(const moe_config_t* c, const moe_weights_t* 
     const int fmt = c->expert_fmt;
     const int H = c->hidden, I = c->inter, S = c->shared_inter, k = c->top_k, E = c->num_experts;
     const int E_loc = local_experts(c);
-    const bool f16_ops = fmt != MOE_W_BF16;   // FP8 / NVFP4 tiles use f16 operands
     uint16_t* xs = at<uint16_t>(ws, L.xs);
     uint16_t* xh = at<uint16_t>(ws, L.xh);
     cudaError_t e = launch_gather(fmt, static_cast<const uint16_t*>(x), n, H, k, at<int32_t>(ws, L.perm),
@@ -239,8 +238,7 @@ static moe_status_t enqueue_grouped(const moe_config_t* c, const moe_weights_t* 
     const bool tiles = E_loc > 0 || S > 0;   // otherwise the output is zero: combine alone
     // gate + up
     TcMaps maps;
-    if (tiles && !build_tc_maps(fmt, true, w, E_loc, H, I, S, n, n * k, xs, f16_ops ? (const void*)xh : x,
-                                &maps))
+    if (tiles && !build_tc_maps(fmt, true, w, E_loc, H, I, S, n, n * k, xs, xh, &maps))
         return MOE_ERR_CUDA;
     p.out_dim = I; p.in_dim = H; p.sh_out = S; p.sh_in = H;
     p.scale[0] = w->gate.scale; p.scale[1] = w->up.scale;

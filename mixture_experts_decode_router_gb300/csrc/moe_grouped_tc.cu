@@ -731,8 +731,11 @@ cudaError_t launch_tc(const TcMaps& maps, const TcParams& p, int num_sms, cudaSt
     return cudaGetLastError();
 }
 
-// xs[p, :] = x[perm[p] / k, :] for the grouped routes (bf16, or f16 for NVFP4),
-// and for NVFP4 also xh = f16(x) (the shared expert's operand).
+// xs[p, :] = x[perm[p] / k, :] for the grouped routes, and xh = x (the shared
+// expert's operand); 16-bit values as the tiles take them (F16: f16 for the FP8
+// and NVFP4 tiles, else bf16).  The tensor-core kernels' TMA copies therefore
+// read only workspace buffers: x itself is read here with plain loads, so it
+// may also live in pinned host memory.
 template <bool F16>
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int n, int H, int k,
                                                      const int32_t* __restrict__ perm,
@@ -740,7 +743,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
                                                      uint16_t* __restrict__ xs, uint16_t* __restrict__ xh) {
     pdl_wait();
     const int n_routes = offsets[E];
-    const int rows = n_routes + (F16 ? n : 0);
+    const int rows = n_routes + n;
     const int C8 = H >> 3;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)rows * C8;
          i += (int64_t)gridDim.x * blockDim.x) {

@@ -197,6 +197,39 @@ def test_exact_ties_go_to_the_lower_index(routing, n):
         assert torch.allclose(w.cpu(), torch.full((n, k), expect), rtol=1e-6)
 
 
+@pytest.mark.parametrize("fmt", [synth.FMT_BF16, synth.FMT_FP8_B128, synth.FMT_NVFP4])
+@pytest.mark.parametrize("n", [1, 3, 16])
+def test_host_mapped_input_and_output(fmt, n):
+    """x and out in pinned host memory: the kernels read x and write out across
+    the host link, with the bits of the device-buffer call."""
+    cfg = small("host_mapped", expert_fmt=fmt, shared_gate=True, top_k=3)
+    lw = synth.make_weights(cfg, "cuda")
+    x = synth.make_input(cfg, n, "cuda", gap_fn=gap_fn_for(oracle_layer(lw)))
+    layer = MoeLayer(lw, n)
+    ref, idx_ref, w_ref = layer.forward(x)
+    x_h = x.cpu().pin_memory()
+    out_h = torch.full((n, cfg.hidden), float("nan"), dtype=torch.bfloat16).pin_memory()
+    idx = torch.empty_like(idx_ref)
+    w = torch.empty_like(w_ref)
+    stream = torch.cuda.current_stream().cuda_stream
+    B.check(B.moe_forward(layer.c_cfg, layer.c_w, x_h, n, out_h, idx, w, layer.ws, layer.ws_bytes, stream))
+    torch.cuda.synchronize()
+    assert torch.equal(out_h.view(torch.int16), ref.cpu().view(torch.int16))
+    assert torch.equal(idx, idx_ref) and torch.equal(w, w_ref)
+    # accumulate: out (host) += the layer output
+    acc_layer = MoeLayer(lw, n, accumulate=True)
+    base = synth.make_input(cfg, n, "cuda").cpu()
+    out2 = base.clone().pin_memory()
+    B.check(B.moe_forward(acc_layer.c_cfg, acc_layer.c_w, x_h, n, out2, idx, w, acc_layer.ws,
+                          acc_layer.ws_bytes, stream))
+    torch.cuda.synchronize()
+    out2_ref = base.cuda()
+    acc_layer.forward(x, out=out2_ref)
+    torch.cuda.synchronize()
+    assert torch.equal(out2.view(torch.int16), out2_ref.cpu().view(torch.int16))
+    assert layer.device_error() == 0 and acc_layer.device_error() == 0
+
+
 def test_zero_tokens_is_a_noop():
     cfg = small("empty")
     lw = synth.make_weights(cfg, "cuda")

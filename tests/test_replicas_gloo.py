@@ -42,3 +42,15 @@ def test_two_replica_ranks_agree_on_slowest_time_and_throughput():
 def test_single_process_is_its_own_maximum():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
+
+
+def test_end_to_end_reports_the_faster_host_buffer_mode_and_both_figures():
+    import bench
+    few = bench.e2e_line(1, 1, 2048, 1000, zero_copy_ms=31.0, copies_ms=45.0)
+    assert few["mode"] == "zero_copy" and few["us_per_call"] == 31.0
+    assert few["h2d_bytes_per_step"] == few["d2h_bytes_per_step"] == 2048 * 2
+    assert few["with_copies"]["us_per_call"] == 45.0
+    many = bench.e2e_line(2, 256, 2048, 100, zero_copy_ms=36.0, copies_ms=30.0)
+    assert many["mode"] == "with_copies" and many["us_per_call"] == 300.0
+    # whole-job tokens/s over both ranks, from the chosen mode's time
+    assert abs(many["value"] - 2 * 256 * 100 / 30e-3) < 1e-6 * many["value"]
