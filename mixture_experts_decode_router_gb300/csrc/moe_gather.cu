@@ -1,0 +1,100 @@
+// moe_gather.cu -- the grouped path's small memory-bound kernels around the
+// tensor-core GEMMs (sm_103a): gathering the token rows into expert order
+// before them, and combining the weighted expert rows after them.
+#include "moe_launch.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// xs[p, :] = x[perm[p] / k, :] for the grouped routes, and xh = x (the shared
+// expert's operand); 16-bit values as the tiles take them (F16: f16 for the FP8
+// and NVFP4 tiles, else bf16).  The tensor-core kernels' TMA copies therefore
+// read only workspace buffers: x itself is read here with plain loads, so it
+// may also live in pinned host memory.
+template <bool F16>
+__global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int n, int H, int k,
+                                                     const int32_t* __restrict__ perm,
+                                                     const int32_t* __restrict__ offsets, int E,
+                                                     uint16_t* __restrict__ xs, uint16_t* __restrict__ xh) {
+    pdl_wait();
+    const int n_routes = offsets[E];
+    const int rows = n_routes + n;
+    const int C8 = H >> 3;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)rows * C8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int r = (int)(i / C8), c = (int)(i - (int64_t)r * C8);
+        const bool routed = r < n_routes;
+        const int t = routed ? perm[r] / k : r - n_routes;
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c);
+        if constexpr (F16) {
+            uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xffff0000u);
+                const __half2 h = __floats2half2_rn(fminf(fmaxf(lo, -65504.f), 65504.f),
+                                                    fminf(fmaxf(hi, -65504.f), 65504.f));
+                w4[q] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        uint16_t* dst = routed ? xs + (size_t)r * H : xh + (size_t)(r - n_routes) * H;
+        reinterpret_cast<uint4*>(dst)[c] = v;
+    }
+    pdl_trigger();
+}
+
+// out[t, h] = bf16( sum_j y[inv[t*k + j], h] (slot order) + y_sh[t, h] ).
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ ysh,
+                                                      const int32_t* __restrict__ inv, int n, int H, int k,
+                                                      int has_shared, int accumulate, uint16_t* __restrict__ out) {
+    pdl_wait();
+    const int C4 = H >> 2;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)n * C4;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / C4), c = (int)(i - (int64_t)t * C4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const int pos = __ldg(inv + t * k + j);
+            if (pos < 0) continue;
+            const float4 v = __ldg(reinterpret_cast<const float4*>(y + (size_t)pos * H) + c);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        if (has_shared) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(ysh + (size_t)t * H) + c);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        if (accumulate) {
+            const uint2 o = reinterpret_cast<const uint2*>(out + (size_t)t * H)[c];
+            acc.x += __uint_as_float(o.x << 16); acc.y += __uint_as_float(o.x & 0xffff0000u);
+            acc.z += __uint_as_float(o.y << 16); acc.w += __uint_as_float(o.y & 0xffff0000u);
+        }
+        const uint32_t lo = pack_bf16(acc.x, acc.y), hi = pack_bf16(acc.z, acc.w);
+        reinterpret_cast<uint2*>(out + (size_t)t * H)[c] = make_uint2(lo, hi);
+    }
+    pdl_trigger();
+}
+
+}  // namespace
+
+cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const int32_t* perm,
+                          const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, int num_sms,
+                          cudaStream_t st) {
+    const int grid = 2 * num_sms;
+    if (fmt != MOE_W_BF16) launch_pdl(gather_kernel<true>, grid, 256, 0, st, x, n, H, k, perm, offsets, E, xs, xh);
+    else launch_pdl(gather_kernel<false>, grid, 256, 0, st, x, n, H, k, perm, offsets, E, xs, xh);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* y, const float* ysh, const int32_t* inv, int n, int H, int k,
+                           int has_shared, int accumulate, uint16_t* out, int num_sms, cudaStream_t st) {
+    launch_pdl(combine_kernel, 2 * num_sms, 256, 0, st, y, ysh, inv, n, H, k, has_shared, accumulate, out);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
