@@ -64,8 +64,9 @@ struct TcCfg {
     // holds only the raw codes and the token tiles, so the raw ring is deep.
     // Tensor memory: kAccBufs accumulators of kMats x NT fp32 columns (two, so
     // a tile's epilogue overlaps the next tile's MMAs; one for dequantised
-    // gate/up, whose 32+ K stages per tile hide the epilogue, so that the
-    // operand ring gets the columns), then (dequantised tiles) the operand
+    // gate/up, so that the operand ring gets the columns -- its thin tiles
+    // still alternate between the accumulator's halves, see AccSlots), then
+    // (dequantised tiles) the operand
     // stages, kMats x BK/2 columns each (two f16 per 32-bit column, row i of
     // the tile in lane i).
     static constexpr int kAccBufs = (kDeq && GU) ? 1 : 2;
@@ -112,6 +113,39 @@ struct TcCfg {
     static_assert(kOffRaw % 1024 == 0 && kRawMat % 1024 == 0, "swizzled raw stages sit on 1024-byte boundaries");
     static_assert(!kDeq || (kPartElems % 16 == 0 && BK % (kDeq ? kPartElems : 1) == 0),
                   "a dequant part is whole 16-code blocks of one matrix");
+};
+
+// Accumulator slots of the tiles, chosen alike by the MMA warp and the
+// epilogue (both walk the same tile sequence).  Two accumulators (kAccBufs
+// == 2): tile i takes buffer i % 2.  One accumulator: it is two slots of NT/2
+// tokens; a tile of at most NT/2 tokens takes one slot, the thin tiles
+// alternating, and a wider tile takes both.  So consecutive thin tiles are
+// double-buffered: one's epilogue overlaps the next one's MMAs.  Each slot has
+// its own full/empty barriers, and each role counts its uses of each slot for
+// the barrier parity.
+template <int kAccBufs, int kAccCols>
+struct AccSlots {
+    uint32_t use[2] = {0u, 0u};
+    uint32_t seq = 0;   // tiles (two accumulators) or thin tiles (one)
+    // mask: bit s = slot s used; col: first accumulator column of the tile.
+    __device__ __forceinline__ void pick(int nmma, int& mask, int& col) {
+        if constexpr (kAccBufs == 2) {
+            const int s = (int)(seq++ & 1u);
+            mask = 1 << s;
+            col = s * kAccCols;
+        } else if (nmma <= NT / 2) {
+            const int s = (int)(seq++ & 1u);
+            mask = 1 << s;
+            col = s * (NT / 2);
+        } else {
+            mask = 3;
+            col = 0;
+        }
+    }
+    __device__ __forceinline__ void done(int mask) {
+        use[0] += mask & 1;
+        use[1] += (mask >> 1) & 1;
+    }
 };
 
 struct Tile {
@@ -385,15 +419,21 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp runs the loop, so the operand descriptors are
         // warp-uniform values; one elected lane issues the MMAs and commits.
-        uint32_t it = 0, git = 0, acc_it = 0;
-        for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x, ++acc_it) {
+        uint32_t it = 0, git = 0;
+        AccSlots<C::kAccBufs, C::kAccCols> slots;
+        for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
-            const int ab = acc_it % C::kAccBufs;
-            if (!ptx::mbar_wait_warp(&acc_empty[ab], ((acc_it / C::kAccBufs) & 1) ^ 1, s_abort, err, 2)) break;
-            ptx::tc_fence_after();
             const int nmma = ((t.ntok + 15) >> 4) << 4;
+            int amask, acol;
+            slots.pick(nmma, amask, acol);
+            bool free_ok = true;
+            for (int sl = 0; sl < 2 && free_ok; ++sl)
+                if ((amask >> sl) & 1)
+                    free_ok = ptx::mbar_wait_warp(&acc_empty[sl], (slots.use[sl] & 1) ^ 1, s_abort, err, 2);
+            if (!free_ok) break;
+            ptx::tc_fence_after();
             const uint32_t idesc = ptx::idesc_f16(BM, nmma, !C::kF16);
-            const uint32_t d0 = tmem + ab * C::kAccCols;
+            const uint32_t d0 = tmem + acol;
             const int KB = (t.K + BK - 1) / BK;
             bool ok = true;
             for (int kb = 0; kb < KB && ok; ++git) {
@@ -444,8 +484,11 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                 __syncwarp();
             }
             if (!ok) break;
-            if (ptx::elect_one()) ptx::mma_commit(&acc_full[ab]);
+            if (ptx::elect_one())
+                for (int sl = 0; sl < 2; ++sl)
+                    if ((amask >> sl) & 1) ptx::mma_commit(&acc_full[sl]);
             __syncwarp();
+            slots.done(amask);
         }
         // Every MMA issued has completed before TMEM is released.
         if (ptx::elect_one()) {
@@ -460,10 +503,11 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         // wait, lane l holding token l and l + 32, and broadcast by shuffles.
         const int q = warp & 3;                     // TMEM lane quarter of this warp
         const int row = 32 * q + lane;
-        uint32_t acc_it = 0;
-        for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x, ++acc_it) {
+        AccSlots<C::kAccBufs, C::kAccCols> slots;
+        for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
-            const int ab = acc_it % C::kAccBufs;
+            int amask, acol;
+            slots.pick(((t.ntok + 15) >> 4) << 4, amask, acol);
             const int m = t.m0 + row;
             const bool valid = m < t.out;
             const bool sh = t.e < 0;
@@ -485,9 +529,13 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                     }
                 }
             }
-            if (!ptx::mbar_wait_warp(&acc_full[ab], (acc_it / C::kAccBufs) & 1, s_abort, err, 3)) break;
+            bool full_ok = true;
+            for (int sl = 0; sl < 2 && full_ok; ++sl)
+                if ((amask >> sl) & 1)
+                    full_ok = ptx::mbar_wait_warp(&acc_full[sl], slots.use[sl] & 1, s_abort, err, 3);
+            if (!full_ok) break;
             ptx::tc_fence_after();
-            const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + ab * C::kAccCols;
+            const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + acol;
             if constexpr (GU) {
                 uint16_t* dst = reinterpret_cast<uint16_t*>(sh ? p.act_sh_out : p.act_out);
                 for (int j0 = 0; j0 < t.ntok; j0 += 16) {
@@ -536,7 +584,10 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);
+            if (lane == 0)
+                for (int sl = 0; sl < 2; ++sl)
+                    if ((amask >> sl) & 1) ptx::mbar_arrive(&acc_empty[sl]);
+            slots.done(amask);
         }
     } else if constexpr (C::kDeq) {
         // ------------------------------------------------------------ dequant
