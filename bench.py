@@ -473,8 +473,7 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16" if fmt == "bf16" else ("fp8e4m3-w/bf16-a" if fmt == "fp8_b128"
-                                                   else "nvfp4-w/bf16-a"),
+            "dtype": compute_dtype(fmt, nm == 7),
             "data": "synthetic (seeded; weights N(0,0.02), input N(0,1))",
             "config": {"workload": cfg.name, "n_tokens": n, "hidden": H, "num_experts": E,
                        "top_k": k, "inter": I, "shared_inter": S, "routing": cfg.routing,
@@ -497,6 +496,18 @@ def run_ours(args):
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def compute_dtype(fmt: str, grouped: bool) -> str:
+    """The arithmetic the path computes in: BF16 operands (tensor cores on the
+    grouped path, CUDA cores otherwise) with fp32 accumulation; FP8 / NVFP4
+    weights dequantised to f16 for the grouped path's f16 MMA, to fp32 in the
+    CUDA-core kernels."""
+    if fmt == "bf16":
+        return "bf16"
+    w = "fp8e4m3" if fmt == "fp8_b128" else "nvfp4"
+    return f"f16 ({w} weights dequantised, bf16 activations as f16, fp32 accumulate)" if grouped \
+        else f"fp32 ({w} weights dequantised, bf16 activations)"
 
 
 def e2e_line(world, n, H, steps, zero_copy_ms, copies_ms):
