@@ -29,13 +29,16 @@
  *    current device; the caller owns every buffer (weights, input, outputs,
  *    workspace).  The library never allocates, frees or synchronises: each call
  *    only enqueues kernels on `stream` and returns.
- *  - The layer input x and output out of moe_forward and moe_experts may
- *    instead be pinned (page-locked) host memory mapped into the device's
- *    address space (cudaHostAlloc, or any pinned allocation under unified
- *    addressing).  The kernels then read x and write out over the host link
- *    (NVLink-C2C on Grace systems) with plain loads and stores, and no copy is
- *    needed before or after the call.  idx, w, logits, the weights and the
- *    workspace stay in device memory.
+ *  - The layer input x (moe_route, moe_experts, moe_forward) and output out
+ *    (moe_experts, moe_forward) may instead be pinned (page-locked) host
+ *    memory mapped into the device's address space (cudaHostAlloc, or any
+ *    pinned allocation under unified addressing).  The kernels then reach x
+ *    and out over the host link (NVLink-C2C on Grace systems) and no copy is
+ *    needed before or after the call: one token's kernel reads x directly;
+ *    for more tokens the call first copies x into the workspace with a kernel
+ *    of its own, so that its other kernels read it from device memory.  Host
+ *    memory that is not pinned is refused (MOE_ERR_HOST_MEMORY).  idx, w,
+ *    logits, the weights and the workspace stay in device memory.
  *  - Device pointers must be 16-byte aligned (MOE_ERR_ALIGNMENT otherwise),
  *    except the scale and scale2 arrays of moe_qmat_t, which need 4 bytes (so
  *    that one rank's slice of a stacked scale array can be passed as it is).
@@ -101,7 +104,8 @@ typedef enum {
     MOE_ERR_WORKSPACE = 4,       /* workspace missing or smaller than moe_workspace_bytes()  */
     MOE_ERR_CUDA = 5,            /* a CUDA call failed while enqueueing (cudaGetLastError)   */
     MOE_ERR_ALIGNMENT = 6,       /* a device pointer is not aligned (16 bytes; 4 for scales) */
-    MOE_ERR_ALIAS = 7            /* `out` overlaps `x`                                       */
+    MOE_ERR_ALIAS = 7,           /* `out` overlaps `x`                                       */
+    MOE_ERR_HOST_MEMORY = 8      /* `x` or `out` is host memory that is not pinned (page-locked) */
 } moe_status_t;
 
 typedef enum { MOE_ROUTE_SOFTMAX = 0, MOE_ROUTE_SIGMOID_BIAS = 1 } moe_routing_t;
@@ -197,7 +201,7 @@ size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t max_tokens);
  *   logits  device fp32  [n, E]   (out, optional: NULL = not returned)
  *   ws      device workspace of at least moe_workspace_bytes(cfg, n) bytes
  * Errors: MOE_ERR_NULL, MOE_ERR_INVALID_CONFIG, MOE_ERR_UNSUPPORTED,
- * MOE_ERR_WORKSPACE, MOE_ERR_ALIGNMENT, MOE_ERR_CUDA. */
+ * MOE_ERR_WORKSPACE, MOE_ERR_ALIGNMENT, MOE_ERR_HOST_MEMORY, MOE_ERR_CUDA. */
 moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* wts,
                        const void* x, int32_t n,
                        int32_t* idx, float* w, float* logits,

@@ -24,6 +24,7 @@ MOE_ERR_WORKSPACE = 4
 MOE_ERR_CUDA = 5
 MOE_ERR_ALIGNMENT = 6
 MOE_ERR_ALIAS = 7
+MOE_ERR_HOST_MEMORY = 8
 
 MOE_ROUTE_SOFTMAX = 0
 MOE_ROUTE_SIGMOID_BIAS = 1

@@ -39,6 +39,20 @@ struct Marks {
 };
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Where a caller's x or out lives: 0 device (or managed) memory, 1 pinned host
+// memory the device addresses at the same pointer, -1 anything else (host memory
+// that is not pinned, or a pointer CUDA does not know).
+static int residency(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return 0;
+    if (a.type == cudaMemoryTypeHost && a.devicePointer == p) return 1;
+    return -1;
+}
 static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 static moe_status_t check_config(const moe_config_t* c) {
@@ -157,6 +171,16 @@ static QMatDev qdev(const moe_qmat_t& q, int out_dim, int in_dim, int e_base) {
     d.in_dim = in_dim;
     d.e_base = e_base;
     return d;
+}
+
+// Copy a pinned-host-resident x ([n, H] BF16) into the workspace; `x` then
+// points there.
+static moe_status_t stage_x(const moe_config_t* c, const void*& x, int32_t n, void* ws, const WsLayout& L,
+                            cudaStream_t st) {
+    void* xd = at<uint16_t>(ws, L.xd);
+    if (launch_copy16(x, xd, (size_t)n * c->hidden * 2, device_sm_count(), st) != cudaSuccess) return MOE_ERR_CUDA;
+    x = xd;
+    return MOE_OK;
 }
 
 // Enqueue router + top-k.  Arguments already validated.  `with_group`: the
@@ -382,9 +406,12 @@ moe_status_t moe_route(const moe_config_t* cfg_in, const moe_weights_t* wts, con
     if (wts->shared_gate_w && !aligned16(wts->shared_gate_w)) return MOE_ERR_ALIGNMENT;
     WsLayout L;
     if ((s = check_ws(cfg, n, ws, ws_bytes, &L)) != MOE_OK) return s;
+    const int x_res = residency(x);
+    if (x_res < 0) return MOE_ERR_HOST_MEMORY;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (x_res == 1 && n > 1 && (s = stage_x(cfg, x, n, ws, L, st)) != MOE_OK) return s;
     Marks mk;
-    return enqueue_route(cfg, wts, x, n, idx, w, logits, ws, L, false, reinterpret_cast<cudaStream_t>(stream),
-                         mk);
+    return enqueue_route(cfg, wts, x, n, idx, w, logits, ws, L, false, st, mk);
 }
 
 moe_status_t moe_experts(const moe_config_t* cfg_in, const moe_weights_t* wts, const void* x, int32_t n,
@@ -402,9 +429,12 @@ moe_status_t moe_experts(const moe_config_t* cfg_in, const moe_weights_t* wts, c
     if (overlaps(x, out, (size_t)n * cfg->hidden * 2)) return MOE_ERR_ALIAS;
     WsLayout L;
     if ((s = check_ws(cfg, n, ws, ws_bytes, &L)) != MOE_OK) return s;
+    const int x_res = residency(x);
+    if (x_res < 0 || residency(out) < 0) return MOE_ERR_HOST_MEMORY;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (x_res == 1 && n > 1 && (s = stage_x(cfg, x, n, ws, L, st)) != MOE_OK) return s;
     Marks mk;
-    return enqueue_experts(cfg, wts, x, n, idx, w, out, ws, L, false, false,
-                           reinterpret_cast<cudaStream_t>(stream), mk);
+    return enqueue_experts(cfg, wts, x, n, idx, w, out, ws, L, false, false, st, mk);
 }
 
 static moe_status_t forward_impl(const moe_config_t* cfg_in, const moe_weights_t* wts, const void* x,
@@ -424,6 +454,8 @@ static moe_status_t forward_impl(const moe_config_t* cfg_in, const moe_weights_t
     if (overlaps(x, out, (size_t)n * cfg->hidden * 2)) return MOE_ERR_ALIAS;
     WsLayout L;
     if ((s = check_ws(cfg, n, ws, ws_bytes, &L)) != MOE_OK) return s;
+    const int x_res = residency(x);
+    if (x_res < 0 || residency(out) < 0) return MOE_ERR_HOST_MEMORY;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int32_t* idx_p = idx ? idx : at<int32_t>(ws, L.idx);
     float* w_p = w ? w : at<float>(ws, L.w);
@@ -469,6 +501,9 @@ static moe_status_t forward_impl(const moe_config_t* cfg_in, const moe_weights_t
             (void)cudaGetLastError();   // not launchable here: the multi-kernel path below
         }
     }
+    // More than one token: a host-resident x is copied into the workspace
+    // once, rather than read across the host link by every kernel and block.
+    if (x_res == 1 && (s = stage_x(cfg, x, n, ws, L, st)) != MOE_OK) return s;
     if (local_experts(cfg) == 0 && !idx && !w) {
         // No expert held here and no routing asked for (the shared-expert call
         // of expert parallelism): only the shared-gate logit is needed.
@@ -532,6 +567,7 @@ const char* moe_status_string(moe_status_t status) {
         case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA launch failed";
         case MOE_ERR_ALIGNMENT: return "MOE_ERR_ALIGNMENT: a device pointer is not aligned (16 bytes; scales 4)";
         case MOE_ERR_ALIAS: return "MOE_ERR_ALIAS: out overlaps x";
+        case MOE_ERR_HOST_MEMORY: return "MOE_ERR_HOST_MEMORY: x or out is host memory that is not pinned";
         default: return "unknown moe_status_t";
     }
 }

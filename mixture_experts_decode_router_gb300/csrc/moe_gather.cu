@@ -1,6 +1,8 @@
 // moe_gather.cu -- the grouped path's small memory-bound kernels around the
 // tensor-core GEMMs (sm_103a): gathering the token rows into expert order
 // before them, and combining the weighted expert rows after them.
+#include <algorithm>
+
 #include "moe_launch.cuh"
 
 namespace moe {
@@ -80,7 +82,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     pdl_trigger();
 }
 
+// dst = src, n16 16-byte words (x staged from pinned host memory).
+__global__ void __launch_bounds__(256) copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                     size_t n16) {
+    pdl_wait();
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+    pdl_trigger();
+}
+
 }  // namespace
+
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t st) {
+    const size_t n16 = bytes / 16;
+    const int grid = (int)std::min<size_t>((size_t)num_sms, (n16 + 255) / 256);
+    launch_pdl(copy16_kernel, grid > 0 ? grid : 1, 256, 0, st, static_cast<const uint4*>(src),
+               static_cast<uint4*>(dst), n16);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const int32_t* perm,
                           const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, int num_sms,

@@ -34,7 +34,7 @@ constexpr int kTcTokensPerTile = 64;
 
 struct WsLayout {
     size_t ctrl, logits, sg_logit, idx, w, counts, offsets, perm, active, act, act_sh,
-        inv, segs, xs, xh, as, ash, y, ysh, xe, total;
+        inv, segs, xs, xh, as, ash, y, ysh, xe, xd, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -66,12 +66,13 @@ inline WsLayout ws_layout(const moe_config_t& c, int64_t n) {
     L.inv = take(sizeof(int32_t) * n * k);                       // route -> sorted position
     L.segs = take(sizeof(int32_t) * 3 * grouped_segs_bound(n, k, E));
     L.xs = take(sizeof(uint16_t) * n * k * H);                   // expert-sorted activations
-    L.xh = take(sizeof(uint16_t) * n * H);                       // f16 copy of x (FP8, NVFP4)
+    L.xh = take(sizeof(uint16_t) * n * H);                       // copy of x for the shared expert (f16 / bf16)
     L.as = take(sizeof(uint16_t) * n * k * I);                   // SiLU(g)*u, sorted rows
     L.ash = take(sizeof(uint16_t) * n * (S > 0 ? S : 1));
     L.y = take(sizeof(float) * n * k * H);                       // weighted down rows
     L.ysh = take(sizeof(float) * n * H);
     L.xe = take(sizeof(uint16_t) * n * H);                       // pre-expert RMSNorm of x
+    L.xd = take(sizeof(uint16_t) * n * H);                       // x staged from pinned host memory
     L.total = off;
     return L;
 }

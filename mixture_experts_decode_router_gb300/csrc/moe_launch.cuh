@@ -68,6 +68,7 @@ bool build_tc_maps(int fmt, bool gate_up, const moe_weights_t* w, int E, int H, 
                    int n_routes_max, const void* act_routed, const void* act_shared, TcMaps* maps);
 cudaError_t launch_grouped_tc(int fmt, bool gate_up, const TcMaps& maps, const TcParams& p, int num_sms,
                               cudaStream_t st);
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t st);
 cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const int32_t* perm,
                           const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, int num_sms,
                           cudaStream_t st);

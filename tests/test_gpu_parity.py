@@ -230,6 +230,32 @@ def test_host_mapped_input_and_output(fmt, n):
     assert layer.device_error() == 0 and acc_layer.device_error() == 0
 
 
+def test_pageable_host_memory_is_refused_and_host_route_matches():
+    cfg = small("host_refuse")
+    lw = synth.make_weights(cfg, "cuda")
+    x = synth.make_input(cfg, 5, "cuda", gap_fn=gap_fn_for(oracle_layer(lw)))
+    layer = MoeLayer(lw, 5)
+    stream = torch.cuda.current_stream().cuda_stream
+    out = torch.empty(5, cfg.hidden, dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty(5, cfg.top_k, dtype=torch.int32, device="cuda")
+    w = torch.empty(5, cfg.top_k, dtype=torch.float32, device="cuda")
+    x_pageable = x.cpu()   # not pinned
+    assert not x_pageable.is_pinned()
+    s = B.moe_forward(layer.c_cfg, layer.c_w, x_pageable, 5, out, idx, w, layer.ws, layer.ws_bytes, stream)
+    assert s == B.MOE_ERR_HOST_MEMORY
+    out_pageable = torch.empty(5, cfg.hidden, dtype=torch.bfloat16)
+    s = B.moe_forward(layer.c_cfg, layer.c_w, x, 5, out_pageable, idx, w, layer.ws, layer.ws_bytes, stream)
+    assert s == B.MOE_ERR_HOST_MEMORY
+    # moe_route with x in pinned host memory: the device-buffer result, bit for bit
+    idx_d, w_d, lg_d = layer.route(x)
+    x_h = x.cpu().pin_memory()
+    lg = torch.empty(5, cfg.num_experts, dtype=torch.float32, device="cuda")
+    B.check(B.moe_route(layer.c_cfg, layer.c_w, x_h, 5, idx, w, lg, layer.ws, layer.ws_bytes, stream))
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx_d) and torch.equal(w, w_d) and torch.equal(lg, lg_d)
+    assert layer.device_error() == 0
+
+
 def test_zero_tokens_is_a_noop():
     cfg = small("empty")
     lw = synth.make_weights(cfg, "cuda")

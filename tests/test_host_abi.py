@@ -221,6 +221,6 @@ def test_zero_tokens_and_negative(lib):
 
 
 def test_status_strings(lib):
-    for s in range(8):
+    for s in range(9):
         assert B.moe_status_string(s).startswith("MOE_")
     assert "unknown" in B.moe_status_string(99)
