@@ -10,7 +10,7 @@ single-token decode, hidden 2048, 256 experts, top-8).  The L2 is flushed
 (a write of 2.5x its size) between steps, outside the timed events, because
 the weights one call touches fit in L2.  Prints one JSON line.
 
-Multi-GPU: the layer has no exchange step in this build, so N GPUs run N
+Multi-GPU: the measured layer has no exchange step, so N GPUs run N
 independent replicas ("scaling": "weak"); value = tokens of all ranks / the
 slowest rank's time.
 """

@@ -440,8 +440,8 @@ def test_accumulate_adds_into_out():
 
 
 def test_expert_parallel_driver_single_rank():
-    """Without a process group the driver is the whole layer: the partial of
-    all experts, then the shared expert added."""
+    """Without a process group ExpertParallelMoe is the whole layer: the partial
+    of all experts, then the shared expert added."""
     from mixture_experts_decode_router_gb300.ep import ExpertParallelMoe
     cfg = small("ep_driver", num_experts=32, top_k=4, routing=synth.ROUTE_SIGMOID_BIAS,
                 routed_scaling_factor=2.5, shared_gate=True, pre_expert_norm=True)
