@@ -1,14 +1,18 @@
 #!/usr/bin/env python
 """Benchmark of the MoE decode-layer forward on one GB300 (or N replicas).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode_n1]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|<name>]
     python bench.py --impl reference ...      # the fp64 CPU oracle, timed on host cores
 
 A step is one ``moe_forward`` call (router, top-k, expert grouping, gate+up,
-down+blend) over one batch of synthetic input of the workload (default: the
-single-token decode, hidden 2048, 256 experts, top-8).  The L2 is flushed
-(a write of 2.5x its size) between steps, outside the timed events, because
-the weights one call touches fit in L2.  Prints one JSON line.
+down+blend) over one batch of synthetic input of a workload.  By default every
+workload is measured (tiny_n1, decode_n1, decode_n16, fp8_n64, nvfp4_n256:
+N = 1 to 256 tokens); the line's headline fields (value, ms_per_step,
+roofline, e2e, cpu_baseline) are the single-token decode's (decode_n1: hidden
+2048, 256 experts, top-8), and ``workloads`` holds one entry per workload with
+the same figures.  The L2 is flushed (a write of 2.5x its size) between steps,
+outside the timed events, because the weights one call touches fit in L2.
+Prints one JSON line.
 
 Multi-GPU: the measured layer has no exchange step, so N GPUs run N
 independent replicas ("scaling": "weak"); value = tokens of all ranks / the
@@ -30,6 +34,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer µs/call, tokens/s and HBM GB/s (frac of ~8 TB/s) at N=1–256"
+HEADLINE = "decode_n1"
+ALL_WORKLOADS = ("tiny_n1", "decode_n1", "decode_n16", "fp8_n64", "nvfp4_n256")
 # Kernel sequence of each expert path, by the number of stage markers a call records.
 STAGES_BY_MARKS = {
     2: ["fused"],
@@ -41,21 +47,29 @@ STAGES_BY_MARKS = {
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=3000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="decode_n1")
+    p.add_argument("--workload", default="all",
+                   help="'all' (every workload; headline decode_n1) or one workload name")
     p.add_argument("--path", default="auto", choices=["auto", "token_major", "grouped"])
     p.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
     p.add_argument("--experts", type=int, default=0,
                    help="override the workload's expert count (a smaller layer of the same kernels, "
                         "for profiler captures)")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--oracle-budget", type=float, default=15.0,
-                   help="seconds of oracle work for the CPU baseline sample")
+    p.add_argument("--oracle-budget", type=float, default=6.0,
+                   help="seconds of oracle work per CPU baseline sample (each workload, each core count)")
     p.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--oracle-tokens", type=int, default=0, help=argparse.SUPPRESS)
+    p.add_argument("--oracle-procs", type=int, default=1, help=argparse.SUPPRESS)
     return p.parse_args(argv)
+
+
+def workload_names(args):
+    if args.workload == "all":
+        return list(ALL_WORKLOADS)
+    return [args.workload]
 
 
 # ------------------------------------------------------------------ helpers
@@ -186,18 +200,29 @@ def _dist():
 
 # ------------------------------------------------------------------ oracle (CPU) leg
 
+def _oracle_pool_tokens(cfg) -> int:
+    """Tokens of the oracle's sample pool: a few, fewer for the largest layer
+    (each of its tokens touches 8 experts of 3 x 14.7 M elements)."""
+    return 4 if cfg.hidden * cfg.inter >= 4 << 20 else 8
+
+
 def _oracle_child(args):
-    """Runs in a fresh process with one BLAS thread: the oracle as it stands on a
-    bounded sample of the workload's tokens.  Prints one JSON object."""
+    """Runs in a fresh process with no GPU and one BLAS thread per process: the
+    oracle as it stands on a bounded sample of the workload's tokens, one token
+    per call, in ``--oracle-procs`` worker processes that each take the pool's
+    tokens in turn.  Prints one JSON object."""
     import numpy as np
     import torch
 
     from mixture_experts_decode_router_gb300 import synth
     from oracle import moe_oracle as O
 
-    torch.set_num_threads(1)
-    cfg = workload_config(args)
-    n_pool = max(cfg.n_tokens, 8)
+    cfg = workload_config(args, args.workload)
+    n_pool = _oracle_pool_tokens(cfg)
+    # Input preparation (outside the timed region): the pool's rows, their
+    # routing, and only the experts that routing touches, generated with every
+    # host thread.
+    torch.set_num_threads(max(1, os.cpu_count() or 1))
     x = synth.make_input(cfg, n_pool, "cpu", dup_frac=0.0, stream=7)
     xb = x.view(torch.int16).numpy().view(np.uint16)
     router = synth.make_router(cfg).view(torch.int16).numpy().view(np.uint16)
@@ -205,69 +230,75 @@ def _oracle_child(args):
     bias = bias.numpy() if bias is not None else None
     sgw = synth.make_shared_gate_w(cfg)
     sgw = sgw.view(torch.int16).numpy().view(np.uint16) if sgw is not None else None
-
-    # Route the pool first (cheap), then generate only the experts it touches
-    # (generation is input preparation, outside the timed region).
     lg = O.router_logits(O.bf16_decode(xb), router)
     idx, _ = O.route(lg, cfg.routing, cfg.top_k, cfg.norm_topk_prob, cfg.routed_scaling_factor,
                      bias)
     need = sorted(set(int(e) for e in np.unique(idx)))
 
-    class Lazy(dict):
-        def __init__(self, tensor, field):
-            super().__init__()
-            self.tensor, self.field = tensor, field
+    def qm(tensor, experts):
+        w, sc, s2 = {}, {}, {}
+        for e in experts:
+            q, s, s2v = synth.expert_matrix(cfg, tensor, e)
+            w[e] = q.view(torch.int16).numpy().view(np.uint16) if q.dtype == torch.bfloat16 \
+                else q.numpy()
+            if s is not None:
+                sc[e] = s.numpy()
+            if s2v is not None:
+                s2[e] = np.float32(s2v)
+        return O.QMat(cfg.expert_fmt, w, sc or None, s2 or None)
 
-        def __missing__(self, e):
-            q, s, s2 = synth.expert_matrix(cfg, self.tensor, int(e))
-            v = {"w": q, "scale": s, "scale2": s2}[self.field]
-            if self.field == "w" and v.dtype == torch.bfloat16:
-                v = v.view(torch.int16).numpy().view(np.uint16)
-            elif self.field == "scale2":
-                v = np.float32(v)
-            else:
-                v = v.numpy()
-            self[e] = v
-            return v
-
-    def qm(tensor):
-        return O.QMat(cfg.expert_fmt, Lazy(tensor, "w"), Lazy(tensor, "scale"),
-                      Lazy(tensor, "scale2"))
-
+    sh = [0] if cfg.shared_inter > 0 else []
     layer = O.OracleLayer(hidden=cfg.hidden, num_experts=cfg.num_experts, top_k=cfg.top_k,
                           inter=cfg.inter, shared_inter=cfg.shared_inter, routing=cfg.routing,
                           norm_topk_prob=cfg.norm_topk_prob,
                           routed_scaling_factor=cfg.routed_scaling_factor, router_w=router,
-                          gate=qm("gate"), up=qm("up"), down=qm("down"), sh_gate=qm("sh_gate"),
-                          sh_up=qm("sh_up"), sh_down=qm("sh_down"), correction_bias=bias,
-                          shared_gate_w=sgw)
-    for q in (layer.gate, layer.up, layer.down):
-        for e in need:
-            q.w[e], q.scale[e] if cfg.expert_fmt != "bf16" else None
-            if cfg.expert_fmt == "nvfp4":
-                q.scale2[e]
-    for q in (layer.sh_gate, layer.sh_up, layer.sh_down):
-        q.w[0], q.scale[0] if cfg.expert_fmt != "bf16" else None
-        if cfg.expert_fmt == "nvfp4":
-            q.scale2[0]
+                          gate=qm("gate", need), up=qm("up", need), down=qm("down", need),
+                          sh_gate=qm("sh_gate", sh) if sh else None,
+                          sh_up=qm("sh_up", sh) if sh else None,
+                          sh_down=qm("sh_down", sh) if sh else None,
+                          correction_bias=bias, shared_gate_w=sgw)
+    torch.set_num_threads(1)
 
     budget = args.oracle_budget
     limit = args.oracle_tokens if args.oracle_tokens > 0 else 10**9
-    done = 0
-    t0 = time.perf_counter()
-    while done < limit:
-        O.moe_forward(layer, xb, rows=[done % n_pool])
-        done += 1
-        if time.perf_counter() - t0 >= budget:
-            break
-    el = time.perf_counter() - t0
-    print(json.dumps({"tokens": done, "seconds": el, "tokens_per_s": done / el}))
+
+    def work(wid: int, q):
+        done = 0
+        t0 = time.perf_counter()
+        while done < limit:
+            O.moe_forward(layer, xb, rows=[(wid + done) % n_pool])
+            done += 1
+            if time.perf_counter() - t0 >= budget:
+                break
+        q.put((done, time.perf_counter() - t0))
+
+    procs = max(1, args.oracle_procs)
+    if procs == 1:
+        import queue
+        q = queue.Queue()
+        work(0, q)
+        done, el = q.get()
+    else:
+        # This process never touches a GPU, so its workers may be forked.
+        import multiprocessing as mp
+        ctx = mp.get_context("fork")
+        q = ctx.Queue()
+        t0 = time.perf_counter()
+        ps = [ctx.Process(target=work, args=(i, q)) for i in range(procs)]
+        for p in ps:
+            p.start()
+        res = [q.get() for _ in ps]
+        for p in ps:
+            p.join()
+        el = time.perf_counter() - t0
+        done = sum(r[0] for r in res)
+    print(json.dumps({"tokens": done, "seconds": el, "tokens_per_s": done / el, "procs": procs}))
 
 
-def workload_config(args):
+def workload_config(args, name):
     """The workload's layer, with the --tokens / --experts overrides applied."""
     from mixture_experts_decode_router_gb300 import synth
-    cfg = synth.WORKLOADS[args.workload]
+    cfg = synth.WORKLOADS[name]
     if args.tokens > 0:
         cfg = cfg.with_(n_tokens=args.tokens, name=f"{cfg.name}@n{args.tokens}")
     if args.experts > 0:
@@ -276,42 +307,106 @@ def workload_config(args):
     return cfg
 
 
-def cpu_baseline(args, budget: float, tokens: int = 0):
+def _oracle_run(args, name, budget, procs, tokens=0):
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[v] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
-    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", args.workload,
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", name,
            "--oracle-budget", str(budget), "--oracle-tokens", str(tokens),
-           "--tokens", str(args.tokens), "--experts", str(args.experts)]
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=budget * 4 + 600)
+           "--oracle-procs", str(procs), "--tokens", str(args.tokens), "--experts", str(args.experts)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=budget * 4 + 900)
     if r.returncode != 0:
         raise RuntimeError(f"oracle child failed:\n{r.stderr[-2000:]}")
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": d["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{d['tokens']} token(s) of {args.workload}, one at a time, fp64 numpy "
-                      f"with 1 BLAS thread, {d['seconds']:.1f} s (expert generation excluded)"}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(args, name: str, budget: float):
+    """The oracle on one host core, and on every host core (one worker process
+    per core, os.cpu_count()), each for about ``budget`` seconds."""
+    ncpu = os.cpu_count() or 1
+    one = _oracle_run(args, name, budget, 1)
+    allc = _oracle_run(args, name, budget, ncpu) if ncpu > 1 else one
+    what = (f"of {name}, one token per oracle call, fp64 numpy, 1 BLAS thread per process "
+            f"(expert generation excluded)")
+    return {"value": one["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{one['tokens']} token(s) {what}, {one['seconds']:.1f} s",
+            "all_cores": {"value": allc["tokens_per_s"], "unit": "tokens/s", "cores": allc["procs"],
+                          "host_cpu_count": ncpu,
+                          "sample": f"{allc['tokens']} token(s) {what}, {allc['procs']} worker "
+                                    f"processes, {allc['seconds']:.1f} s"}}
 
 
 # ------------------------------------------------------------------ our arm
 
-def run_ours(args):
+def compute_dtype(fmt: str, grouped: bool) -> str:
+    """The arithmetic the path computes in: BF16 operands (tensor cores on the
+    grouped path, CUDA cores otherwise) with fp32 accumulation; FP8 / NVFP4
+    weights dequantised to f16 for the grouped path's f16 MMA, to fp32 in the
+    CUDA-core kernels."""
+    if fmt == "bf16":
+        return "bf16"
+    w = "fp8e4m3" if fmt == "fp8_b128" else "nvfp4"
+    return f"f16 ({w} weights dequantised, bf16 activations as f16, fp32 accumulate)" if grouped \
+        else f"fp32 ({w} weights dequantised, bf16 activations)"
+
+
+def e2e_line(world, n, H, steps, zero_copy_ms, copies_ms):
+    """The end-to-end figure: the faster of the two host-buffer modes, both reported.
+    Zero-copy wins at a few tokens (no copy launches); at many tokens the kernels'
+    re-reads of x across the host link cost more than one copy in."""
+    modes = {
+        "zero_copy": ("x and out in pinned host memory, read and written by the kernels", zero_copy_ms),
+        "with_copies": ("cudaMemcpyAsync H2D of x, the call on device buffers, D2H of out", copies_ms),
+    }
+    best = min(modes, key=lambda m: modes[m][1])
+    line = {"value": round(whole_job_tokens_per_s(world, n, steps, modes[best][1]), 2), "unit": "tokens/s",
+            "h2d_bytes_per_step": n * H * 2, "d2h_bytes_per_step": n * H * 2,
+            "us_per_call": round(modes[best][1] / steps * 1e3, 3), "mode": best}
+    for m, (what, ms) in modes.items():
+        line[m] = {"value": round(whole_job_tokens_per_s(world, n, steps, ms), 2), "unit": "tokens/s",
+                   "us_per_call": round(ms / steps * 1e3, 3), "what": what}
+    return line
+
+
+def stage_alg_bytes(cfg, n, distinct, touched, nm, has_bias):
+    """Algorithmic bytes per launch of each stage of the path that ran."""
+    from mixture_experts_decode_router_gb300 import synth
+    H, I, S, E, k = cfg.hidden, cfg.inter, cfg.shared_inter, cfg.num_experts, cfg.top_k
+    mb = synth.matrix_bytes
+    fmt = cfg.expert_fmt
+    nk = n * k
+    w_gu = distinct * 2 * mb(fmt, I, H) + (2 * mb(fmt, S, H) if S else 0)
+    w_dn = distinct * mb(fmt, H, I) + (mb(fmt, H, S) if S else 0)
+    return {
+        "fused": touched,
+        "router": E * H * 2 + n * H * 2 + n * E * 4,
+        # top-k (logits in, routes out) + grouping (routes in, counts/offsets/permutation out)
+        "topk_group": n * E * 4 + nk * 8 + (4 * E if has_bias else 0)
+        + nk * 4 + 4 * (3 * E + 1) + nk * 4,
+        # token-major: fp32 activations; grouped: 16-bit activations
+        "gate_up": w_gu + n * H * 2 + (4 if nm == 5 else 2) * (nk * I + n * S)
+        + (2 * (nk * H + n * H) if nm == 7 else 0),
+        "down_blend": w_dn + 4 * (nk * I + n * S) + n * H * 2 + nk * 8,
+        "gather": 2 * 2 * (nk * H + n * H),
+        "down": w_dn + 2 * (nk * I + n * S) + 4 * (nk * H + (n * H if S else 0)),
+        "combine": 4 * (nk * H + (n * H if S else 0)) + n * H * 2 + nk * 4,
+    }
+
+
+def measure_workload(args, name, dev, flush, world, local):
+    """Times one workload: K moe_forward calls (L2 flushed between them), the
+    per-stage split, the end-to-end legs with host buffers, and a device copy
+    of the same byte count.  Returns the workload's entry of the JSON line
+    (device times are this rank's; the caller takes the maximum over ranks)."""
     import numpy as np
     import torch
-    import torch.distributed as dist
 
     from mixture_experts_decode_router_gb300 import binding as B
     from mixture_experts_decode_router_gb300 import synth
     from mixture_experts_decode_router_gb300.layer import MoeLayer
 
-    world, rank, local = _dist()
-    if world > 1:
-        dist.init_process_group("nccl", init_method="env://")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    B.load()
-
-    cfg = workload_config(args)
+    cfg = workload_config(args, name)
     n = cfg.n_tokens
     lw = synth.make_weights(cfg, dev)
     x = synth.make_input(cfg, device=dev)
@@ -319,8 +414,6 @@ def run_ours(args):
     out = torch.empty(n, cfg.hidden, dtype=torch.bfloat16, device=dev)
     idx = torch.empty(n, cfg.top_k, dtype=torch.int32, device=dev)
     wts = torch.empty(n, cfg.top_k, dtype=torch.float32, device=dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(int(2.5 * l2) // 4 * 4, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
 
@@ -340,6 +433,7 @@ def run_ours(args):
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     clocks = ClockSampler(local)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
@@ -386,27 +480,7 @@ def run_ours(args):
     if dev_err:
         raise B.MoeError(f"device error word {dev_err}")
 
-    # Algorithmic bytes per launch of each stage.
-    H, I, S, E, k = cfg.hidden, cfg.inter, cfg.shared_inter, cfg.num_experts, cfg.top_k
-    mb = synth.matrix_bytes
-    fmt = cfg.expert_fmt
-    nk = n * k
-    w_gu = distinct * 2 * mb(fmt, I, H) + (2 * mb(fmt, S, H) if S else 0)
-    w_dn = distinct * mb(fmt, H, I) + (mb(fmt, H, S) if S else 0)
-    alg = {
-        "fused": touched,
-        "router": E * H * 2 + n * H * 2 + n * E * 4,
-        # top-k (logits in, routes out) + grouping (routes in, counts/offsets/permutation out)
-        "topk_group": n * E * 4 + nk * 8 + (4 * E if lw.correction_bias is not None else 0)
-        + nk * 4 + 4 * (3 * E + 1) + nk * 4,
-        # token-major: fp32 activations; grouped: 16-bit activations
-        "gate_up": w_gu + n * H * 2 + (4 if nm == 5 else 2) * (nk * I + n * S)
-        + (2 * (nk * H + n * H) if nm == 7 else 0),
-        "down_blend": w_dn + 4 * (nk * I + n * S) + n * H * 2 + nk * 8,
-        "gather": 2 * 2 * (nk * H + n * H),
-        "down": w_dn + 2 * (nk * I + n * S) + 4 * (nk * H + (n * H if S else 0)),
-        "combine": 4 * (nk * H + (n * H if S else 0)) + n * H * 2 + nk * 4,
-    }
+    alg = stage_alg_bytes(cfg, n, distinct, touched, nm, lw.correction_bias is not None)
     peak, peak_kind = _peaks()
     dom = stages_run[int(np.argmax(stage_ms))]
     dom_ms = float(stage_ms[stages_run.index(dom)])
@@ -449,103 +523,152 @@ def run_ours(args):
         raise B.MoeError("zero-copy output differs from the device-buffer output")
     e2e_copy_ms = timed_e2e(False)
 
-    cpu = None
+    # A device-to-device copy moving the call's touched bytes (half read, half
+    # written: the measured peak's own method), timed the same way: what one
+    # launch of plain streaming reaches at this size on this GPU.
+    half = max(16, touched // 2 // 16 * 16)
+    src = torch.ones(half, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        flush.zero_()
+        dst.copy_(src)
+    cs = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    ce = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    for i in range(Ke):
+        flush.zero_()
+        cs[i].record(stream)
+        dst.copy_(src)
+        ce[i].record(stream)
+    torch.cuda.synchronize()
+    copy_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(cs, ce)]))
+    del src, dst
+
+    ms_step = dev_ms / K
+    grouped = nm == 7
+    entry = {
+        "us_per_call": round(ms_step * 1e3, 3),
+        "us_per_call_p10_p50_p90": [round(float(np.percentile(per, q)) * 1e3, 3) for q in (10, 50, 90)],
+        "tokens_per_s": round(whole_job_tokens_per_s(world, n, K, dev_ms), 2),
+        "steps": K,
+        "touched_bytes": touched,
+        "distinct_experts": distinct,
+        "hbm_gbs": round(touched / (ms_step * 1e-3) / 1e9, 1),
+        "hbm_frac_of_measured": round(touched / (ms_step * 1e-3) / 1e9 / peak, 4),
+        "size_matched_copy": {
+            "us": round(copy_ms * 1e3, 3), "bytes": 2 * half,
+            "gbs": round(2 * half / (copy_ms * 1e-3) / 1e9, 1),
+            "frac_of_measured": round(2 * half / (copy_ms * 1e-3) / 1e9 / peak, 4),
+            "what": "torch copy_ of touched/2 bytes on the device (read + write = the call's touched "
+                    "bytes), L2 flushed, event-timed like the call"},
+        "call_time_over_copy_time": round(ms_step / copy_ms, 3),
+        "dtype": compute_dtype(cfg.expert_fmt, grouped),
+        "config": {"workload": cfg.name, "n_tokens": n, "hidden": cfg.hidden,
+                   "num_experts": cfg.num_experts, "top_k": cfg.top_k, "inter": cfg.inter,
+                   "shared_inter": cfg.shared_inter, "routing": cfg.routing,
+                   "expert_fmt": cfg.expert_fmt, "dup_frac": cfg.dup_frac, "path": args.path},
+        "wall_s_timed_loop": round(t1 - t0, 3),
+        "gpu_launches": K * len(stages_run),
+        "stages": stages,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": _traffic(dom, cfg.name),
+                     "tensor_pipe_active_pct": _tensor_pipe(dom, cfg.name),
+                     "alg_bytes_per_launch": int(alg[dom]),
+                     "avg_launch_us": round(dom_ms * 1e3, 3)},
+        "e2e": e2e_line(world, n, cfg.hidden, Ke, e2e_ms, e2e_copy_ms),
+        "clocks": clk,
+    }
+    del layer, lw, x, out
+    torch.cuda.empty_cache()
+    return entry
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from mixture_experts_decode_router_gb300 import binding as B
+
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.load()
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(int(2.5 * l2) // 4 * 4, dtype=torch.uint8, device=dev)
+    names = workload_names(args)
+    head = HEADLINE if HEADLINE in names else names[0]
+    entries = {nm: measure_workload(args, nm, dev, flush, world, local) for nm in names}
+
+    # The oracle on the host cores (rank 0 at N = 1 only), after every GPU
+    # measurement so the two never share the host.
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args, args.oracle_budget)
+        for nm in names:
+            entries[nm]["cpu_baseline"] = cpu_baseline(args, nm, args.oracle_budget)
 
     if rank == 0:
-        ms_step = dev_ms / K
-        tok_s = whole_job_tokens_per_s(world, n, K, dev_ms)
+        h = entries[head]
+        K = args.steps
         line = {
             "metric": METRIC,
-            "value": round(tok_s, 2),
+            "value": h["tokens_per_s"],
             "unit": "tokens/s",
             "n_gpus": world,
             "steps": K,
             "warmup": args.warmup,
-            "ms_per_step": round(ms_step, 6),
-            "us_per_call": round(ms_step * 1e3, 3),
-            "us_per_call_p10_p50_p90": [round(float(np.percentile(per, q)) * 1e3, 3)
-                                        for q in (10, 50, 90)],
-            "hbm_gbs": round(touched / (ms_step * 1e-3) / 1e9, 1),
-            "hbm_frac_of_measured": round(touched / (ms_step * 1e-3) / 1e9 / peak, 4),
-            "touched_bytes": touched,
+            "ms_per_step": round(h["us_per_call"] / 1e3, 6),
+            "us_per_call": h["us_per_call"],
+            "us_per_call_p10_p50_p90": h["us_per_call_p10_p50_p90"],
+            "hbm_gbs": h["hbm_gbs"],
+            "hbm_frac_of_measured": h["hbm_frac_of_measured"],
+            "touched_bytes": h["touched_bytes"],
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": compute_dtype(fmt, nm == 7),
+            "dtype": h["dtype"],
             "data": "synthetic (seeded; weights N(0,0.02), input N(0,1))",
-            "config": {"workload": cfg.name, "n_tokens": n, "hidden": H, "num_experts": E,
-                       "top_k": k, "inter": I, "shared_inter": S, "routing": cfg.routing,
-                       "expert_fmt": fmt, "path": args.path,
-                       "l2": "flushed between steps (2.5x L2 write), flush outside the events",
-                       "parallelism": f"replicas{world}" if world > 1 else "single"},
-            "wall_s_timed_loop": round(t1 - t0, 3),
-            "gpu_launches": K * len(stages_run),
-            "stages": stages,
-            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
-                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": _traffic(dom, cfg.name),
-                         "tensor_pipe_active_pct": _tensor_pipe(dom, cfg.name),
-                         "alg_bytes_per_launch": int(alg[dom]),
-                         "avg_launch_us": round(dom_ms * 1e3, 3)},
-            "e2e": e2e_line(world, n, H, Ke, e2e_ms, e2e_copy_ms),
-            "clocks": clk,
-            "cpu_baseline": cpu,
+            "config": dict(h["config"], l2="flushed between steps (2.5x L2 write), flush outside the events",
+                           parallelism=f"replicas{world}" if world > 1 else "single"),
+            "gpu_launches": h["gpu_launches"],
+            "roofline": h["roofline"],
+            "e2e": h["e2e"],
+            "clocks": h["clocks"],
+            "cpu_baseline": h.get("cpu_baseline"),
+            "size_matched_copy": h["size_matched_copy"],
+            "stages": h["stages"],
+            "workloads": entries,
         }
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
 
 
-def compute_dtype(fmt: str, grouped: bool) -> str:
-    """The arithmetic the path computes in: BF16 operands (tensor cores on the
-    grouped path, CUDA cores otherwise) with fp32 accumulation; FP8 / NVFP4
-    weights dequantised to f16 for the grouped path's f16 MMA, to fp32 in the
-    CUDA-core kernels."""
-    if fmt == "bf16":
-        return "bf16"
-    w = "fp8e4m3" if fmt == "fp8_b128" else "nvfp4"
-    return f"f16 ({w} weights dequantised, bf16 activations as f16, fp32 accumulate)" if grouped \
-        else f"fp32 ({w} weights dequantised, bf16 activations)"
-
-
-def e2e_line(world, n, H, steps, zero_copy_ms, copies_ms):
-    """The end-to-end figure: the faster of the two host-buffer modes, both reported.
-    Zero-copy wins at a few tokens (no copy launches); at many tokens the kernels'
-    re-reads of x across the host link cost more than one copy in."""
-    modes = {
-        "zero_copy": ("x and out in pinned host memory, read and written by the kernels", zero_copy_ms),
-        "with_copies": ("cudaMemcpyAsync H2D of x, the call on device buffers, D2H of out", copies_ms),
-    }
-    best = min(modes, key=lambda m: modes[m][1])
-    line = {"value": round(whole_job_tokens_per_s(world, n, steps, modes[best][1]), 2), "unit": "tokens/s",
-            "h2d_bytes_per_step": n * H * 2, "d2h_bytes_per_step": n * H * 2,
-            "us_per_call": round(modes[best][1] / steps * 1e3, 3), "mode": best}
-    for m, (what, ms) in modes.items():
-        line[m] = {"value": round(whole_job_tokens_per_s(world, n, steps, ms), 2), "unit": "tokens/s",
-                   "us_per_call": round(ms / steps * 1e3, 3), "what": what}
-    return line
-
-
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
+    """The fp64 oracle on the host cores (one worker process per core), on the
+    headline workload: each worker takes one token per oracle call until the
+    run has made max(1, steps) tokens per worker or about a minute has passed."""
     world, rank, _ = _dist()
     if rank != 0:
         return
-    cfg = workload_config(args)
-    # One step = one token through the oracle; the run is bounded to ~2 minutes.
-    budget = 120.0
-    cpu = cpu_baseline(args, budget, tokens=max(1, args.steps))
-    tok_s = cpu["value"]
+    name = HEADLINE if args.workload == "all" else args.workload
+    cfg = workload_config(args, name)
+    ncpu = os.cpu_count() or 1
+    d = _oracle_run(args, name, 60.0, ncpu, tokens=max(1, args.steps))
+    tok_s = d["tokens_per_s"]
     line = {
         "metric": METRIC, "impl": "reference", "value": round(tok_s, 4), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * cfg.n_tokens / tok_s, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg.name, "n_tokens": cfg.n_tokens},
-        "cpu_baseline": {"kind": "oracle", "cores": cpu["cores"], "sample": cpu["sample"],
+        "cpu_baseline": {"kind": "oracle", "cores": d["procs"], "host_cpu_count": ncpu,
+                         "sample": f"{d['tokens']} token(s) of {name}, one token per oracle call, "
+                                   f"fp64 numpy, {d['procs']} worker processes with 1 BLAS thread "
+                                   f"each, {d['seconds']:.1f} s",
                          "value": round(tok_s, 4), "unit": "tokens/s"},
         "e2e": {"value": round(tok_s, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

@@ -264,14 +264,33 @@ moe_status_t moe_forward_timed(const moe_config_t* cfg, const moe_weights_t* wts
  *   A call that would need more than MOE_STATIC_WORKSPACE_BYTES of workspace
  *   (moe_workspace_bytes(cfg, n)) returns MOE_ERR_WORKSPACE and launches nothing.
  *   The first call on each device looks up the array's device address and
- *   clears its control block, synchronously; make that first call before any
- *   stream capture.
+ *   clears its control block on `stream`, then synchronises `stream`; make
+ *   that first call before any stream capture (a first call on a stream that
+ *   is being captured returns MOE_ERR_UNSUPPORTED and launches nothing).
  *   Every call shares the one array: calls whose work overlaps on the GPU
  *   (other streams, other host threads) race on it and must be serialised by
- *   the caller. */
+ *   the caller.
+ *   Device-side failures (a bounded wait that gave up; a control block left
+ *   dirty by such a call, which makes every later one-token call refuse and
+ *   leave `out` unwritten) are recorded in the array's control block and are
+ *   not returned by this call: read and clear them with
+ *   moe_static_workspace_check(). */
 moe_status_t moe_forward_static_ws(const moe_config_t* cfg, const moe_weights_t* wts,
                                    const void* x, int32_t n, void* out,
                                    int32_t* idx, float* w, moe_stream_t stream);
+
+/* moe_workspace_check for the static workspace of moe_forward_static_ws on the
+ * current device (no counterpart in the pages: an addition of this library).
+ * Reads, then clears, the array's device error word and resets its
+ * single-token barrier word, so the next static call runs; synchronises
+ * `stream`.
+ *   device_error (out)  as moe_workspace_check: 0, 11-17, 1-5 or 20.
+ *   workspace    (out, optional) the array's device address on this device
+ *                (NULL = not returned); the library owns it.
+ * The first use on a device runs the set-up of moe_forward_static_ws.
+ * Errors: MOE_ERR_NULL (device_error NULL), MOE_ERR_UNSUPPORTED (`stream` is
+ * being captured into a graph), MOE_ERR_CUDA. */
+moe_status_t moe_static_workspace_check(int32_t* device_error, void** workspace, moe_stream_t stream);
 
 /* Reads, then clears, the device error word of a workspace, and resets the
  * single-token kernel's barrier word (which a call that ended early leaves

@@ -37,8 +37,8 @@ MOE_PATH_GROUPED = 2
 
 # Every function include/moe.h declares.
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_experts", "moe_forward",
-            "moe_forward_timed", "moe_forward_static_ws", "moe_workspace_check", "moe_status_string",
-            "moe_abi_version")
+            "moe_forward_timed", "moe_forward_static_ws", "moe_static_workspace_check",
+            "moe_workspace_check", "moe_status_string", "moe_abi_version")
 
 MOE_STATIC_WORKSPACE_BYTES = 16 << 20
 
@@ -100,6 +100,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.moe_forward_timed.restype = ctypes.c_int
     lib.moe_forward_static_ws.argtypes = [cfgp, wp, P, I32, P, P, P, P]
     lib.moe_forward_static_ws.restype = ctypes.c_int
+    lib.moe_static_workspace_check.argtypes = [ctypes.POINTER(I32), ctypes.POINTER(P), P]
+    lib.moe_static_workspace_check.restype = ctypes.c_int
     lib.moe_workspace_check.argtypes = [P, S, ctypes.POINTER(I32), P]
     lib.moe_workspace_check.restype = ctypes.c_int
     lib.moe_status_string.argtypes = [ctypes.c_int]
@@ -169,6 +171,16 @@ def moe_forward_static_ws(cfg, wts, x, n, out, idx, w, stream=None) -> int:
     """moe_forward with the library's static device workspace (no ws argument)."""
     return load().moe_forward_static_ws(_ref(cfg), _ref(wts), _ptr(x), int(n), _ptr(out), _ptr(idx),
                                         _ptr(w), _stream(stream))
+
+
+def moe_static_workspace_check(stream=None):
+    """(status, device error word, static workspace device address) of
+    moe_forward_static_ws on the current device; reads and clears the word,
+    syncing the stream."""
+    v = ctypes.c_int32(0)
+    addr = ctypes.c_void_p(None)
+    s = load().moe_static_workspace_check(ctypes.byref(v), ctypes.byref(addr), _stream(stream))
+    return s, v.value, addr.value
 
 
 def moe_workspace_check(ws, ws_bytes, stream=None):

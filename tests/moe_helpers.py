@@ -3,6 +3,9 @@ near-tie margin as the generator's ``gap_fn``."""
 
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -75,3 +78,32 @@ def tolerance(fmt: str) -> float:
     """max|err| bound as a fraction of RMS(oracle): 2e-2 for BF16 and FP8
     experts, 5e-2 for NVFP4."""
     return 5e-2 if fmt == O.FMT_NVFP4 else 2e-2
+
+
+def oracle_forward_threaded(layer: O.OracleLayer, x_bits: np.ndarray, rows=None, threads=None):
+    """``O.moe_forward`` of ``rows`` computed as the sum of expert-parallel
+    partials over contiguous expert ranges (each holding about the same number
+    of the touched experts) plus the shared-expert-only call, the parts run in
+    threads (numpy releases the GIL in its array loops).  The oracle itself is
+    unchanged: a sum of its own partials, which the oracle pins show equal to
+    the whole layer.  Returns (out, idx, w) like ``O.moe_forward``."""
+    x = O.bf16_decode(x_bits)
+    rows = np.arange(x.shape[0]) if rows is None else np.asarray(rows)
+    lg = O.router_logits(x[rows], O.router_weights(layer))
+    idx, w = O.route(lg, layer.routing, layer.top_k, layer.norm_topk_prob,
+                     layer.routed_scaling_factor, layer.correction_bias)
+    touched = np.unique(idx)
+    threads = threads or max(1, min(8, os.cpu_count() or 1))
+    chunks = [c for c in np.array_split(touched, threads) if len(c)]
+    ranges = [(int(c[0]), int(c[-1]) + 1) for c in chunks]
+
+    def part(r):
+        return O.moe_forward(layer, x_bits, rows=rows, experts=r, include_shared=False)[0]
+
+    def shared():
+        return O.moe_forward(layer, x_bits, rows=rows, experts=(0, 0), include_shared=True)[0]
+
+    with ThreadPoolExecutor(max_workers=len(ranges) + 1) as ex:
+        futs = [ex.submit(part, r) for r in ranges] + [ex.submit(shared)]
+        out = sum(f.result() for f in futs)
+    return out, idx, w

@@ -23,7 +23,8 @@ from mixture_experts_decode_router_gb300 import binding as B
 from mixture_experts_decode_router_gb300 import synth
 from mixture_experts_decode_router_gb300.layer import MoeLayer
 from oracle import moe_oracle as O
-from tests.moe_helpers import bf16_bits, gap_fn_for, oracle_layer, tolerance
+from tests.moe_helpers import (bf16_bits, gap_fn_for, oracle_forward_threaded, oracle_layer,
+                               tolerance)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +47,7 @@ def small(name, **kw):
     return synth.LayerConfig(name, **d)
 
 
-def _check(cfg, n=None, path="auto", rows=None, x=None, lw=None):
+def _check(cfg, n=None, path="auto", rows=None, x=None, lw=None, threaded=False):
     n = cfg.n_tokens if n is None else n
     lw = synth.make_weights(cfg, "cuda") if lw is None else lw
     L = oracle_layer(lw)
@@ -63,7 +64,10 @@ def _check(cfg, n=None, path="auto", rows=None, x=None, lw=None):
     assert np.array_equal(idx.cpu().numpy(), idx_ref), "expert indices differ"
     assert np.max(np.abs(w.cpu().numpy() - w_ref)) <= 1e-5 * max(1.0, cfg.routed_scaling_factor)
     rows = np.arange(n) if rows is None else np.asarray(rows)
-    ref, _, _, _ = O.moe_forward(L, xb, rows=rows)
+    if threaded:    # the full-size layers: the oracle's expert partials in threads
+        ref, _, _ = oracle_forward_threaded(L, xb, rows=rows)
+    else:
+        ref, _, _, _ = O.moe_forward(L, xb, rows=rows)
     got = out.float().cpu().numpy()[rows]
     rms = float(np.sqrt(np.mean(ref ** 2)))
     err = float(np.max(np.abs(got - ref)))
@@ -467,26 +471,17 @@ def test_expert_parallel_full_size():
 
 # ---------------------------------------------------------------- the five workloads at full size
 
-@pytest.mark.parametrize("name,rows", [
-    ("tiny_n1", None),
-    ("decode_n1", None),
-    ("decode_n16", None),
-    ("fp8_n64", [0, 9, 31, 32, 50, 63]),
-    ("nvfp4_n256", list(range(0, 256, 8)) + [255]),
-])
-def test_workloads_full_size(name, rows):
-    cfg = synth.WORKLOADS[name]
-    _check(cfg, rows=rows)
+@pytest.mark.parametrize("name", ["tiny_n1", "decode_n1", "decode_n16", "fp8_n64", "nvfp4_n256"])
+def test_workloads_full_size(name):
+    """Every output row of every workload, element by element (each touched
+    expert decoded once for the whole batch)."""
+    _check(synth.WORKLOADS[name], threaded=True)
 
 
-@pytest.mark.parametrize("name,rows", [
-    ("decode_n1", None),
-    ("decode_n16", None),
-    ("nvfp4_n256", list(range(3, 256, 16)) + [254]),
-])
-def test_nvfp4_router_full_size(name, rows):
-    """The NVFP4 router on the full-size layers (one token: token-major)."""
-    _check(synth.WORKLOADS[name].with_(router_fmt=synth.FMT_NVFP4), rows=rows)
+@pytest.mark.parametrize("name", ["decode_n1", "decode_n16", "nvfp4_n256"])
+def test_nvfp4_router_full_size(name):
+    """The NVFP4 router on the full-size layers (one token: token-major), every row."""
+    _check(synth.WORKLOADS[name].with_(router_fmt=synth.FMT_NVFP4), threaded=True)
 
 
 # ---------------------------------------------------------------- device error word
