@@ -76,10 +76,12 @@ struct TcCfg {
     static constexpr int kTmemCols = kDeq ? 512 : kAccBufs * kAccCols;
     static constexpr int kAStages = kDeq ? (512 - kAColBase) / kACols : (GU ? 5 : 8);
     static constexpr int kASmemStages = kDeq ? 0 : kAStages;
-    // Dequantised tiles hand operand stages to the MMA warp in groups of three
-    // (one barrier round trip per 192 K instead of per 64; measured faster
-    // than groups of one or two).
-    static constexpr int kGrp = kDeq ? 3 : 1;
+    // Dequantised tiles hand operand stages to the MMA warp in groups: three
+    // for gate/up (one barrier round trip per 192 K instead of per 64;
+    // measured faster than groups of one or two), four for down, whose twelve
+    // operand stages make three groups (measured 1-1.5% faster than three;
+    // six was slower).
+    static constexpr int kGrp = kDeq ? (GU ? 3 : 4) : 1;
     static constexpr int kAGroups = kAStages / kGrp;
     // Dequantised tiles: the token (B) tiles have a ring of their own, so they
     // are fetched ahead instead of after the MMA frees an A slot.
