@@ -567,7 +567,7 @@ def measure_workload(args, name, dev, flush, world, local):
                    "shared_inter": cfg.shared_inter, "routing": cfg.routing,
                    "expert_fmt": cfg.expert_fmt, "dup_frac": cfg.dup_frac, "path": args.path},
         "wall_s_timed_loop": round(t1 - t0, 3),
-        "gpu_launches": K * len(stages_run),
+        "gpu_launches": K * len(stages_run),   # this library's kernels: one per stage
         "stages": stages,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
