@@ -27,7 +27,8 @@
 // scale), one rounding with an 11-bit significand; NVFP4: e2m1 * e4m3 scale,
 // exact in f16, with the fp32 scale2 applied to the accumulator).  Those tiles
 // run the f16 MMA with f16 activations (exact for BF16 inputs in f16's normal
-// range, saturated at +-65504).  Warp roles: 0 TMA producer of the weight
+// range, saturated at +-65504).  A pipeline stage covers 64 K (128 K in the
+// NVFP4 down kernel: 64-byte raw rows, like FP8's).  Warp roles: 0 TMA producer of the weight
 // codes (and FP8/NVFP4 block scales), 1 MMA issuer (one thread) and TMEM
 // owner, 2-5 epilogue (TMEM -> registers -> global), then the dequant warps,
 // then (dequantised formats) the TMA producer of the token tiles.
@@ -44,7 +45,7 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;   // weight rows per tile (MMA M)
-constexpr int BK = 64;    // K elements per pipeline stage
+constexpr int BK = 64;    // K elements of one 128-byte-swizzled token-tile box (and a BF16 / FP8 stage)
 constexpr int NT = kTcTokensPerTile;   // tokens per tile (max MMA N)
 
 template <int FMT, bool GU>
@@ -52,10 +53,18 @@ struct TcCfg {
     static constexpr bool kDeq = FMT != MOE_W_BF16;
     static constexpr bool kF16 = FMT != MOE_W_BF16;   // FP8 and NVFP4 tiles: f16 operands
     static constexpr int kMats = GU ? 2 : 1;
-    static constexpr int kAMat = BM * BK * 2;
+    // K elements per pipeline stage: 64, or 128 for the NVFP4 down kernel,
+    // whose 64-K stages carry only 4 KB of codes for the same handshakes as
+    // gate/up's 8 KB (measured: down 103.7 -> 78.8 us at nvfp4_n256; gate/up
+    // at 128 K, three TMEM operand stages, was slower: 128.2 -> 136.2 us).
+    static constexpr int kBK = (FMT == MOE_W_NVFP4 && !GU) ? 128 : BK;
+    static constexpr int kAMat = BM * kBK * 2;
     static constexpr int kAStage = kMats * kAMat;
-    static constexpr int kBStage = NT * BK * 2;
-    static constexpr int kRawRow = FMT == MOE_W_FP8_B128 ? BK : (FMT == MOE_W_NVFP4 ? BK / 2 : 0);
+    // Token tiles: kBK / BK boxes of BK columns (one 128-byte swizzle atom each),
+    // kBAtom bytes apart.
+    static constexpr int kBAtom = NT * BK * 2;
+    static constexpr int kBStage = (kBK / BK) * kBAtom;
+    static constexpr int kRawRow = FMT == MOE_W_FP8_B128 ? kBK : (FMT == MOE_W_NVFP4 ? kBK / 2 : 0);
     static constexpr int kRawMat = BM * kRawRow;
     static constexpr int kRawStage = kMats * kRawMat;
     // BF16 tiles: operand stages in shared memory (TMA, 128-byte swizzle).
@@ -67,11 +76,11 @@ struct TcCfg {
     // gate/up, so that the operand ring gets the columns -- its thin tiles
     // still alternate between the accumulator's halves, see AccSlots), then
     // (dequantised tiles) the operand
-    // stages, kMats x BK/2 columns each (two f16 per 32-bit column, row i of
+    // stages, kMats x kBK/2 columns each (two f16 per 32-bit column, row i of
     // the tile in lane i).
     static constexpr int kAccBufs = (kDeq && GU) ? 1 : 2;
     static constexpr int kAccCols = kMats * NT;
-    static constexpr int kACols = kMats * BK / 2;
+    static constexpr int kACols = kMats * kBK / 2;
     static constexpr int kAColBase = kAccBufs * kAccCols;
     static constexpr int kTmemCols = kDeq ? 512 : kAccBufs * kAccCols;
     static constexpr int kAStages = kDeq ? (512 - kAColBase) / kACols : (GU ? 5 : 8);
@@ -81,17 +90,20 @@ struct TcCfg {
     // measured faster than groups of one or two), four for down, whose twelve
     // operand stages make three groups (measured 1-1.5% faster than three;
     // six was slower).
-    static constexpr int kGrp = kDeq ? (GU ? 3 : 4) : 1;
+    // NVFP4 down (128-K stages): its six operand stages in pairs.
+    static constexpr int kGrp = (FMT == MOE_W_NVFP4 && !GU) ? 2 : (kDeq ? (GU ? 3 : 4) : 1);
     static constexpr int kAGroups = kAStages / kGrp;
     // Dequantised tiles: the token (B) tiles have a ring of their own, so they
     // are fetched ahead instead of after the MMA frees an A slot.
     static constexpr int kBStages = kDeq ? (GU ? 4 : 6) : kAStages;
-    static constexpr int kRawStages = !kDeq ? 0 : (GU ? (FMT == MOE_W_FP8_B128 ? 10 : 16) : (FMT == MOE_W_FP8_B128 ? 16 : 24));
+    // Raw stages: FP8 10 / 16, NVFP4 16 (gate/up, 64 K) and 12 (down, 128 K: the
+    // bytes of 24 stages of 64 K).
+    static constexpr int kRawStages = !kDeq ? 0 : (GU ? (FMT == MOE_W_FP8_B128 ? 10 : 16) : (FMT == MOE_W_FP8_B128 ? 16 : 12));
     static constexpr int kDeqWarps = kDeq ? (FMT == MOE_W_NVFP4 ? 16 : 8) : 0;
     // Dequant work split: warp 6 + dw serves TMEM lane quarter (6 + dw) & 3 (the
-    // quarter a warp may access) and part dw >> 2 of each row's kMats x BK codes.
+    // quarter a warp may access) and part dw >> 2 of each row's kMats x kBK codes.
     static constexpr int kParts = kDeqWarps / 4;
-    static constexpr int kPartElems = kDeq ? kMats * BK / kParts : 0;
+    static constexpr int kPartElems = kDeq ? kMats * kBK / kParts : 0;
     // Dequantised tiles: a second producer warp for the token (B) tiles, after
     // the dequant warps, so a full B ring never holds up the weight copies.
     static constexpr int kBWarp = 6 + kDeqWarps;
@@ -100,8 +112,9 @@ struct TcCfg {
     static constexpr int kOffB = kOffA + kASmemStages * kAStage;
     static constexpr int kOffRaw = kOffB + kBStages * kBStage;
     // Block scales of each raw stage, fetched by the producer warp with the
-    // raw codes: FP8 one fp32 per matrix; NVFP4 4 E4M3 bytes per row per matrix.
-    static constexpr int kScaleStage = FMT == MOE_W_FP8_B128 ? 16 : (FMT == MOE_W_NVFP4 ? kMats * BM * 4 : 0);
+    // raw codes: FP8 one fp32 per matrix; NVFP4 kBK / 16 E4M3 bytes per row per matrix.
+    static constexpr int kScaleRow = FMT == MOE_W_NVFP4 ? kBK / 16 : 0;
+    static constexpr int kScaleStage = FMT == MOE_W_FP8_B128 ? 16 : (FMT == MOE_W_NVFP4 ? kMats * BM * kScaleRow : 0);
     static constexpr int kOffScale = kOffRaw + kRawStages * kRawStage;
     static constexpr int kOffBar = kOffScale + kRawStages * kScaleStage;
     // a_full, a_empty per A stage; b_full, b_empty per B stage; raw_full,
@@ -114,8 +127,9 @@ struct TcCfg {
     static_assert(!kDeq || kAColBase + kAStages * kACols <= kTmemCols, "TMEM operand stages");
     static_assert(kAStages % kGrp == 0, "operand stages come in whole groups");
     static_assert(kOffRaw % 1024 == 0 && kRawMat % 1024 == 0, "swizzled raw stages sit on 1024-byte boundaries");
-    static_assert(!kDeq || (kPartElems % 16 == 0 && BK % (kDeq ? kPartElems : 1) == 0),
+    static_assert(!kDeq || (kPartElems % 16 == 0 && kBK % (kDeq ? kPartElems : 1) == 0),
                   "a dequant part is whole 16-code blocks of one matrix");
+    static_assert(kBK % BK == 0 && kBStage % 1024 == 0, "token-tile boxes on swizzle-atom boundaries");
 };
 
 // Accumulator slots of the tiles, chosen alike by the MMA warp and the
@@ -237,14 +251,15 @@ __device__ __forceinline__ float2 f16x2_to_float2(uint32_t h2) {
     return __half22float2(__half2(raw));
 }
 
-// Byte offset of 16-byte chunk c of row r in a raw stage.  The TMA writes the
-// raw codes swizzled, the row's chunk index XORed with address bits 7 and up
-// (FP8, 64-byte rows, 64-byte swizzle: c ^ ((r >> 1) & 3); NVFP4, 32-byte
-// rows, 32-byte swizzle: c ^ ((r >> 2) & 1)), so that 32 lanes reading one
-// chunk of 32 consecutive rows spread over all banks.
-template <int FMT>
+// Byte offset of 16-byte chunk c of row r in a raw stage of kRawRow-byte rows.
+// The TMA writes the raw codes swizzled, the row's chunk index XORed with
+// address bits 7 and up (64-byte rows -- FP8's 64 codes, the NVFP4 down
+// kernel's 128 -- with the 64-byte swizzle: c ^ ((r >> 1) & 3); NVFP4 gate/up's
+// 32-byte rows with the 32-byte swizzle: c ^ ((r >> 2) & 1)), so that 32 lanes
+// reading one chunk of 32 consecutive rows spread over all banks.
+template <int kRawRow>
 __device__ __forceinline__ int raw_chunk(int r, int c) {
-    if constexpr (FMT == MOE_W_FP8_B128) return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+    if constexpr (kRawRow == 64) return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
     else return r * 32 + ((c ^ ((r >> 2) & 1)) << 4);
 }
 
@@ -319,10 +334,10 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             const int wrow = sh ? t.m0 : t.le * t.out + t.m0;
             const int nbox = (t.ntok + 15) >> 4;
             const CUtensorMap* bmap = sh ? &maps.bs : &maps.b;
-            const int KB = (t.K + BK - 1) / BK;
-            const bool nv_smem_scales = (FMT == MOE_W_NVFP4) && (t.K % 64 == 0);
+            const int KB = (t.K + C::kBK - 1) / C::kBK;
+            const bool nv_smem_scales = (FMT == MOE_W_NVFP4) && (t.K % C::kBK == 0);
             for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int k0 = kb * BK;
+                const int k0 = kb * C::kBK;
                 if constexpr (C::kDeq) {
                     const int rs = it % C::kRawStages;
                     if (!ptx::mbar_wait_warp(&raw_empty[rs], ((it / C::kRawStages) & 1) ^ 1, s_abort, err, 1)) {
@@ -345,16 +360,20 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                                            sp + (size_t)t.le * ob * ib + (t.m0 >> 7) * ib + (k0 >> 7));
                         }
                     } else if (nv_smem_scales) {
-                        // Row r's 4 scale bytes of this stage: columns [k0, k0 + 64).
+                        // Row r's kScaleRow scale bytes of this stage: columns [k0, k0 + kBK),
+                        // four bytes per copy (the scale arrays are 4-byte aligned).
                         for (int m = 0; m < C::kMats; ++m) {
                             const uint8_t* sp = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[m] : p.scale[m]);
 #pragma unroll
                             for (int q = 0; q < BM / 32; ++q) {
                                 const int r = lane + 32 * q, mrow = t.m0 + r;
-                                const uint8_t* src = (mrow < t.out)
-                                    ? sp + ((size_t)t.le * t.out + mrow) * (t.K / 16) + k0 / 16
-                                    : reinterpret_cast<const uint8_t*>(p.zero4);
-                                ptx::cp_async4(ssc + (m * BM + r) * 4, src);
+#pragma unroll
+                                for (int h = 0; h < C::kScaleRow / 4; ++h) {
+                                    const uint8_t* src = (mrow < t.out)
+                                        ? sp + ((size_t)t.le * t.out + mrow) * (t.K / 16) + k0 / 16 + 4 * h
+                                        : reinterpret_cast<const uint8_t*>(p.zero4);
+                                    ptx::cp_async4(ssc + (m * BM + r) * C::kScaleRow + 4 * h, src);
+                                }
                             }
                         }
                     }
@@ -366,13 +385,14 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                         break;
                     }
                     if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(&a_full[as], C::kAStage + nbox * 2048);
+                        ptx::mbar_arrive_expect_tx(&a_full[as], C::kAStage + nbox * 2048 * (C::kBK / BK));
                         for (int m = 0; m < C::kMats; ++m)
                             ptx::tma_load_2d(sA + as * C::kAStage + m * C::kAMat,
                                              sh ? &maps.ws[m] : &maps.w[m], k0, wrow, &a_full[as]);
-                        for (int j = 0; j < nbox; ++j)
-                            ptx::tma_load_2d(sB + as * C::kBStage + j * 2048, bmap, k0, t.pos0 + 16 * j,
-                                             &a_full[as]);
+                        for (int a = 0; a < C::kBK / BK; ++a)
+                            for (int j = 0; j < nbox; ++j)
+                                ptx::tma_load_2d(sB + as * C::kBStage + a * C::kBAtom + j * 2048, bmap, k0 + a * BK,
+                                                 t.pos0 + 16 * j, &a_full[as]);
                     }
                 }
             }
@@ -397,17 +417,18 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                 const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
                 const int nbox = (t.ntok + 15) >> 4;
                 const CUtensorMap* bmap = t.e < 0 ? &maps.bs : &maps.b;
-                const int KB = (t.K + BK - 1) / BK;
+                const int KB = (t.K + C::kBK - 1) / C::kBK;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int bs = it % C::kBStages;
                     if (!ptx::mbar_wait(&b_empty[bs], ((it / C::kBStages) & 1) ^ 1, s_abort, err, 5)) {
                         stop = true;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(&b_full[bs], nbox * 2048);
-                    for (int j = 0; j < nbox; ++j)
-                        ptx::tma_load_2d(sB + bs * C::kBStage + j * 2048, bmap, kb * BK, t.pos0 + 16 * j,
-                                         &b_full[bs]);
+                    ptx::mbar_arrive_expect_tx(&b_full[bs], nbox * 2048 * (C::kBK / BK));
+                    for (int a = 0; a < C::kBK / BK; ++a)
+                        for (int j = 0; j < nbox; ++j)
+                            ptx::tma_load_2d(sB + bs * C::kBStage + a * C::kBAtom + j * 2048, bmap,
+                                             kb * C::kBK + a * BK, t.pos0 + 16 * j, &b_full[bs]);
                 }
             }
             if (*s_abort) {
@@ -437,7 +458,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             ptx::tc_fence_after();
             const uint32_t idesc = ptx::idesc_f16(BM, nmma, !C::kF16);
             const uint32_t d0 = tmem + acol;
-            const int KB = (t.K + BK - 1) / BK;
+            const int KB = (t.K + C::kBK - 1) / C::kBK;
             bool ok = true;
             for (int kb = 0; kb < KB && ok; ++git) {
                 // One group of operand stages: one a_full wait, one a_empty commit.
@@ -454,7 +475,8 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                         }
                     ptx::tc_fence_after();
                     // Descriptors of the stage's first K step; a later step (or the
-                    // second matrix) only moves the start address field (16-byte units).
+                    // second matrix) only moves the start address field (16-byte units):
+                    // K step kk of the token tile is 32 bytes into swizzle atom kk / 4.
                     const uint64_t b_desc = ptx::sw128_desc(ptx::smem_u32(sB + bs * C::kBStage));
                     if constexpr (C::kDeq) {
                         // A in tensor memory: K step kk of matrix m is 8 columns on.
@@ -463,10 +485,10 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     #pragma unroll
                             for (int m = 0; m < C::kMats; ++m)
     #pragma unroll
-                                for (int kk = 0; kk < BK / 16; ++kk)
-                                    ptx::mma_f16_ts(d0 + m * NT, a_t + m * (BK / 2) + kk * 8,
-                                                    b_desc + (uint64_t)((kk * 32) >> 4), idesc,
-                                                    (kb > 0 || kk > 0) ? 1u : 0u);
+                                for (int kk = 0; kk < C::kBK / 16; ++kk)
+                                    ptx::mma_f16_ts(d0 + m * NT, a_t + m * (C::kBK / 2) + kk * 8,
+                                                    b_desc + (uint64_t)(((kk >> 2) * C::kBAtom + (kk & 3) * 32) >> 4),
+                                                    idesc, (kb > 0 || kk > 0) ? 1u : 0u);
                             ptx::mma_commit(&b_empty[bs]);
                         }
                     } else {
@@ -475,7 +497,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     #pragma unroll
                             for (int m = 0; m < C::kMats; ++m)
     #pragma unroll
-                                for (int kk = 0; kk < BK / 16; ++kk)
+                                for (int kk = 0; kk < C::kBK / 16; ++kk)   // BF16: kBK == BK, one atom
                                     ptx::mma_f16(d0 + m * NT, a_desc + (uint64_t)((m * C::kAMat + kk * 32) >> 4),
                                                  b_desc + (uint64_t)((kk * 32) >> 4), idesc,
                                                  (kb > 0 || kk > 0) ? 1u : 0u);
@@ -601,13 +623,13 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         constexpr int PE = C::kPartElems, NC = PE / 2;
         const int qd = warp & 3, part = (warp - 6) >> 2;
         const int r = 32 * qd + lane;
-        const int pm = (part * PE) / BK, pk0 = (part * PE) % BK;
-        const uint32_t t_row = tmem + ((uint32_t)(32 * qd) << 16) + C::kAColBase + pm * (BK / 2) + pk0 / 2;
+        const int pm = (part * PE) / C::kBK, pk0 = (part * PE) % C::kBK;
+        const uint32_t t_row = tmem + ((uint32_t)(32 * qd) << 16) + C::kAColBase + pm * (C::kBK / 2) + pk0 / 2;
         uint32_t it = 0, git = 0;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
             const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
             const bool sh = t.e < 0;
-            const int KB = (t.K + BK - 1) / BK;
+            const int KB = (t.K + C::kBK - 1) / C::kBK;
             const int mrow = t.m0 + r;
             bool ok = true;
             for (int kb = 0; kb < KB && ok; ++git) {
@@ -619,7 +641,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                 for (int u = 0; u < n; ++u, ++kb, ++it) {
                     const int rs = it % C::kRawStages, as = g * C::kGrp + u;
                     if (!ptx::mbar_wait_warp(&raw_full[rs], (it / C::kRawStages) & 1, s_abort, err, 4)) { ok = false; break; }
-                    const int k0 = kb * BK;
+                    const int k0 = kb * C::kBK;
                     const uint8_t* raw = sRaw + rs * C::kRawStage + pm * C::kRawMat;
                     uint32_t o[NC];
                     if constexpr (FMT == MOE_W_FP8_B128) {
@@ -633,7 +655,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                         const uint32_t s2u = *reinterpret_cast<const uint32_t*>(&s2);
     #pragma unroll
                         for (int c = 0; c < PE / 16; ++c) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(raw + raw_chunk<FMT>(r, pk0 / 16 + c));
+                            const uint4 v = *reinterpret_cast<const uint4*>(raw + raw_chunk<C::kRawRow>(r, pk0 / 16 + c));
                             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
                             if (f16_scale) {
     #pragma unroll
@@ -658,13 +680,14 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     #pragma unroll
                         for (int b = 0; b < PE / 16; ++b) {
                             const int qb = pk0 / 16 + b;   // scale block of the stage
-                            const uint2 v = *reinterpret_cast<const uint2*>(raw + raw_chunk<FMT>(r, qb >> 1) + 8 * (qb & 1));
+                            const uint2 v = *reinterpret_cast<const uint2*>(raw + raw_chunk<C::kRawRow>(r, qb >> 1) + 8 * (qb & 1));
                             const int kc = k0 + 16 * qb;
                             uint32_t sc = 0;   // f16x2 of the block scale (0 outside the matrix)
-                            if (t.K % 64 == 0) {
+                            if (t.K % C::kBK == 0) {
                                 // Fetched into shared memory with the codes (0 past the last row).
-                                const uint32_t w = reinterpret_cast<const uint32_t*>(sScale + rs * C::kScaleStage)[pm * BM + r];
-                                const uint32_t bb = (w >> (8 * qb)) & 0xffu;
+                                const uint32_t w = reinterpret_cast<const uint32_t*>(
+                                    sScale + rs * C::kScaleStage + (pm * BM + r) * C::kScaleRow)[qb >> 2];
+                                const uint32_t bb = (w >> (8 * (qb & 3))) & 0xffu;
                                 sc = e4m3x2_to_f16x2(bb | (bb << 8));
                             } else if (mrow < t.out && kc < t.K) {
                                 const uint8_t* sp = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[pm] : p.scale[pm]) +
@@ -744,17 +767,21 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
 }
 
 // Weight map: BF16 (128-byte swizzle, the MMA operand layout) or raw codes
-// (FP8: 64-byte rows, 64-byte swizzle; NVFP4: 32-byte rows, 32-byte swizzle;
-// the layout raw_chunk reads).
-bool weight_map(CUtensorMap* m, int fmt, const void* w, int rows_total, int in_dim) {
+// (FP8: 64-byte rows, 64-byte swizzle; NVFP4: 32-byte rows and the 32-byte
+// swizzle for gate/up, 64-byte rows and the 64-byte swizzle for down; the
+// layout raw_chunk reads).
+bool weight_map(CUtensorMap* m, int fmt, const void* w, int rows_total, int in_dim, bool gate_up) {
     if (fmt == MOE_W_BF16)
         return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, in_dim, rows_total, BK, BM,
                         CU_TENSOR_MAP_SWIZZLE_128B);
     if (fmt == MOE_W_FP8_B128)
         return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim, rows_total, BK, BM,
                         CU_TENSOR_MAP_SWIZZLE_64B);
-    return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim / 2, rows_total, BK / 2, BM,
-                    CU_TENSOR_MAP_SWIZZLE_32B);
+    if (gate_up)
+        return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim / 2, rows_total,
+                        TcCfg<MOE_W_NVFP4, true>::kBK / 2, BM, CU_TENSOR_MAP_SWIZZLE_32B);
+    return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim / 2, rows_total,
+                    TcCfg<MOE_W_NVFP4, false>::kBK / 2, BM, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 bool act_map(CUtensorMap* m, int fmt, const void* a, int rows, int cols) {
@@ -795,15 +822,15 @@ bool build_tc_maps(int fmt, bool gate_up, const moe_weights_t* w, int E, int H, 
     if (E == 0 && S == 0) return false;
     if (gate_up) {
         if (E > 0) {
-            ok &= weight_map(&maps->w[0], fmt, w->gate.w, E * I, H);
-            ok &= weight_map(&maps->w[1], fmt, w->up.w, E * I, H);
+            ok &= weight_map(&maps->w[0], fmt, w->gate.w, E * I, H, true);
+            ok &= weight_map(&maps->w[1], fmt, w->up.w, E * I, H, true);
         } else {
-            ok &= weight_map(&maps->w[0], fmt, w->sh_gate.w, S, H);
-            ok &= weight_map(&maps->w[1], fmt, w->sh_up.w, S, H);
+            ok &= weight_map(&maps->w[0], fmt, w->sh_gate.w, S, H, true);
+            ok &= weight_map(&maps->w[1], fmt, w->sh_up.w, S, H, true);
         }
         if (S > 0) {
-            ok &= weight_map(&maps->ws[0], fmt, w->sh_gate.w, S, H);
-            ok &= weight_map(&maps->ws[1], fmt, w->sh_up.w, S, H);
+            ok &= weight_map(&maps->ws[0], fmt, w->sh_gate.w, S, H, true);
+            ok &= weight_map(&maps->ws[1], fmt, w->sh_up.w, S, H, true);
             ok &= act_map(&maps->bs, fmt, act_shared, n, H);
         } else {
             maps->ws[0] = maps->w[0];
@@ -812,11 +839,11 @@ bool build_tc_maps(int fmt, bool gate_up, const moe_weights_t* w, int E, int H, 
         }
         ok &= act_map(&maps->b, fmt, act_routed, n_routes_max, H);
     } else {
-        ok &= (E > 0) ? weight_map(&maps->w[0], fmt, w->down.w, E * H, I)
-                      : weight_map(&maps->w[0], fmt, w->sh_down.w, H, S);
+        ok &= (E > 0) ? weight_map(&maps->w[0], fmt, w->down.w, E * H, I, false)
+                      : weight_map(&maps->w[0], fmt, w->sh_down.w, H, S, false);
         maps->w[1] = maps->w[0];
         if (S > 0) {
-            ok &= weight_map(&maps->ws[0], fmt, w->sh_down.w, H, S);
+            ok &= weight_map(&maps->ws[0], fmt, w->sh_down.w, H, S, false);
             ok &= act_map(&maps->bs, fmt, act_shared, n, S);
         } else {
             maps->ws[0] = maps->w[0];
