@@ -676,32 +676,46 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                             }
                         }
                     } else {
-                        // NVFP4: 16 codes (8 bytes) per E4M3 block scale.
+                        // NVFP4: 16 codes (8 bytes) per E4M3 block scale.  A part is whole
+                        // pairs of blocks, one 16-byte chunk of the raw row each (a
+                        // conflict-free shared load under either swizzle).
+                        static_assert(PE % 32 == 0, "NVFP4 dequant parts are pairs of scale blocks");
     #pragma unroll
-                        for (int b = 0; b < PE / 16; ++b) {
-                            const int qb = pk0 / 16 + b;   // scale block of the stage
-                            const uint2 v = *reinterpret_cast<const uint2*>(raw + raw_chunk<C::kRawRow>(r, qb >> 1) + 8 * (qb & 1));
-                            const int kc = k0 + 16 * qb;
-                            uint32_t sc = 0;   // f16x2 of the block scale (0 outside the matrix)
+                        for (int b = 0; b < PE / 16; b += 2) {
+                            const int qb = pk0 / 16 + b;   // even scale block of the stage
+                            const uint4 v = *reinterpret_cast<const uint4*>(raw + raw_chunk<C::kRawRow>(r, qb >> 1));
+                            uint32_t sc[2] = {0u, 0u};   // f16x2 of the two block scales (0 outside the matrix)
                             if (t.K % C::kBK == 0) {
-                                // Fetched into shared memory with the codes (0 past the last row).
+                                // Fetched into shared memory with the codes (0 past the last row):
+                                // bytes qb and qb + 1 of the row's scales, in one 4-byte word.
                                 const uint32_t w = reinterpret_cast<const uint32_t*>(
                                     sScale + rs * C::kScaleStage + (pm * BM + r) * C::kScaleRow)[qb >> 2];
-                                const uint32_t bb = (w >> (8 * (qb & 3))) & 0xffu;
-                                sc = e4m3x2_to_f16x2(bb | (bb << 8));
-                            } else if (mrow < t.out && kc < t.K) {
-                                const uint8_t* sp = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[pm] : p.scale[pm]) +
-                                                    ((size_t)t.le * t.out + mrow) * (t.K / 16) + kc / 16;
-                                const uint32_t bb = __ldg(sp);
-                                sc = e4m3x2_to_f16x2(bb | (bb << 8));
-                            }
-                            uint32_t lo[4], hi[4];
-                            e2m1x8_to_f16x2x4(v.x, lo);
-                            e2m1x8_to_f16x2x4(v.y, hi);
+                                const uint32_t s2 = e4m3x2_to_f16x2((w >> (8 * (qb & 3))) & 0xffffu);
+                                sc[0] = __byte_perm(s2, 0u, 0x1010);
+                                sc[1] = __byte_perm(s2, 0u, 0x3232);
+                            } else {
     #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                o[8 * b + i] = f16x2_mul(lo[i], sc);
-                                o[8 * b + 4 + i] = f16x2_mul(hi[i], sc);
+                                for (int h = 0; h < 2; ++h) {
+                                    const int kc = k0 + 16 * (qb + h);
+                                    if (mrow < t.out && kc < t.K) {
+                                        const uint8_t* sp = reinterpret_cast<const uint8_t*>(sh ? p.sh_scale[pm] : p.scale[pm]) +
+                                                            ((size_t)t.le * t.out + mrow) * (t.K / 16) + kc / 16;
+                                        const uint32_t bb = __ldg(sp);
+                                        sc[h] = e4m3x2_to_f16x2(bb | (bb << 8));
+                                    }
+                                }
+                            }
+                            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    #pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                uint32_t lo[4], hi[4];
+                                e2m1x8_to_f16x2x4(w4[2 * h], lo);
+                                e2m1x8_to_f16x2x4(w4[2 * h + 1], hi);
+    #pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    o[8 * (b + h) + i] = f16x2_mul(lo[i], sc[h]);
+                                    o[8 * (b + h) + 4 + i] = f16x2_mul(hi[i], sc[h]);
+                                }
                             }
                         }
                     }
