@@ -609,9 +609,8 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                for (int sl = 0; sl < 2; ++sl)
-                    if ((amask >> sl) & 1) ptx::mbar_arrive(&acc_empty[sl]);
+            for (int sl = 0; sl < 2; ++sl)
+                if ((amask >> sl) & 1) ptx::mbar_arrive_elect(&acc_empty[sl]);
             slots.done(amask);
         }
     } else if constexpr (C::kDeq) {
@@ -725,13 +724,13 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                     else ptx::tmem_st32(ta, o);
                     // The codes are in registers: the raw stage may be refilled.
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&raw_empty[rs]);
+                    ptx::mbar_arrive_elect(&raw_empty[rs]);
                 }
                 if (!ok) break;
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&a_full[g]);
+                ptx::mbar_arrive_elect(&a_full[g]);
             }
             if (!ok) break;
         }
