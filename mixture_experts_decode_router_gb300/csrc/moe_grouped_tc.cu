@@ -175,7 +175,9 @@ struct Tile {
     int K;        // reduction length
 };
 
-__device__ __forceinline__ Tile decode_tile(int tau, const TcParams& p, int n_ssegs, int n_rsegs) {
+// Tiles in order: the shared expert's (token segments of sh_seg rows x its
+// BM-row blocks), then each routed segment's row blocks.
+__device__ __forceinline__ Tile decode_tile(int tau, const TcParams& p, int n_ssegs, int sh_seg) {
     Tile t;
     const int mbs = (p.sh_out + BM - 1) / BM;
     const int mbr = (p.out_dim + BM - 1) / BM;
@@ -183,8 +185,8 @@ __device__ __forceinline__ Tile decode_tile(int tau, const TcParams& p, int n_ss
         const int s = tau / mbs, mb = tau - s * mbs;
         t.e = -1;
         t.le = 0;
-        t.pos0 = s * NT;
-        t.ntok = min(NT, p.n - t.pos0);
+        t.pos0 = s * sh_seg;
+        t.ntok = min(sh_seg, p.n - t.pos0);
         t.m0 = mb * BM;
         t.out = p.sh_out;
         t.K = p.sh_in;
@@ -200,7 +202,6 @@ __device__ __forceinline__ Tile decode_tile(int tau, const TcParams& p, int n_ss
         t.out = p.out_dim;
         t.K = p.in_dim;
     }
-    (void)n_rsegs;
     return t;
 }
 
@@ -317,7 +318,12 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     pdl_wait();
 
     const int n_rsegs = p.ctrl->n_rsegs;
-    const int n_ssegs = (p.sh_out > 0) ? (p.n + NT - 1) / NT : 0;
+    // The shared expert's token segments: NT rows, or NT / 2 with one
+    // accumulator, so that its tiles alternate between the accumulator's two
+    // slots like the routed ones (a wide tile would hold both and stall the
+    // next tile's MMAs for its whole epilogue).
+    constexpr int kShSeg = C::kAccBufs == 1 ? NT / 2 : NT;
+    const int n_ssegs = (p.sh_out > 0) ? (p.n + kShSeg - 1) / kShSeg : 0;
     const int n_tiles = n_ssegs * ((p.sh_out + BM - 1) / BM) + n_rsegs * ((p.out_dim + BM - 1) / BM);
     int32_t* err = p.err;
 
@@ -329,7 +335,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         uint32_t it = 0;
         bool stop = false;
         for (int tau = blockIdx.x; tau < n_tiles && !stop && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
-            const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
+            const Tile t = decode_tile(tau, p, n_ssegs, kShSeg);
             const bool sh = t.e < 0;
             const int wrow = sh ? t.m0 : t.le * t.out + t.m0;
             const int nbox = (t.ntok + 15) >> 4;
@@ -414,7 +420,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             uint32_t it = 0;
             bool stop = false;
             for (int tau = blockIdx.x; tau < n_tiles && !stop && !*s_abort; tau += gridDim.x) {
-                const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
+                const Tile t = decode_tile(tau, p, n_ssegs, kShSeg);
                 const int nbox = (t.ntok + 15) >> 4;
                 const CUtensorMap* bmap = t.e < 0 ? &maps.bs : &maps.b;
                 const int KB = (t.K + C::kBK - 1) / C::kBK;
@@ -446,7 +452,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         uint32_t it = 0, git = 0;
         AccSlots<C::kAccBufs, C::kAccCols> slots;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
-            const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
+            const Tile t = decode_tile(tau, p, n_ssegs, kShSeg);
             const int nmma = ((t.ntok + 15) >> 4) << 4;
             int amask, acol;
             slots.pick(nmma, amask, acol);
@@ -530,7 +536,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const int row = 32 * q + lane;
         AccSlots<C::kAccBufs, C::kAccCols> slots;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
-            const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
+            const Tile t = decode_tile(tau, p, n_ssegs, kShSeg);
             int amask, acol;
             slots.pick(((t.ntok + 15) >> 4) << 4, amask, acol);
             const int m = t.m0 + row;
@@ -626,7 +632,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const uint32_t t_row = tmem + ((uint32_t)(32 * qd) << 16) + C::kAColBase + pm * (C::kBK / 2) + pk0 / 2;
         uint32_t it = 0, git = 0;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
-            const Tile t = decode_tile(tau, p, n_ssegs, n_rsegs);
+            const Tile t = decode_tile(tau, p, n_ssegs, kShSeg);
             const bool sh = t.e < 0;
             const int KB = (t.K + C::kBK - 1) / C::kBK;
             const int mrow = t.m0 + r;
