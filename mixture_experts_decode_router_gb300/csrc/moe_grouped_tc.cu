@@ -94,8 +94,11 @@ struct TcCfg {
     static constexpr int kGrp = (FMT == MOE_W_NVFP4 && !GU) ? 2 : (kDeq ? (GU ? 3 : 4) : 1);
     static constexpr int kAGroups = kAStages / kGrp;
     // Dequantised tiles: the token (B) tiles have a ring of their own, so they
-    // are fetched ahead instead of after the MMA frees an A slot.
-    static constexpr int kBStages = kDeq ? (GU ? 4 : 6) : kAStages;
+    // are fetched ahead instead of after the MMA frees an A slot.  It holds
+    // kBGroups groups of kGrp stages with one full / empty barrier pair per
+    // group, so the MMA warp waits and commits once per group, not per stage.
+    static constexpr int kBGroups = kDeq ? 2 : 1;   // (BF16: no token ring of its own)
+    static constexpr int kBStages = kDeq ? kBGroups * kGrp : kAStages;
     // Raw stages: FP8 10 / 16, NVFP4 16 (gate/up, 64 K) and 12 (down, 128 K: the
     // bytes of 24 stages of 64 K).
     static constexpr int kRawStages = !kDeq ? 0 : (GU ? (FMT == MOE_W_FP8_B128 ? 10 : 16) : (FMT == MOE_W_FP8_B128 ? 16 : 12));
@@ -416,32 +419,37 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
     } else if (C::kDeq && warp == C::kBWarp) {
         // ------------------------------------------------------------ token-tile producer
+        // Group by group, as the MMA warp consumes them: group gb (of the MMA
+        // warp's group sequence) fills B group gb % kBGroups, its stages' token
+        // tiles completing on that group's barrier.
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t gb = 0;
             bool stop = false;
             for (int tau = blockIdx.x; tau < n_tiles && !stop && !*s_abort; tau += gridDim.x) {
                 const Tile t = decode_tile(tau, p, n_ssegs, kShSeg);
                 const int nbox = (t.ntok + 15) >> 4;
                 const CUtensorMap* bmap = t.e < 0 ? &maps.bs : &maps.b;
                 const int KB = (t.K + C::kBK - 1) / C::kBK;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int bs = it % C::kBStages;
-                    if (!ptx::mbar_wait(&b_empty[bs], ((it / C::kBStages) & 1) ^ 1, s_abort, err, 5)) {
+                for (int kb = 0; kb < KB; ++gb) {
+                    const int bg = gb % C::kBGroups;
+                    const int n = min(C::kGrp, KB - kb);
+                    if (!ptx::mbar_wait(&b_empty[bg], ((gb / C::kBGroups) & 1) ^ 1, s_abort, err, 5)) {
                         stop = true;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(&b_full[bs], nbox * 2048 * (C::kBK / BK));
-                    for (int a = 0; a < C::kBK / BK; ++a)
-                        for (int j = 0; j < nbox; ++j)
-                            ptx::tma_load_2d(sB + bs * C::kBStage + a * C::kBAtom + j * 2048, bmap,
-                                             kb * C::kBK + a * BK, t.pos0 + 16 * j, &b_full[bs]);
+                    ptx::mbar_arrive_expect_tx(&b_full[bg], n * nbox * 2048 * (C::kBK / BK));
+                    for (int u = 0; u < n; ++u, ++kb)
+                        for (int a = 0; a < C::kBK / BK; ++a)
+                            for (int j = 0; j < nbox; ++j)
+                                ptx::tma_load_2d(sB + (bg * C::kGrp + u) * C::kBStage + a * C::kBAtom + j * 2048,
+                                                 bmap, kb * C::kBK + a * BK, t.pos0 + 16 * j, &b_full[bg]);
                 }
             }
             if (*s_abort) {
-                const uint32_t nb = it < (uint32_t)C::kBStages ? it : C::kBStages;
+                const uint32_t nb = gb < (uint32_t)C::kBGroups ? gb : C::kBGroups;
                 for (uint32_t q = 0; q < nb; ++q) {
-                    const uint32_t i2 = it - 1 - q, s2 = i2 % C::kBStages;
-                    ptx::mbar_wait_quiet(&b_full[s2], (i2 / C::kBStages) & 1, 100000000ull);
+                    const uint32_t i2 = gb - 1 - q, s2 = i2 % C::kBGroups;
+                    ptx::mbar_wait_quiet(&b_full[s2], (i2 / C::kBGroups) & 1, 100000000ull);
                 }
             }
         }
@@ -449,7 +457,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp runs the loop, so the operand descriptors are
         // warp-uniform values; one elected lane issues the MMAs and commits.
-        uint32_t it = 0, git = 0;
+        uint32_t git = 0;
         AccSlots<C::kAccBufs, C::kAccCols> slots;
         for (int tau = blockIdx.x; tau < n_tiles && !ptx::aborted_warp(s_abort); tau += gridDim.x) {
             const Tile t = decode_tile(tau, p, n_ssegs, kShSeg);
@@ -469,17 +477,18 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             for (int kb = 0; kb < KB && ok; ++git) {
                 // One group of operand stages: one a_full wait, one a_empty commit.
                 const int g = git % C::kAGroups;
+                const int bg = C::kDeq ? (int)(git % C::kBGroups) : 0;
                 if (!ptx::mbar_wait_warp(&a_full[g], (git / C::kAGroups) & 1, s_abort, err, 2)) { ok = false; break; }
+                if constexpr (C::kDeq)
+                    if (!ptx::mbar_wait_warp(&b_full[bg], (git / C::kBGroups) & 1, s_abort, err, 2)) {
+                        ok = false;
+                        break;
+                    }
+                ptx::tc_fence_after();
                 const int n = min(C::kGrp, KB - kb);
-                for (int u = 0; u < n; ++u, ++kb, ++it) {
+                for (int u = 0; u < n; ++u, ++kb) {
                     const int as = g * C::kGrp + u;
-                    const int bs = C::kDeq ? (int)(it % C::kBStages) : as;
-                    if constexpr (C::kDeq)
-                        if (!ptx::mbar_wait_warp(&b_full[bs], (it / C::kBStages) & 1, s_abort, err, 2)) {
-                            ok = false;
-                            break;
-                        }
-                    ptx::tc_fence_after();
+                    const int bs = C::kDeq ? bg * C::kGrp + u : as;
                     // Descriptors of the stage's first K step; a later step (or the
                     // second matrix) only moves the start address field (16-byte units):
                     // K step kk of the token tile is 32 bytes into swizzle atom kk / 4.
@@ -495,7 +504,6 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                                     ptx::mma_f16_ts(d0 + m * NT, a_t + m * (C::kBK / 2) + kk * 8,
                                                     b_desc + (uint64_t)(((kk >> 2) * C::kBAtom + (kk & 3) * 32) >> 4),
                                                     idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                            ptx::mma_commit(&b_empty[bs]);
                         }
                     } else {
                         const uint64_t a_desc = ptx::sw128_desc(ptx::smem_u32(sA + as * C::kAStage));
@@ -511,7 +519,10 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                     }
                     __syncwarp();
                 }
-                if (ptx::elect_one()) ptx::mma_commit(&a_empty[g]);   // after the group's MMAs
+                if (ptx::elect_one()) {   // after the group's MMAs
+                    ptx::mma_commit(&a_empty[g]);
+                    if constexpr (C::kDeq) ptx::mma_commit(&b_empty[bg]);
+                }
                 __syncwarp();
             }
             if (!ok) break;
