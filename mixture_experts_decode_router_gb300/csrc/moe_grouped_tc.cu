@@ -85,13 +85,13 @@ struct TcCfg {
     static constexpr int kTmemCols = kDeq ? 512 : kAccBufs * kAccCols;
     static constexpr int kAStages = kDeq ? (512 - kAColBase) / kACols : (GU ? 5 : 8);
     static constexpr int kASmemStages = kDeq ? 0 : kAStages;
-    // Dequantised tiles hand operand stages to the MMA warp in groups: three
-    // for gate/up (one barrier round trip per 192 K instead of per 64;
-    // measured faster than groups of one or two), four for down, whose twelve
-    // operand stages make three groups (measured 1-1.5% faster than three;
-    // six was slower).
-    // NVFP4 down (128-K stages): its six operand stages in pairs.
-    static constexpr int kGrp = (FMT == MOE_W_NVFP4 && !GU) ? 2 : (kDeq ? (GU ? 3 : 4) : 1);
+    // Dequantised tiles hand operand stages to the MMA warp in groups (one
+    // barrier round trip per group instead of per stage), sizes measured on
+    // GB300: NVFP4 gate/up three of its six 64-K stages, NVFP4 down two of its
+    // six 128-K stages; FP8 gate/up two of six, FP8 down three of twelve
+    // (fp8_n64 1129 -> 1113 us for gate/up pairs, -> 1121 us for down triples;
+    // NVFP4 gate/up pairs were slower, 214 -> 219 us at nvfp4_n256).
+    static constexpr int kGrp = !kDeq ? 1 : (FMT == MOE_W_NVFP4 ? (GU ? 3 : 2) : (GU ? 2 : 3));
     static constexpr int kAGroups = kAStages / kGrp;
     // Dequantised tiles: the token (B) tiles have a ring of their own, so they
     // are fetched ahead instead of after the MMA frees an A slot.  It holds
@@ -102,7 +102,9 @@ struct TcCfg {
     // Raw stages: FP8 10 / 16, NVFP4 16 (gate/up, 64 K) and 12 (down, 128 K: the
     // bytes of 24 stages of 64 K).
     static constexpr int kRawStages = !kDeq ? 0 : (GU ? (FMT == MOE_W_FP8_B128 ? 10 : 16) : (FMT == MOE_W_FP8_B128 ? 16 : 12));
-    static constexpr int kDeqWarps = kDeq ? (FMT == MOE_W_NVFP4 ? 16 : 8) : 0;
+    // Dequant warps: 8 (two per TMEM lane quarter); NVFP4 with 16 measured
+    // slower once the handshakes were cheap (nvfp4_n256 219.5 -> 213.7 us with 8).
+    static constexpr int kDeqWarps = kDeq ? 8 : 0;
     // Dequant work split: warp 6 + dw serves TMEM lane quarter (6 + dw) & 3 (the
     // quarter a warp may access) and part dw >> 2 of each row's kMats x kBK codes.
     static constexpr int kParts = kDeqWarps / 4;
@@ -486,44 +488,43 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                     }
                 ptx::tc_fence_after();
                 const int n = min(C::kGrp, KB - kb);
-                for (int u = 0; u < n; ++u, ++kb) {
-                    const int as = g * C::kGrp + u;
-                    const int bs = C::kDeq ? bg * C::kGrp + u : as;
-                    // Descriptors of the stage's first K step; a later step (or the
-                    // second matrix) only moves the start address field (16-byte units):
-                    // K step kk of the token tile is 32 bytes into swizzle atom kk / 4.
-                    const uint64_t b_desc = ptx::sw128_desc(ptx::smem_u32(sB + bs * C::kBStage));
-                    if constexpr (C::kDeq) {
-                        // A in tensor memory: K step kk of matrix m is 8 columns on.
-                        const uint32_t a_t = tmem + C::kAColBase + as * C::kACols;
-                        if (ptx::elect_one()) {
+                // The group's MMAs and its commits from one elected lane (one
+                // divergent region per group, not per stage).
+                if (ptx::elect_one()) {
+                    for (int u = 0; u < n; ++u) {
+                        const int as = g * C::kGrp + u;
+                        const int bs = C::kDeq ? bg * C::kGrp + u : as;
+                        const bool first = kb + u == 0;   // the tile's first stage starts the accumulator
+                        // Descriptors of the stage's first K step; a later step (or the
+                        // second matrix) only moves the start address field (16-byte units):
+                        // K step kk of the token tile is 32 bytes into swizzle atom kk / 4.
+                        const uint64_t b_desc = ptx::sw128_desc(ptx::smem_u32(sB + bs * C::kBStage));
+                        if constexpr (C::kDeq) {
+                            // A in tensor memory: K step kk of matrix m is 8 columns on.
+                            const uint32_t a_t = tmem + C::kAColBase + as * C::kACols;
     #pragma unroll
                             for (int m = 0; m < C::kMats; ++m)
     #pragma unroll
                                 for (int kk = 0; kk < C::kBK / 16; ++kk)
                                     ptx::mma_f16_ts(d0 + m * NT, a_t + m * (C::kBK / 2) + kk * 8,
                                                     b_desc + (uint64_t)(((kk >> 2) * C::kBAtom + (kk & 3) * 32) >> 4),
-                                                    idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                        }
-                    } else {
-                        const uint64_t a_desc = ptx::sw128_desc(ptx::smem_u32(sA + as * C::kAStage));
-                        if (ptx::elect_one()) {
+                                                    idesc, (!first || kk > 0) ? 1u : 0u);
+                        } else {
+                            const uint64_t a_desc = ptx::sw128_desc(ptx::smem_u32(sA + as * C::kAStage));
     #pragma unroll
                             for (int m = 0; m < C::kMats; ++m)
     #pragma unroll
                                 for (int kk = 0; kk < C::kBK / 16; ++kk)   // BF16: kBK == BK, one atom
                                     ptx::mma_f16(d0 + m * NT, a_desc + (uint64_t)((m * C::kAMat + kk * 32) >> 4),
                                                  b_desc + (uint64_t)((kk * 32) >> 4), idesc,
-                                                 (kb > 0 || kk > 0) ? 1u : 0u);
+                                                 (!first || kk > 0) ? 1u : 0u);
                         }
                     }
-                    __syncwarp();
-                }
-                if (ptx::elect_one()) {   // after the group's MMAs
-                    ptx::mma_commit(&a_empty[g]);
+                    ptx::mma_commit(&a_empty[g]);   // after the group's MMAs
                     if constexpr (C::kDeq) ptx::mma_commit(&b_empty[bg]);
                 }
                 __syncwarp();
+                kb += n;
             }
             if (!ok) break;
             if (ptx::elect_one())
