@@ -20,52 +20,82 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // read only workspace buffers: x itself is read here with plain loads, so it
 // may also live in pinned host memory.
 template <bool F16>
+__device__ __forceinline__ uint4 to_tile16(uint4 v) {
+    if constexpr (F16) {
+        uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xffff0000u);
+            const __half2 h = __floats2half2_rn(fminf(fmaxf(lo, -65504.f), 65504.f),
+                                                fminf(fmaxf(hi, -65504.f), 65504.f));
+            w4[q] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        return make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+    return v;
+}
+
+// One warp per destination row (the row's source index read once), its lanes
+// taking 16-byte chunks lane, lane + 32, ...: kU chunks per lane loaded before
+// any is stored, so a row costs one round of load latency, not one per chunk.
+template <bool F16>
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int n, int H, int k,
                                                      const int32_t* __restrict__ perm,
                                                      const int32_t* __restrict__ offsets, int E,
                                                      uint16_t* __restrict__ xs, uint16_t* __restrict__ xh) {
+    constexpr int kU = 8;
     pdl_wait();
     const int n_routes = offsets[E];
     const int rows = n_routes + n;
     const int C8 = H >> 3;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)rows * C8;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int r = (int)(i / C8), c = (int)(i - (int64_t)r * C8);
+    const int lane = threadIdx.x & 31;
+    const int nwarps = gridDim.x * (blockDim.x >> 5);
+    for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
         const bool routed = r < n_routes;
         const int t = routed ? perm[r] / k : r - n_routes;
-        uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c);
-        if constexpr (F16) {
-            uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+        uint4* dst = reinterpret_cast<uint4*>(routed ? xs + (size_t)r * H : xh + (size_t)(r - n_routes) * H);
+        for (int c0 = lane; c0 < C8; c0 += 32 * kU) {
+            uint4 v[kU];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xffff0000u);
-                const __half2 h = __floats2half2_rn(fminf(fmaxf(lo, -65504.f), 65504.f),
-                                                    fminf(fmaxf(hi, -65504.f), 65504.f));
-                w4[q] = *reinterpret_cast<const uint32_t*>(&h);
+            for (int u = 0; u < kU; ++u) {
+                const int c = c0 + 32 * u;
+                if (c < C8) v[u] = __ldg(src + c);
             }
-            v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int c = c0 + 32 * u;
+                if (c < C8) dst[c] = to_tile16<F16>(v[u]);
+            }
         }
-        uint16_t* dst = routed ? xs + (size_t)r * H : xh + (size_t)(r - n_routes) * H;
-        reinterpret_cast<uint4*>(dst)[c] = v;
     }
     pdl_trigger();
 }
 
 // out[t, h] = bf16( sum_j y[inv[t*k + j], h] (slot order) + y_sh[t, h] ).
+// The slots' positions and rows are loaded kU at a time before they are
+// summed (one round of load latency per kU slots); the sum keeps slot order.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ ysh,
                                                       const int32_t* __restrict__ inv, int n, int H, int k,
                                                       int has_shared, int accumulate, uint16_t* __restrict__ out) {
+    constexpr int kU = 8;
     pdl_wait();
     const int C4 = H >> 2;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)n * C4;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int t = (int)(i / C4), c = (int)(i - (int64_t)t * C4);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            const int pos = __ldg(inv + t * k + j);
-            if (pos < 0) continue;
-            const float4 v = __ldg(reinterpret_cast<const float4*>(y + (size_t)pos * H) + c);
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        for (int j0 = 0; j0 < k; j0 += kU) {
+            int pos[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) pos[u] = (j0 + u < k) ? __ldg(inv + t * k + j0 + u) : -1;
+            float4 v[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                if (pos[u] >= 0) v[u] = __ldg(reinterpret_cast<const float4*>(y + (size_t)pos[u] * H) + c);
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                if (pos[u] >= 0) { acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w; }
         }
         if (has_shared) {
             const float4 v = __ldg(reinterpret_cast<const float4*>(ysh + (size_t)t * H) + c);

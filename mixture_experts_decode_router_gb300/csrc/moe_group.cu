@@ -25,6 +25,7 @@ namespace moe {
 
 constexpr int kGroupThreads = 1024;
 constexpr int kSegWarps = 8;   // warps that own contiguous route segments
+constexpr int kIdxBatch = 8;   // rounds of 32 routes a segment warp loads before using them
 
 // The grouping of all n*k routes by one block of kGroupThreads threads.
 // sm: (kSegWarps + 1) * E ints of shared memory.
@@ -44,9 +45,17 @@ __device__ __forceinline__ void group_block(const int32_t* __restrict__ idx, int
     const int seg = (nk + kSegWarps - 1) / kSegWarps;
     if (warp < kSegWarps) {
         const int b = warp * seg, e_ = min(nk, b + seg);
-        for (int r = b + lane; r < e_; r += 32) {
-            const int e = __ldcg(idx + r);   // L2: the fused kernel's other blocks wrote idx
-            if (e >= e_begin && e < e_end) atomicAdd(&cnt[warp * E + e], 1);   // not held here: dropped
+        for (int r0 = b; r0 < e_; r0 += 32 * kIdxBatch) {
+            int ev[kIdxBatch];   // L2 (__ldcg): the fused kernel's other blocks wrote idx
+#pragma unroll
+            for (int u = 0; u < kIdxBatch; ++u) {
+                const int r = r0 + 32 * u + lane;
+                ev[u] = r < e_ ? __ldcg(idx + r) : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < kIdxBatch; ++u)
+                if (r0 + 32 * u + lane < e_ && ev[u] >= e_begin && ev[u] < e_end)
+                    atomicAdd(&cnt[warp * E + ev[u]], 1);   // not held here: dropped
         }
     }
     __syncthreads();
@@ -118,26 +127,38 @@ __device__ __forceinline__ void group_block(const int32_t* __restrict__ idx, int
     }
     __syncthreads();
 
-    // Stable scatter: each segment warp walks its routes in order.
+    // Stable scatter: each segment warp walks its routes in order (loaded
+    // kIdxBatch rounds of 32 at a time).
     if (warp < kSegWarps) {
         const int b = warp * seg, e_ = min(nk, b + seg);
-        for (int r0 = b; r0 < e_; r0 += 32) {
-            const int r = r0 + lane;
-            const bool valid = r < e_;
-            const int e = valid ? __ldcg(idx + r) : -1;
-            const bool in_range = valid && e >= e_begin && e < e_end;
-            if (valid && !in_range) inv[r] = -1;
-            const unsigned vmask = __ballot_sync(0xffffffffu, in_range);
-            if (in_range) {
-                const unsigned peers = __match_any_sync(vmask, e);
-                const int rank = __popc(peers & ((1u << lane) - 1u));
-                const int pos = tot[e] + cnt[warp * E + e] + rank;
-                perm[pos] = r;
-                inv[r] = pos;
-                __syncwarp(vmask);
-                if (rank == 0) cnt[warp * E + e] += __popc(peers);
+        for (int r1 = b; r1 < e_; r1 += 32 * kIdxBatch) {
+            int ev[kIdxBatch];
+#pragma unroll
+            for (int u = 0; u < kIdxBatch; ++u) {
+                const int r = r1 + 32 * u + lane;
+                ev[u] = r < e_ ? __ldcg(idx + r) : -1;
             }
-            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < kIdxBatch; ++u) {
+                const int r0 = r1 + 32 * u;
+                if (r0 >= e_) break;   // warp-uniform
+                const int r = r0 + lane;
+                const bool valid = r < e_;
+                const int e = ev[u];
+                const bool in_range = valid && e >= e_begin && e < e_end;
+                if (valid && !in_range) inv[r] = -1;
+                const unsigned vmask = __ballot_sync(0xffffffffu, in_range);
+                if (in_range) {
+                    const unsigned peers = __match_any_sync(vmask, e);
+                    const int rank = __popc(peers & ((1u << lane) - 1u));
+                    const int pos = tot[e] + cnt[warp * E + e] + rank;
+                    perm[pos] = r;
+                    inv[r] = pos;
+                    __syncwarp(vmask);
+                    if (rank == 0) cnt[warp * E + e] += __popc(peers);
+                }
+                __syncwarp();
+            }
         }
     }
 }
