@@ -17,6 +17,7 @@
 //   segs[s]     (expert, first sorted position, routes) for runs of at most
 //               kTcTokensPerTile routes of one expert, ascending expert;
 //               ctrl->n_rsegs of them (the tiles of the grouped path)
+#include <algorithm>
 #include <mutex>
 
 #include "moe_launch.cuh"
@@ -24,26 +25,35 @@
 namespace moe {
 
 constexpr int kGroupThreads = 1024;
-constexpr int kSegWarps = 8;   // warps that own contiguous route segments
 constexpr int kIdxBatch = 8;   // rounds of 32 routes a segment warp loads before using them
 
-// The grouping of all n*k routes by one block of kGroupThreads threads.
-// sm: (kSegWarps + 1) * E ints of shared memory.
+// Warps that own contiguous route segments: 8, or one per 64 routes (two
+// rounds of 32 each) above 512 routes, at most as many as keep the per-warp
+// counts, (warps + 1) * E ints, within 36 KB -- 32 for E <= 256, 16 for
+// E <= 512, 8 for E <= 1024.  (Measured on GB300: 2048 routes group faster
+// with 32 warps; 128 routes slower with 2 or 32 than with 8.)
+inline int seg_warps(int E, int nk) {
+    const int cap = E <= 256 ? 32 : (E <= 512 ? 16 : 8);
+    return std::min(cap, std::max(8, nk / 64));
+}
+
+// The grouping of all n*k routes by one block of kGroupThreads threads, sw of
+// whose warps own route segments.  sm: (sw + 1) * E ints of shared memory.
 __device__ __forceinline__ void group_block(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_end,
                                             int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                             int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                                             int32_t* __restrict__ active, int32_t* __restrict__ segs,
-                                            Ctrl* __restrict__ ctrl, int32_t* sm) {
-    int32_t* cnt = sm;                           // [kSegWarps][E]
-    int32_t* tot = sm + kSegWarps * E;           // [E]
+                                            Ctrl* __restrict__ ctrl, int32_t* sm, int sw) {
+    int32_t* cnt = sm;                           // [sw][E]
+    int32_t* tot = sm + sw * E;                  // [E]
     __shared__ int32_t warp_sums[3][32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    for (int i = tid; i < kSegWarps * E; i += blockDim.x) cnt[i] = 0;
+    for (int i = tid; i < sw * E; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
 
-    const int seg = (nk + kSegWarps - 1) / kSegWarps;
-    if (warp < kSegWarps) {
+    const int seg = (nk + sw - 1) / sw;
+    if (warp < sw) {
         const int b = warp * seg, e_ = min(nk, b + seg);
         for (int r0 = b; r0 < e_; r0 += 32 * kIdxBatch) {
             int ev[kIdxBatch];   // L2 (__ldcg): the fused kernel's other blocks wrote idx
@@ -63,7 +73,7 @@ __device__ __forceinline__ void group_block(const int32_t* __restrict__ idx, int
     // Per expert: exclusive scan over the segment warps, and the total.
     for (int e = tid; e < E; e += blockDim.x) {
         int run = 0;
-        for (int w = 0; w < kSegWarps; ++w) {
+        for (int w = 0; w < sw; ++w) {
             const int c = cnt[w * E + e];
             cnt[w * E + e] = run;
             run += c;
@@ -129,7 +139,7 @@ __device__ __forceinline__ void group_block(const int32_t* __restrict__ idx, int
 
     // Stable scatter: each segment warp walks its routes in order (loaded
     // kIdxBatch rounds of 32 at a time).
-    if (warp < kSegWarps) {
+    if (warp < sw) {
         const int b = warp * seg, e_ = min(nk, b + seg);
         for (int r1 = b; r1 < e_; r1 += 32 * kIdxBatch) {
             int ev[kIdxBatch];
@@ -167,10 +177,10 @@ __global__ void __launch_bounds__(kGroupThreads)
 group_kernel(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_end,
              int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
              int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ active,
-             int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl) {
+             int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl, int sw) {
     extern __shared__ int32_t sm[];
     pdl_wait();
-    group_block(idx, nk, E, e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, sm);
+    group_block(idx, nk, E, e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, sm, sw);
     pdl_trigger();
 }
 
@@ -178,13 +188,14 @@ group_kernel(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_
 // arithmetic) and then, in the CTA that finishes last, the grouping of all
 // routes: one launch instead of two.  The last CTA is found with a counter in
 // the control block (release fence before the increment, acquire fence after
-// it), which that CTA returns to zero.
-__global__ void __launch_bounds__(kGroupThreads)
+// it), which that CTA returns to zero.  Two CTAs per SM (at most 32 registers
+// a thread), so 256 tokens route in one wave.
+__global__ void __launch_bounds__(kGroupThreads, 2)
 topk_group_kernel(const float* __restrict__ logits, int n, int E, int k, int routing,
                   const float* __restrict__ bias, int norm, float scale, int32_t* idx_out,
                   float* __restrict__ w_out, int e_begin, int e_end, int32_t* __restrict__ counts,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-                  int32_t* __restrict__ active, int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl) {
+                  int32_t* __restrict__ active, int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl, int sw) {
     extern __shared__ __align__(16) float smf[];
     float* slg = smf;                                                    // [E]
     unsigned long long* skey =
@@ -212,7 +223,7 @@ topk_group_kernel(const float* __restrict__ logits, int n, int E, int k, int rou
     }
     __syncthreads();
     if (s_last) {
-        group_block(idx_out, n * k, E, e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, gsm);
+        group_block(idx_out, n * k, E, e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, gsm, sw);
         if (tid == 0) ctrl->routed = 0;
     }
     pdl_trigger();
@@ -221,10 +232,11 @@ topk_group_kernel(const float* __restrict__ logits, int n, int E, int k, int rou
 cudaError_t launch_group(const int32_t* idx, int nk, int E, int e_begin, int e_end, int32_t* counts,
                          int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
                          Ctrl* ctrl, cudaStream_t st) {
-    const size_t smem = sizeof(int32_t) * (size_t)(kSegWarps + 1) * E;
-    // (kSegWarps + 1) * E ints <= 36 KB for E <= 1024: under the 48 KB default.
-    launch_pdl(group_kernel, 1, kGroupThreads, smem, st, idx, nk, E, e_begin, e_end, counts, offsets, perm, inv, active, segs,
-                                                  ctrl);
+    const int sw = seg_warps(E, nk);
+    const size_t smem = sizeof(int32_t) * (size_t)(sw + 1) * E;
+    // (sw + 1) * E ints <= 36 KB for E <= 1024: under the 48 KB default.
+    launch_pdl(group_kernel, 1, kGroupThreads, smem, st, idx, nk, E, e_begin, e_end, counts, offsets, perm, inv,
+               active, segs, ctrl, sw);
     return cudaGetLastError();
 }
 
@@ -232,8 +244,9 @@ cudaError_t launch_topk_group(const float* logits, int n, int E, int k, int rout
                               float scale, int32_t* idx, float* w, int e_begin, int e_end, int32_t* counts,
                               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
                               Ctrl* ctrl, cudaStream_t st) {
+    const int sw = seg_warps(E, n * k);
     const size_t smem = (size_t)((E + 3) & ~3) * sizeof(float) + (size_t)(E + 32) * sizeof(unsigned long long) +
-                        sizeof(int32_t) * (size_t)(kSegWarps + 1) * E;
+                        sizeof(int32_t) * (size_t)(sw + 1) * E;
     static std::mutex mu;
     static size_t configured[128] = {};
     int dev = 0;
@@ -248,7 +261,7 @@ cudaError_t launch_topk_group(const float* logits, int n, int E, int k, int rout
         }
     }
     launch_pdl(topk_group_kernel, n, kGroupThreads, smem, st, logits, n, E, k, routing, bias, norm, scale, idx, w,
-               e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl);
+               e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, sw);
     return cudaGetLastError();
 }
 

@@ -94,9 +94,24 @@ router_tiled_kernel(const uint16_t* __restrict__ x, int n, int H,
     const int t0 = blockIdx.y * RT;
     const int C = H >> 3;
     if constexpr (XS) {
-        for (int i = threadIdx.x; i < RT * C; i += blockDim.x) {
-            const int b = i / C, c = i - b * C;
-            sxt[i] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)min(t0 + b, n - 1) * H) + c);
+        // Eight chunks a thread loaded before any is stored: one round of load
+        // latency for (up to) 8 x 256 chunks, not one per chunk.
+        constexpr int kU = 8;
+        for (int i0 = threadIdx.x; i0 < RT * C; i0 += kU * blockDim.x) {
+            uint4 v[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + u * blockDim.x;
+                if (i < RT * C) {
+                    const int b = i / C, c = i - b * C;
+                    v[u] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)min(t0 + b, n - 1) * H) + c);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + u * blockDim.x;
+                if (i < RT * C) sxt[i] = v[u];
+            }
         }
         __syncthreads();
         if (r0 >= rows) {
