@@ -212,7 +212,7 @@ static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w,
                               c->routed_scaling_factor, idx, wt, c->expert_begin, c->expert_end,
                               at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm),
                               at<int32_t>(ws, L.inv), at<int32_t>(ws, L.active), at<int32_t>(ws, L.segs),
-                              at<Ctrl>(ws, L.ctrl), st);
+                              at<Ctrl>(ws, L.ctrl), sms, st);
     else
         e = launch_topk(lg, n, c->num_experts, c->top_k, c->routing, w->correction_bias,
                         c->norm_topk_prob, c->routed_scaling_factor, idx, wt, st);

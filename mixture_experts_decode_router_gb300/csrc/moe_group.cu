@@ -188,9 +188,11 @@ group_kernel(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_
 // arithmetic) and then, in the CTA that finishes last, the grouping of all
 // routes: one launch instead of two.  The last CTA is found with a counter in
 // the control block (release fence before the increment, acquire fence after
-// it), which that CTA returns to zero.  Two CTAs per SM (at most 32 registers
-// a thread), so 256 tokens route in one wave.
-__global__ void __launch_bounds__(kGroupThreads, 2)
+// it), which that CTA returns to zero.  kMinBlocks = 2 (at most 32 registers
+// a thread) when there are more tokens than SMs, so that up to two SMs' worth
+// route in one wave; 1 otherwise (no register cap).
+template <int kMinBlocks>
+__global__ void __launch_bounds__(kGroupThreads, kMinBlocks)
 topk_group_kernel(const float* __restrict__ logits, int n, int E, int k, int routing,
                   const float* __restrict__ bias, int norm, float scale, int32_t* idx_out,
                   float* __restrict__ w_out, int e_begin, int e_end, int32_t* __restrict__ counts,
@@ -243,24 +245,25 @@ cudaError_t launch_group(const int32_t* idx, int nk, int E, int e_begin, int e_e
 cudaError_t launch_topk_group(const float* logits, int n, int E, int k, int routing, const float* bias, int norm,
                               float scale, int32_t* idx, float* w, int e_begin, int e_end, int32_t* counts,
                               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
-                              Ctrl* ctrl, cudaStream_t st) {
+                              Ctrl* ctrl, int num_sms, cudaStream_t st) {
     const int sw = seg_warps(E, n * k);
     const size_t smem = (size_t)((E + 3) & ~3) * sizeof(float) + (size_t)(E + 32) * sizeof(unsigned long long) +
                         sizeof(int32_t) * (size_t)(sw + 1) * E;
     static std::mutex mu;
-    static size_t configured[128] = {};
+    static size_t configured[128][2] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    const bool two = n > num_sms;
+    auto kern = two ? topk_group_kernel<2> : topk_group_kernel<1>;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (configured[dev] < smem) {
-            const cudaError_t e =
-                cudaFuncSetAttribute(topk_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (configured[dev][two] < smem) {
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            configured[dev] = smem;
+            configured[dev][two] = smem;
         }
     }
-    launch_pdl(topk_group_kernel, n, kGroupThreads, smem, st, logits, n, E, k, routing, bias, norm, scale, idx, w,
+    launch_pdl(kern, n, kGroupThreads, smem, st, logits, n, E, k, routing, bias, norm, scale, idx, w,
                e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, sw);
     return cudaGetLastError();
 }

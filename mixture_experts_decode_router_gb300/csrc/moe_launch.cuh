@@ -119,7 +119,7 @@ cudaError_t launch_group(const int32_t* idx, int nk, int E, int e_begin, int e_e
 cudaError_t launch_topk_group(const float* logits, int n, int E, int k, int routing, const float* bias, int norm,
                               float scale, int32_t* idx, float* w, int e_begin, int e_end, int32_t* counts,
                               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
-                              Ctrl* ctrl, cudaStream_t st);
+                              Ctrl* ctrl, int num_sms, cudaStream_t st);
 cudaError_t launch_rmsnorm(const uint16_t* x, int n, int H, const uint16_t* w, float eps, uint16_t* xe,
                            cudaStream_t st);
 cudaError_t launch_gate_up_tm(int fmt, const GateUpParams& gu, int num_sms, cudaStream_t st);
