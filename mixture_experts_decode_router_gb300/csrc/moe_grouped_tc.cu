@@ -102,12 +102,20 @@ struct TcCfg {
     // Raw stages: FP8 10 / 16, NVFP4 16 (gate/up, 64 K) and 12 (down, 128 K: the
     // bytes of 24 stages of 64 K).
     static constexpr int kRawStages = !kDeq ? 0 : (GU ? (FMT == MOE_W_FP8_B128 ? 10 : 16) : (FMT == MOE_W_FP8_B128 ? 16 : 12));
-    // Dequant warps: 8 (two per TMEM lane quarter); NVFP4 with 16 measured
-    // slower once the handshakes were cheap (nvfp4_n256 219.5 -> 213.7 us with 8).
-    static constexpr int kDeqWarps = kDeq ? 8 : 0;
+    // Dequant warps: kDeqSets sets of 8 (two per TMEM lane quarter); set s
+    // converts the stages with stage counter = s (mod kDeqSets), so a set's
+    // warps overlap their per-stage chains with the other set's while every
+    // stage still has 8 handshakes.  Measured on GB300: FP8 gate/up two sets
+    // (fp8_n64 gate/up 668 -> 638 us; its down kernel was slower with two,
+    // 405 -> 418 us), NVFP4 one (two: nvfp4_n256 207.4 -> 211.3 us; 16 warps
+    // each converting a quarter of every stage: 213.7 -> 219.5).
+    static constexpr int kDeqSets = !kDeq ? 0 : ((FMT == MOE_W_FP8_B128 && GU) ? 2 : 1);
+    static constexpr int kSetWarps = 8;
+    static constexpr int kDeqWarps = kDeqSets * kSetWarps;
     // Dequant work split: warp 6 + dw serves TMEM lane quarter (6 + dw) & 3 (the
-    // quarter a warp may access) and part dw >> 2 of each row's kMats x kBK codes.
-    static constexpr int kParts = kDeqWarps / 4;
+    // quarter a warp may access), set dw / 8 and part (dw % 8) >> 2 of each row's
+    // kMats x kBK codes.
+    static constexpr int kParts = kSetWarps / 4;
     static constexpr int kPartElems = kDeq ? kMats * kBK / kParts : 0;
     // Dequantised tiles: a second producer warp for the token (B) tiles, after
     // the dequant warps, so a full B ring never holds up the weight copies.
@@ -305,7 +313,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
         for (int s = 0; s < C::kRawStages; ++s) {
             ptx::mbar_init(&raw_full[s], 1 + 32);   // TMA expect_tx + the producer warp's scale copies
-            ptx::mbar_init(&raw_empty[s], C::kDeqWarps);
+            ptx::mbar_init(&raw_empty[s], C::kSetWarps);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
@@ -638,7 +646,8 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         // the stage, kPartElems / 2 f16x2 words written to that row's lane of
         // the stage's TMEM operand columns.
         constexpr int PE = C::kPartElems, NC = PE / 2;
-        const int qd = warp & 3, part = (warp - 6) >> 2;
+        const int dset = (warp - 6) / C::kSetWarps;
+        const int qd = warp & 3, part = ((warp - 6) % C::kSetWarps) >> 2;
         const int r = 32 * qd + lane;
         const int pm = (part * PE) / C::kBK, pk0 = (part * PE) % C::kBK;
         const uint32_t t_row = tmem + ((uint32_t)(32 * qd) << 16) + C::kAColBase + pm * (C::kBK / 2) + pk0 / 2;
@@ -656,6 +665,7 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                 ptx::tc_fence_after();   // the MMAs that read these columns are complete
                 const int n = min(C::kGrp, KB - kb);
                 for (int u = 0; u < n; ++u, ++kb, ++it) {
+                    if (C::kDeqSets > 1 && (int)(it % C::kDeqSets) != dset) continue;   // the other set's stage
                     const int rs = it % C::kRawStages, as = g * C::kGrp + u;
                     if (!ptx::mbar_wait_warp(&raw_full[rs], (it / C::kRawStages) & 1, s_abort, err, 4)) { ok = false; break; }
                     const int k0 = kb * C::kBK;
