@@ -195,6 +195,11 @@ typedef struct {
 size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t max_tokens);
 
 /* Router and top-k for n tokens (the pages' gate and topk steps, grouped_route).
+ * The router runs where moe_forward's would for the same cfg and n: a BF16
+ * router on the grouped path (cfg->path, or n > 3 under MOE_PATH_AUTO) on the
+ * tensor cores (fp32 accumulation per K range, the ranges summed in a fixed
+ * order), otherwise on the CUDA cores; so moe_route + moe_experts is
+ * moe_forward bit for bit.
  *   x       device BF16 [n, H]
  *   idx     device int32 [n, k]   (out) selected experts, descending score
  *   w       device fp32  [n, k]   (out) routing weights
@@ -284,7 +289,7 @@ moe_status_t moe_forward_static_ws(const moe_config_t* cfg, const moe_weights_t*
  * Reads, then clears, the array's device error word and resets its
  * single-token barrier word, so the next static call runs; synchronises
  * `stream`.
- *   device_error (out)  as moe_workspace_check: 0, 11-17, 1-5 or 20.
+ *   device_error (out)  as moe_workspace_check: 0, 11-17, 1-7 or 20.
  *   workspace    (out, optional) the array's device address on this device
  *                (NULL = not returned); the library owns it.
  * The first use on a device runs the set-up of moe_forward_static_ws.
@@ -298,8 +303,9 @@ moe_status_t moe_static_workspace_check(int32_t* device_error, void** workspace,
  * (the only entry point that does).
  *   device_error (out)  0: no failure since the last check; 11-17: a bounded
  *                       wait of the single-token kernel gave up; 1-5: a bounded
- *                       wait of the grouped tensor-core kernels gave up; 20: the
- *                       workspace control block was not zeroed before use.
+ *                       wait of the grouped tensor-core kernels gave up; 6-7:
+ *                       one of the tensor-core router's; 20: the workspace
+ *                       control block was not zeroed before use.
  * Errors: MOE_ERR_NULL, MOE_ERR_ALIGNMENT, MOE_ERR_WORKSPACE (ws_bytes < 256),
  * MOE_ERR_CUDA. */
 moe_status_t moe_workspace_check(void* ws, size_t ws_bytes, int32_t* device_error,

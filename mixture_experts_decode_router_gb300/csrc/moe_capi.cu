@@ -183,16 +183,49 @@ static moe_status_t stage_x(const moe_config_t* c, const void*& x, int32_t n, vo
     return MOE_OK;
 }
 
+// Token counts up to this use the token-major CUDA-core kernels under AUTO
+// (one token: the single-token kernel); above it the grouped tensor-core path.
+// Measured on GB300 at H=2048, E=256, k=8, BF16: grouped is faster from 4
+// tokens on (4: 90 vs 95 us, 8: 128 vs 177 us, 16: 160 vs 279 us), token-major
+// at 2 (63 vs 74 us).
+constexpr int kTokenMajorMaxN = 3;
+
+// The multi-kernel path a call of n tokens takes.
+static int effective_path(const moe_config_t* c, int32_t n) {
+    return c->path == MOE_PATH_AUTO ? (n <= kTokenMajorMaxN ? MOE_PATH_TOKEN_MAJOR : MOE_PATH_GROUPED) : c->path;
+}
+
 // Enqueue router + top-k.  Arguments already validated.  `with_group`: the
 // top-k launch also groups the routes by expert (the fused top-k + grouping
 // kernel), so the expert stage that follows skips its grouping launch.
+// `x_dev`: x is in device memory.  A BF16 router on the grouped path runs on
+// the tensor cores (partial logits per K split, summed in order by the top-k
+// kernel; the shared-gate row keeps the CUDA-core kernel); the token-major
+// path keeps the CUDA-core router, whose arithmetic the single-token kernel
+// repeats, so that a token alone and in a batch route alike.
 static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w, const void* x,
                                   int32_t n, int32_t* idx, float* wt, float* logits, void* ws,
-                                  const WsLayout& L, bool with_group, cudaStream_t st, Marks& mk) {
+                                  const WsLayout& L, bool with_group, bool x_dev, cudaStream_t st, Marks& mk) {
     const int sms = device_sm_count();
     float* lg = logits ? logits : at<float>(ws, L.logits);
+    const float* lin = lg;   // what the top-k kernel reads: logits, or the partials
+    float* lsum = nullptr;   // where it writes summed logits (moe_route's output)
+    int ns = 1;
     cudaError_t e;
-    if (c->router_fmt == MOE_W_NVFP4) {
+    if (c->router_fmt == MOE_W_BF16 && x_dev && effective_path(c, n) == MOE_PATH_GROUPED &&
+        router_tc_fits(n, c->num_experts, c->hidden)) {
+        float* part = at<float>(ws, L.lgp);
+        e = launch_router_tc(static_cast<const uint16_t*>(x), n, c->hidden,
+                             static_cast<const uint16_t*>(w->router_w), c->num_experts, part,
+                             &at<Ctrl>(ws, L.ctrl)->err, st);
+        if (e == cudaSuccess && w->shared_gate_w)
+            e = launch_router(static_cast<const uint16_t*>(x), n, c->hidden, nullptr, 0,
+                              static_cast<const uint16_t*>(w->shared_gate_w), nullptr,
+                              at<float>(ws, L.sg_logit), sms, st);
+        lin = part;
+        ns = router_tc_split(c->hidden).splits;
+        lsum = logits;
+    } else if (c->router_fmt == MOE_W_NVFP4) {
         e = launch_router_nvfp4(static_cast<const uint16_t*>(x), n, c->hidden,
                                 qdev(w->router_q, c->num_experts, c->hidden, 0), c->num_experts, lg, st);
         if (e == cudaSuccess && w->shared_gate_w)   // the BF16 shared-gate row on its own
@@ -208,24 +241,18 @@ static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w,
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     mk.mark(st);
     if (with_group)
-        e = launch_topk_group(lg, n, c->num_experts, c->top_k, c->routing, w->correction_bias, c->norm_topk_prob,
+        e = launch_topk_group(lin, ns, n, c->num_experts, c->top_k, c->routing, w->correction_bias, c->norm_topk_prob,
                               c->routed_scaling_factor, idx, wt, c->expert_begin, c->expert_end,
                               at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm),
                               at<int32_t>(ws, L.inv), at<int32_t>(ws, L.active), at<int32_t>(ws, L.segs),
                               at<Ctrl>(ws, L.ctrl), sms, st);
     else
-        e = launch_topk(lg, n, c->num_experts, c->top_k, c->routing, w->correction_bias,
+        e = launch_topk(lin, ns, lsum, n, c->num_experts, c->top_k, c->routing, w->correction_bias,
                         c->norm_topk_prob, c->routed_scaling_factor, idx, wt, st);
     mk.mark(st);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-// Token counts up to this use the token-major CUDA-core kernels under AUTO
-// (one token: the single-token kernel); above it the grouped tensor-core path.
-// Measured on GB300 at H=2048, E=256, k=8, BF16: grouped is faster from 4
-// tokens on (4: 90 vs 95 us, 8: 128 vs 177 us, 16: 160 vs 279 us), token-major
-// at 2 (63 vs 74 us).
-constexpr int kTokenMajorMaxN = 3;
 
 // The grouped tensor-core expert stage (after the grouping kernel).
 // x: the experts' input (the layer input or its pre-expert RMSNorm).
@@ -327,9 +354,7 @@ static moe_status_t enqueue_experts(const moe_config_t* c, const moe_weights_t* 
         mk.mark(st);
     }
 
-    const int path = (c->path == MOE_PATH_AUTO) ? (n <= kTokenMajorMaxN ? MOE_PATH_TOKEN_MAJOR
-                                                                        : MOE_PATH_GROUPED)
-                                                : c->path;
+    const int path = effective_path(c, n);
     if (path == MOE_PATH_GROUPED)
         return enqueue_grouped(c, w, xin, n, wt, out, ws, L, sg_logit, st, mk);
 
@@ -411,7 +436,7 @@ moe_status_t moe_route(const moe_config_t* cfg_in, const moe_weights_t* wts, con
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (x_res == 1 && n > 1 && (s = stage_x(cfg, x, n, ws, L, st)) != MOE_OK) return s;
     Marks mk;
-    return enqueue_route(cfg, wts, x, n, idx, w, logits, ws, L, false, st, mk);
+    return enqueue_route(cfg, wts, x, n, idx, w, logits, ws, L, false, x_res == 0 || n > 1, st, mk);
 }
 
 moe_status_t moe_experts(const moe_config_t* cfg_in, const moe_weights_t* wts, const void* x, int32_t n,
@@ -517,7 +542,7 @@ static moe_status_t forward_impl(const moe_config_t* cfg_in, const moe_weights_t
         mk.mark(st);
         return enqueue_experts(cfg, wts, x, n, idx_p, w_p, out, ws, L, true, false, st, mk);
     }
-    if ((s = enqueue_route(cfg, wts, x, n, idx_p, w_p, nullptr, ws, L, true, st, mk)) != MOE_OK) return s;
+    if ((s = enqueue_route(cfg, wts, x, n, idx_p, w_p, nullptr, ws, L, true, true, st, mk)) != MOE_OK) return s;
     return enqueue_experts(cfg, wts, x, n, idx_p, w_p, out, ws, L, true, true, st, mk);
 }
 

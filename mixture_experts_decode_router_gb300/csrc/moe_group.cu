@@ -193,7 +193,7 @@ group_kernel(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_
 // route in one wave; 1 otherwise (no register cap).
 template <int kMinBlocks>
 __global__ void __launch_bounds__(kGroupThreads, kMinBlocks)
-topk_group_kernel(const float* __restrict__ logits, int n, int E, int k, int routing,
+topk_group_kernel(const float* __restrict__ logits, int ns, int n, int E, int k, int routing,
                   const float* __restrict__ bias, int norm, float scale, int32_t* idx_out,
                   float* __restrict__ w_out, int e_begin, int e_end, int32_t* __restrict__ counts,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
@@ -210,8 +210,8 @@ topk_group_kernel(const float* __restrict__ logits, int n, int E, int k, int rou
     __shared__ int s_last;
     const int t = blockIdx.x, tid = threadIdx.x;
     pdl_wait();
-    route_token_block(logits + (size_t)t * E, E, k, routing, bias, norm, scale, slg, skey, cand_k, gmax, zg, ssel,
-                      sselw);
+    route_token_block(logits + (size_t)t * E, ns, (size_t)n * E, nullptr, E, k, routing, bias, norm, scale, slg, skey,
+                      cand_k, gmax, zg, ssel, sselw);
     if (tid < k) {
         idx_out[(size_t)t * k + tid] = ssel[tid];
         w_out[(size_t)t * k + tid] = sselw[tid];
@@ -242,7 +242,7 @@ cudaError_t launch_group(const int32_t* idx, int nk, int E, int e_begin, int e_e
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk_group(const float* logits, int n, int E, int k, int routing, const float* bias, int norm,
+cudaError_t launch_topk_group(const float* logits, int ns, int n, int E, int k, int routing, const float* bias, int norm,
                               float scale, int32_t* idx, float* w, int e_begin, int e_end, int32_t* counts,
                               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
                               Ctrl* ctrl, int num_sms, cudaStream_t st) {
@@ -263,7 +263,7 @@ cudaError_t launch_topk_group(const float* logits, int n, int E, int k, int rout
             configured[dev][two] = smem;
         }
     }
-    launch_pdl(kern, n, kGroupThreads, smem, st, logits, n, E, k, routing, bias, norm, scale, idx, w,
+    launch_pdl(kern, n, kGroupThreads, smem, st, logits, ns, n, E, k, routing, bias, norm, scale, idx, w,
                e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, sw);
     return cudaGetLastError();
 }

@@ -32,9 +32,52 @@ struct Ctrl {
 // Tokens per tile of the grouped tensor-core path (its MMA N is at most this).
 constexpr int kTcTokensPerTile = 64;
 
+// Tensor-core router (grouped path): K splits fixed by H alone -- at most
+// kRouterTcMaxSplits splits of a multiple of 64 elements -- so that a token's
+// partial logits do not depend on the batch; token tiles of at most
+// kRouterTcMaxTile rows; partials [splits][n][E] fp32, used while they fit in
+// kRouterTcMaxPartialBytes (larger calls take the CUDA-core router).
+constexpr int kRouterTcMaxSplits = 16;
+constexpr int kRouterTcMaxTile = 128;
+constexpr int64_t kRouterTcMaxPartialBytes = 8ll << 20;
+
+struct RouterTcSplit {
+    int splits;   // K splits
+    int kc;       // K elements per split (a multiple of 64)
+};
+
+inline RouterTcSplit router_tc_split(int H) {
+    RouterTcSplit r;
+    const int boxes = (H + 63) / 64;
+    r.splits = boxes < kRouterTcMaxSplits ? (boxes > 0 ? boxes : 1) : kRouterTcMaxSplits;
+    r.kc = 64 * ((boxes + r.splits - 1) / r.splits);
+    r.splits = (H + r.kc - 1) / r.kc;
+    if (r.splits < 1) r.splits = 1;
+    return r;
+}
+
+// Token tile of a call with n tokens, and the kernel's shared memory for it.
+inline int router_tc_tile(int64_t n) { return n >= kRouterTcMaxTile ? kRouterTcMaxTile : (int)((n + 15) / 16) * 16; }
+inline size_t router_tc_smem(int H, int64_t n) {
+    return (size_t)(router_tc_split(H).kc / 64) * (128 + router_tc_tile(n)) * 128 + 64 + 1024;
+}
+
+// Bytes reserved for the partials (monotone in n, so a workspace sized for
+// max_tokens serves every smaller call).
+inline size_t router_tc_partials_bytes(int64_t n, int64_t E, int H) {
+    const int64_t b = (int64_t)router_tc_split(H).splits * n * E * (int64_t)sizeof(float);
+    return (size_t)(b < kRouterTcMaxPartialBytes ? b : kRouterTcMaxPartialBytes);
+}
+
+// Whether a call of n tokens can take the tensor-core router.
+inline bool router_tc_fits(int64_t n, int64_t E, int H) {
+    const int64_t b = (int64_t)router_tc_split(H).splits * n * E * (int64_t)sizeof(float);
+    return n >= 1 && E >= 1 && H % 8 == 0 && b <= kRouterTcMaxPartialBytes && router_tc_smem(H, n) <= 232448;
+}
+
 struct WsLayout {
     size_t ctrl, logits, sg_logit, idx, w, counts, offsets, perm, active, act, act_sh,
-        inv, segs, xs, xh, as, ash, y, ysh, xe, xd, total;
+        inv, segs, xs, xh, as, ash, y, ysh, xe, xd, lgp, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -73,6 +116,7 @@ inline WsLayout ws_layout(const moe_config_t& c, int64_t n) {
     L.ysh = take(sizeof(float) * n * H);
     L.xe = take(sizeof(uint16_t) * n * H);                       // pre-expert RMSNorm of x
     L.xd = take(sizeof(uint16_t) * n * H);                       // x staged from pinned host memory
+    L.lgp = take(router_tc_partials_bytes(n, E, (int)H));        // tensor-core router partials
     L.total = off;
     return L;
 }
@@ -382,7 +426,11 @@ __device__ __forceinline__ void route_weights_block(const float* slg, int E, int
 // keys (sigmoid routing: sigmoid(l) + bias selects; NaN scores rank last),
 // then route_select_block and route_weights_block.  ssel / sselw receive the
 // k experts and weights.  slg [E] and skey [E + 32] as above.
-__device__ __forceinline__ void route_token_block(const float* __restrict__ lrow, int E, int k, int routing,
+// lrow holds ns partial rows sstride floats apart (the tensor-core router's
+// K splits; ns = 1 for the other routers): the logit is their sum in split
+// order, written to lsum (when not null).
+__device__ __forceinline__ void route_token_block(const float* __restrict__ lrow, int ns, size_t sstride,
+                                                  float* __restrict__ lsum, int E, int k, int routing,
                                                   const float* __restrict__ bias, int norm, float scale,
                                                   float* slg, unsigned long long* skey,
                                                   unsigned long long* cand_k, float* gmax, float* zg, int* ssel,
@@ -390,7 +438,16 @@ __device__ __forceinline__ void route_token_block(const float* __restrict__ lrow
     const int tid = threadIdx.x, nthr = blockDim.x;
     for (int e = tid; e < E + 32; e += nthr) {
         if (e < E) {
-            const float l = lrow[e];
+            float l = lrow[e];
+            for (int q0 = 1; q0 < ns; q0 += 8) {   // eight partials in flight, added in order
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = q0 + u < ns ? lrow[(size_t)(q0 + u) * sstride + e] : 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (q0 + u < ns) l += v[u];
+            }
+            if (lsum) lsum[e] = l;
             float sc;
             if (routing == MOE_ROUTE_SOFTMAX) sc = l;
             else sc = 1.0f / (1.0f + expf(-l)) + bias[e];

@@ -109,14 +109,23 @@ cudaError_t launch_fused_n1(int fmt, const FusedParams& p, int num_sms, cudaStre
 cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, int E,
                           const uint16_t* gw, float* logits, float* sg_logit, int num_sms,
                           cudaStream_t st);
+// Tensor-core router (moe_router_tc.cu): partial logits [splits][n][E] of the
+// BF16 router (rows E) for device-resident x; the caller checked router_tc_fits.
+cudaError_t launch_router_tc(const uint16_t* x, int n, int H, const uint16_t* wr, int E, float* part,
+                             int32_t* err, cudaStream_t st);
+// 2-D TMA map over a row-major [rows, cols] matrix of `esize`-byte elements (moe_grouped_tc.cu).
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t cols,
+              uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle);
 cudaError_t launch_router_nvfp4(const uint16_t* x, int n, int H, const QMatDev& wq, int E, float* logits,
                                 cudaStream_t st);
-cudaError_t launch_topk(const float* logits, int n, int E, int k, int routing, const float* bias,
+// logits: ns partial rows per token ([ns][n][E], ns = 1 for a plain logit
+// matrix), summed in order; lsum (may be null) receives the sums.
+cudaError_t launch_topk(const float* logits, int ns, float* lsum, int n, int E, int k, int routing, const float* bias,
                         int norm, float scale, int32_t* idx, float* w, cudaStream_t st);
 cudaError_t launch_group(const int32_t* idx, int nk, int E, int e_begin, int e_end, int32_t* counts,
                          int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
                          Ctrl* ctrl, cudaStream_t st);
-cudaError_t launch_topk_group(const float* logits, int n, int E, int k, int routing, const float* bias, int norm,
+cudaError_t launch_topk_group(const float* logits, int ns, int n, int E, int k, int routing, const float* bias, int norm,
                               float scale, int32_t* idx, float* w, int e_begin, int e_end, int32_t* counts,
                               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
                               Ctrl* ctrl, int num_sms, cudaStream_t st);

@@ -240,8 +240,8 @@ cudaError_t launch_router_nvfp4(const uint16_t* x, int n, int H, const QMatDev& 
 // route_weights_block (exact ranks, fixed-order softmax normaliser), which the
 // single-token kernel also uses.
 __global__ void __launch_bounds__(256)
-topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int routing,
-                  const float* __restrict__ bias, int norm, float scale,
+topk_block_kernel(const float* __restrict__ logits, int ns, float* __restrict__ lsum, int n, int E, int k,
+                  int routing, const float* __restrict__ bias, int norm, float scale,
                   int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
     extern __shared__ float smf[];
     float* slg = smf;                                                    // [E]
@@ -253,8 +253,8 @@ topk_block_kernel(const float* __restrict__ logits, int n, int E, int k, int rou
     __shared__ float gmax[kMaxExperts / 32], zg[kMaxExperts / 32];
     const int t = blockIdx.x, tid = threadIdx.x;
     pdl_wait();
-    route_token_block(logits + (size_t)t * E, E, k, routing, bias, norm, scale, slg, skey, cand_k, gmax, zg, ssel,
-                      sselw);
+    route_token_block(logits + (size_t)t * E, ns, (size_t)n * E, lsum ? lsum + (size_t)t * E : nullptr, E, k,
+                      routing, bias, norm, scale, slg, skey, cand_k, gmax, zg, ssel, sselw);
     if (tid < k) {
         idx_out[(size_t)t * k + tid] = ssel[tid];
         w_out[(size_t)t * k + tid] = sselw[tid];
@@ -341,11 +341,11 @@ cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, i
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_topk(const float* logits, int n, int E, int k, int routing, const float* bias,
-                        int norm, float scale, int32_t* idx, float* w, cudaStream_t st) {
+cudaError_t launch_topk(const float* logits, int ns, float* lsum, int n, int E, int k, int routing,
+                        const float* bias, int norm, float scale, int32_t* idx, float* w, cudaStream_t st) {
     // Logits and keys: ~12 E + 272 bytes of shared memory (<= 13 KB for E <= 1024).
     const size_t smem = (size_t)((E + 3) & ~3) * sizeof(float) + (size_t)(E + 32) * sizeof(unsigned long long);
-    launch_pdl(topk_block_kernel, n, 256, smem, st, logits, n, E, k, routing, bias, norm, scale, idx, w);
+    launch_pdl(topk_block_kernel, n, 256, smem, st, logits, ns, lsum, n, E, k, routing, bias, norm, scale, idx, w);
     return cudaGetLastError();
 }
 
