@@ -163,6 +163,66 @@ def test_route_and_experts_entry_points(norm, router):
     assert torch.equal(own, fwd)
 
 
+# ---------------------------------------------------------------- the grouped path's tensor-core router
+
+def _route_against_oracle(cfg, n, path="auto"):
+    lw = synth.make_weights(cfg, "cuda")
+    L = oracle_layer(lw)
+    x = synth.make_input(cfg, n, "cuda", gap_fn=gap_fn_for(L))
+    layer = MoeLayer(lw, n, path)
+    idx, w, lg = layer.route(x)
+    torch.cuda.synchronize()
+    lg_ref = O.router_logits(O.bf16_decode(bf16_bits(x)), O.router_weights(L))
+    idx_ref, w_ref = O.route(lg_ref, L.routing, L.top_k, L.norm_topk_prob,
+                             L.routed_scaling_factor, L.correction_bias)
+    rms = float(np.sqrt(np.mean(lg_ref ** 2)))
+    err = float(np.max(np.abs(lg.cpu().numpy() - lg_ref)))
+    assert err <= 1e-4 * rms, f"logits max|err| {err:.3e} vs RMS {rms:.3e}"
+    assert np.array_equal(idx.cpu().numpy(), idx_ref), "expert indices differ"
+    assert np.max(np.abs(w.cpu().numpy() - w_ref)) <= 1e-5 * max(1.0, cfg.routed_scaling_factor)
+    return x, layer, idx, w, lg
+
+
+@pytest.mark.parametrize("n", [4, 16, 129, 300])
+def test_tensor_core_router_logits(n):
+    """moe_route on the grouped path (the tensor-core router: 16 K splits of 128
+    at H = 2048; 129 and 300 tokens span two and three token tiles, the last
+    ragged) against the oracle's fp64 logits and routing."""
+    cfg = dataclasses.replace(synth.WORKLOADS["decode_n16"], name="tc_router")
+    _route_against_oracle(cfg, n)
+
+
+def test_tensor_core_router_wide_splits():
+    """H = 7168: 16 K splits of 448 (seven 64-element boxes each)."""
+    cfg = small("tc_router_7168", hidden=7168, num_experts=64, top_k=4, inter=128, shared_inter=128)
+    _route_against_oracle(cfg, 20)
+
+
+def test_tensor_core_and_cuda_core_routers_agree():
+    """The same tokens routed by the grouped path's tensor-core router and by the
+    token-major path's CUDA-core router: the same experts, logits within the
+    accumulation-order difference."""
+    cfg = small("tc_vs_cc", num_experts=40, top_k=5, routing=synth.ROUTE_SIGMOID_BIAS,
+                routed_scaling_factor=2.5)
+    x, _, idx_g, w_g, lg_g = _route_against_oracle(cfg, 24, path="grouped")
+    lw = synth.make_weights(cfg, "cuda")
+    idx_t, w_t, lg_t = MoeLayer(lw, 24, "token_major").route(x)
+    torch.cuda.synchronize()
+    assert torch.equal(idx_g, idx_t)
+    scale = float(lg_t.abs().max())
+    assert float((lg_g - lg_t).abs().max()) <= 1e-5 * scale
+    assert float((w_g - w_t).abs().max()) <= 1e-5 * cfg.routed_scaling_factor
+
+
+def test_router_partials_over_the_cap_take_the_cuda_core_router():
+    """E = 1024 at 160 tokens: 16 x 160 x 1024 x 4 bytes of partials exceed the
+    8 MiB cap, so the grouped path routes on the CUDA cores; the layer still
+    matches the oracle."""
+    cfg = small("tc_cap", num_experts=1024, top_k=8, hidden=2048, inter=64, shared_inter=64)
+    _route_against_oracle(cfg, 160)
+    _check(cfg, 160)
+
+
 @pytest.mark.parametrize("routing", [synth.ROUTE_SOFTMAX, synth.ROUTE_SIGMOID_BIAS])
 @pytest.mark.parametrize("n", [1, 3, 16])
 def test_exact_ties_go_to_the_lower_index(routing, n):
