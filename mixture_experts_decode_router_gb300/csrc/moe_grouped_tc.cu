@@ -22,13 +22,13 @@
 // tokens (padded to a multiple of 16), so a thin token set still fills the
 // MMA.  Weights: BF16 arrive by TMA straight in the 128-byte swizzled K-major
 // layout the MMA reads from shared memory.  FP8 and NVFP4 arrive raw by TMA
-// and dequant warps (8 for FP8, 16 for NVFP4) write them as f16 into tensor
+// and dequant warps (8; 16 in two sets for FP8 gate/up) write them as f16 into tensor
 // memory, where tcgen05.mma reads its A operand (FP8: RNE_f16(e4m3 * block
 // scale), one rounding with an 11-bit significand; NVFP4: e2m1 * e4m3 scale,
 // exact in f16, with the fp32 scale2 applied to the accumulator).  Those tiles
 // run the f16 MMA with f16 activations (exact for BF16 inputs in f16's normal
 // range, saturated at +-65504).  A pipeline stage covers 64 K (128 K in the
-// NVFP4 down kernel: 64-byte raw rows, like FP8's).  Warp roles: 0 TMA producer of the weight
+// FP8 and NVFP4 down kernels).  Warp roles: 0 TMA producer of the weight
 // codes (and FP8/NVFP4 block scales), 1 MMA issuer (one thread) and TMEM
 // owner, 2-5 epilogue (TMEM -> registers -> global), then the dequant warps,
 // then (dequantised formats) the TMA producer of the token tiles.
@@ -53,11 +53,12 @@ struct TcCfg {
     static constexpr bool kDeq = FMT != MOE_W_BF16;
     static constexpr bool kF16 = FMT != MOE_W_BF16;   // FP8 and NVFP4 tiles: f16 operands
     static constexpr int kMats = GU ? 2 : 1;
-    // K elements per pipeline stage: 64, or 128 for the NVFP4 down kernel,
-    // whose 64-K stages carry only 4 KB of codes for the same handshakes as
-    // gate/up's 8 KB (measured: down 103.7 -> 78.8 us at nvfp4_n256; gate/up
-    // at 128 K, three TMEM operand stages, was slower: 128.2 -> 136.2 us).
-    static constexpr int kBK = (FMT == MOE_W_NVFP4 && !GU) ? 128 : BK;
+    // K elements per pipeline stage: 64, or 128 for the dequantised down
+    // kernels, whose one matrix gives a 64-K stage half the codes of gate/up's
+    // for the same handshakes (measured on GB300: NVFP4 down 103.7 -> 78.8 us
+    // at nvfp4_n256, fp8_n64 1076 -> 1009 us; gate/up at 128 K, three TMEM
+    // operand stages, was slower: NVFP4 128.2 -> 136.2 us).
+    static constexpr int kBK = (kDeq && !GU) ? 128 : BK;
     static constexpr int kAMat = BM * kBK * 2;
     static constexpr int kAStage = kMats * kAMat;
     // Token tiles: kBK / BK boxes of BK columns (one 128-byte swizzle atom each),
@@ -87,11 +88,11 @@ struct TcCfg {
     static constexpr int kASmemStages = kDeq ? 0 : kAStages;
     // Dequantised tiles hand operand stages to the MMA warp in groups (one
     // barrier round trip per group instead of per stage), sizes measured on
-    // GB300: NVFP4 gate/up three of its six 64-K stages, NVFP4 down two of its
-    // six 128-K stages; FP8 gate/up two of six, FP8 down three of twelve
-    // (fp8_n64 1129 -> 1113 us for gate/up pairs, -> 1121 us for down triples;
-    // NVFP4 gate/up pairs were slower, 214 -> 219 us at nvfp4_n256).
-    static constexpr int kGrp = !kDeq ? 1 : (FMT == MOE_W_NVFP4 ? (GU ? 3 : 2) : (GU ? 2 : 3));
+    // GB300: NVFP4 gate/up three of its six 64-K stages, FP8 gate/up two of
+    // six (fp8_n64 1129 -> 1113 us against three), both down kernels pairs of
+    // their six 128-K stages (FP8 triples: 1065 against 1009 us; NVFP4
+    // gate/up pairs were slower, 214 -> 219 us at nvfp4_n256).
+    static constexpr int kGrp = !kDeq ? 1 : ((FMT == MOE_W_NVFP4 && GU) ? 3 : 2);
     static constexpr int kAGroups = kAStages / kGrp;
     // Dequantised tiles: the token (B) tiles have a ring of their own, so they
     // are fetched ahead instead of after the MMA frees an A slot.  It holds
@@ -99,9 +100,9 @@ struct TcCfg {
     // group, so the MMA warp waits and commits once per group, not per stage.
     static constexpr int kBGroups = kDeq ? 2 : 1;   // (BF16: no token ring of its own)
     static constexpr int kBStages = kDeq ? kBGroups * kGrp : kAStages;
-    // Raw stages: FP8 10 / 16, NVFP4 16 (gate/up, 64 K) and 12 (down, 128 K: the
-    // bytes of 24 stages of 64 K).
-    static constexpr int kRawStages = !kDeq ? 0 : (GU ? (FMT == MOE_W_FP8_B128 ? 10 : 16) : (FMT == MOE_W_FP8_B128 ? 16 : 12));
+    // Raw stages: FP8 gate/up 10 of 16 KB (64 K), FP8 down 8 of 16 KB (128 K),
+    // NVFP4 gate/up 16 of 8 KB (64 K), NVFP4 down 12 of 8 KB (128 K).
+    static constexpr int kRawStages = !kDeq ? 0 : (GU ? (FMT == MOE_W_FP8_B128 ? 10 : 16) : (FMT == MOE_W_FP8_B128 ? 8 : 12));
     // Dequant warps: kDeqSets sets of 8 (two per TMEM lane quarter); set s
     // converts the stages with stage counter = s (mod kDeqSets), so a set's
     // warps overlap their per-stage chains with the other set's while every
@@ -267,13 +268,16 @@ __device__ __forceinline__ float2 f16x2_to_float2(uint32_t h2) {
 
 // Byte offset of 16-byte chunk c of row r in a raw stage of kRawRow-byte rows.
 // The TMA writes the raw codes swizzled, the row's chunk index XORed with
-// address bits 7 and up (64-byte rows -- FP8's 64 codes, the NVFP4 down
-// kernel's 128 -- with the 64-byte swizzle: c ^ ((r >> 1) & 3); NVFP4 gate/up's
-// 32-byte rows with the 32-byte swizzle: c ^ ((r >> 2) & 1)), so that 32 lanes
-// reading one chunk of 32 consecutive rows spread over all banks.
+// address bits 7 and up: 128-byte rows (the FP8 down kernel's 128 codes) with
+// the 128-byte swizzle, c ^ (r & 7); 64-byte rows (FP8 gate/up's 64 codes,
+// the NVFP4 down kernel's 128) with the 64-byte swizzle, c ^ ((r >> 1) & 3);
+// NVFP4 gate/up's 32-byte rows with the 32-byte swizzle, c ^ ((r >> 2) & 1).
+// So each 8-lane phase of 32 lanes reading one chunk of 32 consecutive rows
+// touches 8 distinct 16-byte bank groups.
 template <int kRawRow>
 __device__ __forceinline__ int raw_chunk(int r, int c) {
-    if constexpr (kRawRow == 64) return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+    if constexpr (kRawRow == 128) return r * 128 + ((c ^ (r & 7)) << 4);
+    else if constexpr (kRawRow == 64) return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
     else return r * 32 + ((c ^ ((r >> 2) & 1)) << 4);
 }
 
@@ -784,8 +788,10 @@ bool weight_map(CUtensorMap* m, int fmt, const void* w, int rows_total, int in_d
         return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, in_dim, rows_total, BK, BM,
                         CU_TENSOR_MAP_SWIZZLE_128B);
     if (fmt == MOE_W_FP8_B128)
-        return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim, rows_total, BK, BM,
-                        CU_TENSOR_MAP_SWIZZLE_64B);
+        return gate_up ? make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim, rows_total,
+                                  TcCfg<MOE_W_FP8_B128, true>::kBK, BM, CU_TENSOR_MAP_SWIZZLE_64B)
+                       : make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim, rows_total,
+                                  TcCfg<MOE_W_FP8_B128, false>::kBK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (gate_up)
         return make_map(m, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, in_dim / 2, rows_total,
                         TcCfg<MOE_W_NVFP4, true>::kBK / 2, BM, CU_TENSOR_MAP_SWIZZLE_32B);
