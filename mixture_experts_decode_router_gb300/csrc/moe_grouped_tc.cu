@@ -106,11 +106,12 @@ struct TcCfg {
     // Dequant warps: kDeqSets sets of 8 (two per TMEM lane quarter); set s
     // converts the stages with stage counter = s (mod kDeqSets), so a set's
     // warps overlap their per-stage chains with the other set's while every
-    // stage still has 8 handshakes.  Measured on GB300: FP8 gate/up two sets
-    // (fp8_n64 gate/up 668 -> 638 us; its down kernel was slower with two,
-    // 405 -> 418 us), NVFP4 one (two: nvfp4_n256 207.4 -> 211.3 us; 16 warps
-    // each converting a quarter of every stage: 213.7 -> 219.5).
-    static constexpr int kDeqSets = !kDeq ? 0 : ((FMT == MOE_W_FP8_B128 && GU) ? 2 : 1);
+    // stage still has 8 handshakes.  Measured on GB300: FP8 two sets (gate/up
+    // 668 -> 638 us at fp8_n64; the down kernel at 128-K stages 1009.7 ->
+    // 992.7 us for the layer), NVFP4 one (two: nvfp4_n256 207.4 -> 211.3 us
+    // for both kernels, no change for down alone; 16 warps each converting a
+    // quarter of every stage: 213.7 -> 219.5).
+    static constexpr int kDeqSets = !kDeq ? 0 : (FMT == MOE_W_FP8_B128 ? 2 : 1);
     static constexpr int kSetWarps = 8;
     static constexpr int kDeqWarps = kDeqSets * kSetWarps;
     // Dequant work split: warp 6 + dw serves TMEM lane quarter (6 + dw) & 3 (the
