@@ -215,13 +215,16 @@ topk_group_kernel(const float* __restrict__ logits, int ns, int n, int E, int k,
     if (tid < k) {
         idx_out[(size_t)t * k + tid] = ssel[tid];
         w_out[(size_t)t * k + tid] = sselw[tid];
-        __threadfence();
     }
+    // Release: the barrier orders the block's writes before thread 0's fence,
+    // which is cumulative over them, then the count.  The block that counts
+    // last takes an acquire fence before it reads every block's routes.
     __syncthreads();
     if (tid == 0) {
+        __threadfence();
         const int done = atomicAdd(&ctrl->routed, 1);
         s_last = done == n - 1;
-        __threadfence();
+        if (s_last) __threadfence();
     }
     __syncthreads();
     if (s_last) {

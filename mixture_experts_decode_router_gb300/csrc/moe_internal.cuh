@@ -438,14 +438,17 @@ __device__ __forceinline__ void route_token_block(const float* __restrict__ lrow
     const int tid = threadIdx.x, nthr = blockDim.x;
     for (int e = tid; e < E + 32; e += nthr) {
         if (e < E) {
-            float l = lrow[e];
-            for (int q0 = 1; q0 < ns; q0 += 8) {   // eight partials in flight, added in order
-                float v[8];
+            float l;
+            if (ns == 1) {
+                l = lrow[e];
+            } else {   // all partials (ns <= kRouterTcMaxSplits) in flight, added in order
+                float v[kRouterTcMaxSplits];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) v[u] = q0 + u < ns ? lrow[(size_t)(q0 + u) * sstride + e] : 0.f;
+                for (int u = 0; u < kRouterTcMaxSplits; ++u) v[u] = u < ns ? lrow[(size_t)u * sstride + e] : 0.f;
+                l = v[0];
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (q0 + u < ns) l += v[u];
+                for (int u = 1; u < kRouterTcMaxSplits; ++u)
+                    if (u < ns) l += v[u];
             }
             if (lsum) lsum[e] = l;
             float sc;
