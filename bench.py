@@ -40,6 +40,7 @@ ALL_WORKLOADS = ("tiny_n1", "decode_n1", "decode_n16", "fp8_n64", "nvfp4_n256")
 STAGES_BY_MARKS = {
     2: ["fused"],
     5: ["router", "topk_group", "gate_up", "down_blend"],
+    6: ["router", "topk_group", "gather", "gate_up", "down_combine"],
     7: ["router", "topk_group", "gather", "gate_up", "down", "combine"],
 }
 
@@ -386,11 +387,14 @@ def stage_alg_bytes(cfg, n, distinct, touched, nm, has_bias):
         + nk * 4 + 4 * (3 * E + 1) + nk * 4,
         # token-major: fp32 activations; grouped: 16-bit activations
         "gate_up": w_gu + n * H * 2 + (4 if nm == 5 else 2) * (nk * I + n * S)
-        + (2 * (nk * H + n * H) if nm == 7 else 0),
+        + (2 * (nk * H + n * H) if nm in (6, 7) else 0),
         "down_blend": w_dn + 4 * (nk * I + n * S) + n * H * 2 + nk * 8,
         "gather": 2 * 2 * (nk * H + n * H),
         "down": w_dn + 2 * (nk * I + n * S) + 4 * (nk * H + (n * H if S else 0)),
         "combine": 4 * (nk * H + (n * H if S else 0)) + n * H * 2 + nk * 4,
+        # the down kernel with the combine folded in: weights and activations in,
+        # the BF16 output and the route positions (its fp32 rows stay internal)
+        "down_combine": w_dn + 2 * (nk * I + n * S) + n * H * 2 + nk * 4,
     }
 
 

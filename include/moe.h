@@ -289,7 +289,7 @@ moe_status_t moe_forward_static_ws(const moe_config_t* cfg, const moe_weights_t*
  * Reads, then clears, the array's device error word and resets its
  * single-token barrier word, so the next static call runs; synchronises
  * `stream`.
- *   device_error (out)  as moe_workspace_check: 0, 11-17, 1-7 or 20.
+ *   device_error (out)  as moe_workspace_check: 0, 11-17, 1-8 or 20.
  *   workspace    (out, optional) the array's device address on this device
  *                (NULL = not returned); the library owns it.
  * The first use on a device runs the set-up of moe_forward_static_ws.
@@ -298,14 +298,20 @@ moe_status_t moe_forward_static_ws(const moe_config_t* cfg, const moe_weights_t*
 moe_status_t moe_static_workspace_check(int32_t* device_error, void** workspace, moe_stream_t stream);
 
 /* Reads, then clears, the device error word of a workspace, and resets the
- * single-token kernel's barrier word (which a call that ended early leaves
- * non-zero), so the workspace serves the next call.  Synchronises `stream`
- * (the only entry point that does).
+ * single-token kernel's and the grouped down kernel's barrier words (which a
+ * call that ended early leaves non-zero) and the routed-token count, so the
+ * workspace serves the next call.  Synchronises `stream` (the only entry
+ * point that does).
  *   device_error (out)  0: no failure since the last check; 11-17: a bounded
  *                       wait of the single-token kernel gave up; 1-5: a bounded
- *                       wait of the grouped tensor-core kernels gave up; 6-7:
+ *                       wait of the grouped tensor-core kernels gave up (8: the
+ *                       down kernel's grid barrier before its combine); 6-7:
  *                       one of the tensor-core router's; 20: the workspace
- *                       control block was not zeroed before use.
+ *                       control block was not zeroed before use.  An FP8
+ *                       call on the grouped path made while an error is
+ *                       pending does not write out (its down kernel, which
+ *                       also combines, skips the combine); check (and so
+ *                       clear) after a failure.
  * Errors: MOE_ERR_NULL, MOE_ERR_ALIGNMENT, MOE_ERR_WORKSPACE (ws_bytes < 256),
  * MOE_ERR_CUDA. */
 moe_status_t moe_workspace_check(void* ws, size_t ws_bytes, int32_t* device_error,

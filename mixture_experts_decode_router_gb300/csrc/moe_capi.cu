@@ -307,13 +307,28 @@ static moe_status_t enqueue_grouped(const moe_config_t* c, const moe_weights_t* 
     p.sh_scale[0] = p.sh_scale[1] = w->sh_down.scale;
     p.scale2[0] = p.scale2[1] = w->down.scale2;
     p.sh_scale2[0] = p.sh_scale2[1] = w->sh_down.scale2;
+    // The FP8 down kernel also runs the combine, after a grid barrier on its
+    // persistent blocks (fp8_n64 992 -> 983 us on GB300).  The BF16 and NVFP4
+    // down kernels have 192 and 480 threads a block against FP8's 736, too
+    // few for the latency-bound combine (decode_n16 128.7 -> 131.3 us,
+    // nvfp4_n256 196.8 -> 198.2 us with it), so theirs runs on its own, as
+    // it does when there are no tiles.
+    p.combine = (tiles && fmt == MOE_W_FP8_B128) ? 1 : 0;
+    p.inv = at<int32_t>(ws, L.inv);
+    p.out = static_cast<uint16_t*>(out);
+    p.has_shared = S > 0 ? 1 : 0;
+    p.accumulate = c->accumulate;
+    p.tc_count = &at<Ctrl>(ws, L.ctrl)->tc_count;
+    p.tc_gen = &at<Ctrl>(ws, L.ctrl)->tc_gen;
     if (tiles && (e = launch_grouped_tc(fmt, false, maps, p, sms, st)) != cudaSuccess) return MOE_ERR_CUDA;
     mk.mark(st);
 
-    e = launch_combine(p.y, p.y_sh, at<int32_t>(ws, L.inv), n, H, k, S > 0 ? 1 : 0, c->accumulate,
-                       static_cast<uint16_t*>(out), sms, st);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    mk.mark(st);
+    if (!p.combine) {
+        e = launch_combine(p.y, p.y_sh, p.inv, n, H, k, S > 0 ? 1 : 0, c->accumulate, static_cast<uint16_t*>(out),
+                           sms, st);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        mk.mark(st);
+    }
     return MOE_OK;
 }
 
@@ -576,7 +591,8 @@ moe_status_t moe_workspace_check(void* ws, size_t ws_bytes, int32_t* device_erro
     if (cudaMemcpyAsync(&v, &c->err, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
     // Clear the error word and the single-token kernel's barrier word (left
     // non-zero when a call ends early), so the workspace serves the next call.
-    if (cudaMemsetAsync(&c->err, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+    // err, gbar, routed and tc_count (adjacent): zero between calls.
+    if (cudaMemsetAsync(&c->err, 0, 4 * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
     *device_error = v;
     return MOE_OK;

@@ -9,11 +9,6 @@ namespace moe {
 
 namespace {
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
-
 // xs[p, :] = x[perm[p] / k, :] for the grouped routes, and xh = x (the shared
 // expert's operand); 16-bit values as the tiles take them (F16: f16 for the FP8
 // and NVFP4 tiles, else bf16).  The tensor-core kernels' TMA copies therefore
@@ -72,43 +67,14 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
     pdl_trigger();
 }
 
-// out[t, h] = bf16( sum_j y[inv[t*k + j], h] (slot order) + y_sh[t, h] ).
-// The slots' positions and rows are loaded kU at a time before they are
-// summed (one round of load latency per kU slots); the sum keeps slot order.
+// out[t, h] = bf16( sum_j y[inv[t*k + j], h] (slot order) + y_sh[t, h] ), for
+// calls whose down kernel does not run the combine itself.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ ysh,
                                                       const int32_t* __restrict__ inv, int n, int H, int k,
                                                       int has_shared, int accumulate, uint16_t* __restrict__ out) {
-    constexpr int kU = 8;
     pdl_wait();
-    const int C4 = H >> 2;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)n * C4;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int t = (int)(i / C4), c = (int)(i - (int64_t)t * C4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j0 = 0; j0 < k; j0 += kU) {
-            int pos[kU];
-#pragma unroll
-            for (int u = 0; u < kU; ++u) pos[u] = (j0 + u < k) ? __ldg(inv + t * k + j0 + u) : -1;
-            float4 v[kU];
-#pragma unroll
-            for (int u = 0; u < kU; ++u)
-                if (pos[u] >= 0) v[u] = __ldg(reinterpret_cast<const float4*>(y + (size_t)pos[u] * H) + c);
-#pragma unroll
-            for (int u = 0; u < kU; ++u)
-                if (pos[u] >= 0) { acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w; }
-        }
-        if (has_shared) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(ysh + (size_t)t * H) + c);
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-        }
-        if (accumulate) {
-            const uint2 o = reinterpret_cast<const uint2*>(out + (size_t)t * H)[c];
-            acc.x += __uint_as_float(o.x << 16); acc.y += __uint_as_float(o.x & 0xffff0000u);
-            acc.z += __uint_as_float(o.y << 16); acc.w += __uint_as_float(o.y & 0xffff0000u);
-        }
-        const uint32_t lo = pack_bf16(acc.x, acc.y), hi = pack_bf16(acc.z, acc.w);
-        reinterpret_cast<uint2*>(out + (size_t)t * H)[c] = make_uint2(lo, hi);
-    }
+    combine_range<false>(y, ysh, inv, n, H, k, has_shared, accumulate, out,
+                         blockIdx.x * (int64_t)blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
     pdl_trigger();
 }
 

@@ -334,6 +334,16 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     ptx::tc_fence_after();
     const uint32_t tmem = *s_tmem;
     pdl_wait();
+    // Down kernel with the combine: whether this block takes part (no device
+    // error pending from an earlier call), and the generation of the grid
+    // barrier before the combine, read before this block arrives (it advances
+    // only after every block's arrival, this one's included).
+    volatile int* s_comb = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+    volatile uint32_t* s_gen = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 12);
+    if (!GU && threadIdx.x == 0 && p.combine) {
+        *s_comb = ptx::ld_relaxed_gpu(reinterpret_cast<const uint32_t*>(p.err)) == 0u ? 1 : 0;
+        *s_gen = ptx::ld_relaxed_gpu(p.tc_gen);
+    }
 
     const int n_rsegs = p.ctrl->n_rsegs;
     // The shared expert's token segments: NT rows, or NT / 2 with one
@@ -769,6 +779,39 @@ grouped_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
     }
 
+    if constexpr (!GU) {
+        if (p.combine) {
+            // Grid barrier: every block's y / y_sh rows are written before any
+            // block combines.  The block's writes are ordered before thread 0's
+            // fence by the barrier; the last arrival zeroes the count for the
+            // next call and publishes the next generation; the others wait
+            // (bounded) for it.
+            __syncthreads();
+            if (threadIdx.x == 0 && *s_comb) {
+                __threadfence();
+                const uint32_t g0 = *s_gen;
+                if (atomicAdd(p.tc_count, 1u) == gridDim.x - 1) {
+                    atomicExch(p.tc_count, 0u);
+                    __threadfence();
+                    ptx::st_release_gpu(p.tc_gen, g0 + 1u);
+                } else {
+                    const uint64_t t0 = ptx::globaltimer();
+                    while (ptx::ld_acquire_gpu(p.tc_gen) == g0) {
+                        if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+                            atomicExch(p.err, 8);
+                            *s_comb = 0;
+                            break;
+                        }
+                    }
+                }
+                __threadfence();
+            }
+            __syncthreads();
+            if (*s_comb)
+                combine_range<true>(p.y, p.y_sh, p.inv, p.n, p.out_dim, p.k, p.has_shared, p.accumulate, p.out,
+                                    blockIdx.x * (int64_t)blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
+        }
+    }
     pdl_trigger();
     ptx::tc_fence_before();
     __syncthreads();

@@ -26,7 +26,9 @@ struct Ctrl {
     int32_t err;           // sticky device error code (bounded waits that gave up); 0 = none
     uint32_t gbar;         // grid-barrier arrivals of the single-token kernel (0 between calls)
     int32_t routed;        // tokens routed so far by the fused top-k + grouping kernel (0 between calls)
-    int32_t pad[59];
+    uint32_t tc_count;     // grid-barrier arrivals of the grouped down kernel before its combine (0 between calls)
+    uint32_t tc_gen;       // that barrier's generation (advanced by the last arrival)
+    int32_t pad[57];
 };
 
 // Tokens per tile of the grouped tensor-core path (its MMA N is at most this).
@@ -465,6 +467,52 @@ __device__ __forceinline__ void route_token_block(const float* __restrict__ lrow
     route_select_block(slg, skey, E, k, routing, tid, nthr, cand_k, gmax, ssel, [] { __syncthreads(); });
     route_weights_block(slg, E, k, routing, norm, scale, tid, nthr, gmax, zg, ssel, sselw,
                         [] { __syncthreads(); });
+}
+
+// The combine (the blend step), elements [i0, n*H/4) in steps of `step`
+// float4s: out[t, h] = BF16(sum_j y[inv[t*k + j], h] in slot order, then
+// + y_sh[t, h], then + out[t, h] when accumulating).  kL2: y and y_sh were
+// written by other blocks of the same kernel, so they are read through L2,
+// not the read-only path.
+template <bool kL2>
+__device__ __forceinline__ void combine_range(const float* __restrict__ y, const float* __restrict__ ysh,
+                                              const int32_t* __restrict__ inv, int n, int H, int k,
+                                              int has_shared, int accumulate, uint16_t* __restrict__ out,
+                                              int64_t i0, int64_t step) {
+    constexpr int kU = 8;
+    auto ld4 = [](const float* p) -> float4 {
+        if constexpr (kL2) return __ldcg(reinterpret_cast<const float4*>(p));
+        else return __ldg(reinterpret_cast<const float4*>(p));
+    };
+    const int C4 = H >> 2;
+    for (int64_t i = i0; i < (int64_t)n * C4; i += step) {
+        const int t = (int)(i / C4), c = (int)(i - (int64_t)t * C4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j0 = 0; j0 < k; j0 += kU) {
+            int pos[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) pos[u] = (j0 + u < k) ? __ldg(inv + t * k + j0 + u) : -1;
+            float4 v[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                if (pos[u] >= 0) v[u] = ld4(y + (size_t)pos[u] * H + 4 * c);
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                if (pos[u] >= 0) { acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w; }
+        }
+        if (has_shared) {
+            const float4 v = ld4(ysh + (size_t)t * H + 4 * c);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        if (accumulate) {
+            const uint2 o = reinterpret_cast<const uint2*>(out + (size_t)t * H)[c];
+            acc.x += __uint_as_float(o.x << 16); acc.y += __uint_as_float(o.x & 0xffff0000u);
+            acc.z += __uint_as_float(o.y << 16); acc.w += __uint_as_float(o.y & 0xffff0000u);
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        reinterpret_cast<uint2*>(out + (size_t)t * H)[c] =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    }
 }
 
 // 1 / sqrt(mean(x^2) + eps) of one BF16 row of H elements, by one warp: lane l

@@ -62,6 +62,14 @@ struct TcParams {
     const float* sg_logit;   // shared gate logits or NULL
     int32_t* err;            // Ctrl::err
     const void* zero4;       // 4 zero bytes (stand-in scale source past the last row)
+    // Down kernel only: after every tile, a grid barrier and the combine
+    // (out = BF16(sum_j y[inv[t*k + j]] in slot order + y_sh[t] (+ out))).
+    int combine;             // 0: the combine runs as a kernel of its own
+    const int32_t* inv;      // route id -> sorted position (-1: dropped)
+    uint16_t* out;           // [n, H] BF16 (device or mapped pinned host memory)
+    int has_shared, accumulate;
+    uint32_t* tc_count;      // Ctrl::tc_count
+    uint32_t* tc_gen;        // Ctrl::tc_gen
 };
 
 bool build_tc_maps(int fmt, bool gate_up, const moe_weights_t* w, int E, int H, int I, int S, int n,

@@ -558,6 +558,32 @@ def test_workspace_check_clean_after_calls():
     assert int(layer.ws[12:20].count_nonzero()) == 0
 
 
+def test_fp8_grouped_combine_waits_for_a_cleared_error():
+    """The FP8 grouped path's down kernel also runs the combine, after a grid
+    barrier.  With a device error pending (a failed earlier call may have left
+    the barrier's count dirty) it does not combine: out is left unwritten, the
+    check reports the error and clears the control block, and the next call
+    matches the first bit for bit."""
+    cfg = small("fp8_pending", expert_fmt=synth.FMT_FP8_B128, num_experts=32, top_k=4)
+    lw = synth.make_weights(cfg, "cuda")
+    L = oracle_layer(lw)
+    x = synth.make_input(cfg, 40, "cuda", gap_fn=gap_fn_for(L))
+    layer = MoeLayer(lw, 40)
+    good, _, _ = layer.forward(x)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    layer.ws[8:12] = torch.tensor([5, 0, 0, 0], dtype=torch.uint8, device="cuda")   # Ctrl::err = 5
+    sentinel = torch.full_like(good, 7)
+    out, _, _ = layer.forward(x, out=sentinel.clone())
+    torch.cuda.synchronize()
+    assert torch.equal(out, sentinel)          # not combined: nothing written
+    assert layer.device_error() == 5           # reported, and cleared
+    again, _, _ = layer.forward(x)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.equal(again, good)
+
+
 def test_single_token_kernel_refuses_a_dirty_control_block():
     cfg = small("dirty", num_experts=32, top_k=4)
     lw = synth.make_weights(cfg, "cuda")
