@@ -419,13 +419,12 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                 // Phase 2a: each lane's partial dot product of every (slot, row) of
                 // this CTA -- slot j < k a routed expert, slot k the shared one --
                 // with the token-major kernel's chunk order.  The (slot, row) pairs
-                // are split evenly over the warps in slot-major order; a warp keeps
-                // a slot's activation chunk in registers across its rows.
+                // are split evenly over the warps in slot-major order; a warp walks
+                // exactly its rows.
                 float* spart = reinterpret_cast<float*>(sm + p.off_part);   // [J][rpc][32]
                 const int J = k + (S > 0 ? 1 : 0);
                 const int P = J * nrows;
                 const int q1 = (int)((int64_t)P * (warp + 1) / kFComputeWarps);
-                constexpr int kPR = 16;                                      // rows per pass
                 for (int q = (int)((int64_t)P * warp / kFComputeWarps); q < q1;) {
                     const int j = q / nrows, rb0 = q - j * nrows;
                     const int nr = min(q1 - q, nrows - rb0);   // this warp's rows of slot j
@@ -438,33 +437,51 @@ __global__ void __launch_bounds__(kFThreads, 1) fused_n1_kernel(const FusedParam
                     const float* a = sact + (size_t)j * I;
                     const uint8_t* base = sdown + (size_t)j * rpc * p.drow_bytes;
                     const uint32_t rb = shj ? p.dsh_row_bytes : p.drow_bytes;
-                    for (int r0 = rb0; r0 < rb0 + nr; r0 += kPR) {
-                        const int rn = min(kPR, rb0 + nr - r0);
-                        float part[kPR];
-#pragma unroll
-                        for (int i = 0; i < kPR; ++i) part[i] = 0.f;
-#pragma unroll 2
-                        for (int c = lane; c < (K >> 3); c += 32) {
-                            float av[8];
-                            const float4 a0 = reinterpret_cast<const float4*>(a)[2 * c];
-                            const float4 a1 = reinterpret_cast<const float4*>(a)[2 * c + 1];
-                            av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
-                            av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
-#pragma unroll
-                            for (int i = 0; i < kPR; ++i) {
-                                if (i < rn) {
-                                    const int r = r0 + i;
-                                    float wv[8];
-                                    decode_at<FMT>(base + (size_t)r * rb, c, wv);
-                                    WChunk<FMT> sch;
-                                    const float cs = sch.scale(M, e, h0 + r, c);
-                                    part[i] = fmaf(dot8(wv, av), cs, part[i]);
-                                }
-                            }
+                    const int C8 = K >> 3;
+                    auto load_act = [&](int c, float (&av)[8]) {
+                        const float4 a0 = reinterpret_cast<const float4*>(a)[2 * c];
+                        const float4 a1 = reinterpret_cast<const float4*>(a)[2 * c + 1];
+                        av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
+                        av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
+                    };
+                    auto term = [&](int r, int c, const float (&av)[8], float acc) {
+                        float wv[8];
+                        decode_at<FMT>(base + (size_t)r * rb, c, wv);
+                        WChunk<FMT> sch;
+                        return fmaf(dot8(wv, av), sch.scale(M, e, h0 + r, c), acc);
+                    };
+                    if (C8 <= 64) {
+                        // At most two chunks a lane (c = lane, lane + 32): the slot's
+                        // activation chunks stay in registers across its rows, and
+                        // rows go two at a time (independent chains).
+                        const bool two = lane + 32 < C8, one = lane < C8;
+                        float av0[8], av1[8];
+                        if (one) load_act(lane, av0);
+                        if (two) load_act(lane + 32, av1);
+                        int r = rb0;
+                        for (; r + 1 < rb0 + nr; r += 2) {
+                            float p0 = 0.f, p1 = 0.f;
+                            if (one) { p0 = term(r, lane, av0, p0); p1 = term(r + 1, lane, av0, p1); }
+                            if (two) { p0 = term(r, lane + 32, av1, p0); p1 = term(r + 1, lane + 32, av1, p1); }
+                            spart[((size_t)j * rpc + r) * 32 + lane] = p0;
+                            spart[((size_t)j * rpc + r + 1) * 32 + lane] = p1;
                         }
-#pragma unroll
-                        for (int i = 0; i < kPR; ++i)
-                            if (i < rn) spart[((size_t)j * rpc + r0 + i) * 32 + lane] = part[i];
+                        if (r < rb0 + nr) {
+                            float p0 = 0.f;
+                            if (one) p0 = term(r, lane, av0, p0);
+                            if (two) p0 = term(r, lane + 32, av1, p0);
+                            spart[((size_t)j * rpc + r) * 32 + lane] = p0;
+                        }
+                    } else {
+                        for (int r = rb0; r < rb0 + nr; ++r) {
+                            float part = 0.f;
+                            for (int c = lane; c < C8; c += 32) {
+                                float av[8];
+                                load_act(c, av);
+                                part = term(r, c, av, part);
+                            }
+                            spart[((size_t)j * rpc + r) * 32 + lane] = part;
+                        }
                     }
                 }
                 ptx::named_bar(1, kFCompute);
