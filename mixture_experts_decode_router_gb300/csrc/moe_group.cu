@@ -37,52 +37,16 @@ inline int seg_warps(int E, int nk) {
     return std::min(cap, std::max(8, nk / 64));
 }
 
-// The grouping of all n*k routes by one block of kGroupThreads threads, sw of
-// whose warps own route segments.  sm: (sw + 1) * E ints of shared memory.
-__device__ __forceinline__ void group_block(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_end,
-                                            int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                                            int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-                                            int32_t* __restrict__ active, int32_t* __restrict__ segs,
-                                            Ctrl* __restrict__ ctrl, int32_t* sm, int sw) {
-    int32_t* cnt = sm;                           // [sw][E]
-    int32_t* tot = sm + sw * E;                  // [E]
+// From tot[e] = routes of expert e (e < E <= blockDim.x): counts, offsets,
+// active, segs and the control block's totals; tot[e] becomes the first sorted
+// position of expert e.  Called by every thread of the block; ends with a
+// barrier.
+__device__ __forceinline__ void group_scan_experts(int32_t* tot, int E, int32_t* __restrict__ counts,
+                                                   int32_t* __restrict__ offsets, int32_t* __restrict__ active,
+                                                   int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl) {
     __shared__ int32_t warp_sums[3][32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    for (int i = tid; i < sw * E; i += blockDim.x) cnt[i] = 0;
-    __syncthreads();
-
-    const int seg = (nk + sw - 1) / sw;
-    if (warp < sw) {
-        const int b = warp * seg, e_ = min(nk, b + seg);
-        for (int r0 = b; r0 < e_; r0 += 32 * kIdxBatch) {
-            int ev[kIdxBatch];   // L2 (__ldcg): the fused kernel's other blocks wrote idx
-#pragma unroll
-            for (int u = 0; u < kIdxBatch; ++u) {
-                const int r = r0 + 32 * u + lane;
-                ev[u] = r < e_ ? __ldcg(idx + r) : -1;
-            }
-#pragma unroll
-            for (int u = 0; u < kIdxBatch; ++u)
-                if (r0 + 32 * u + lane < e_ && ev[u] >= e_begin && ev[u] < e_end)
-                    atomicAdd(&cnt[warp * E + ev[u]], 1);   // not held here: dropped
-        }
-    }
-    __syncthreads();
-
-    // Per expert: exclusive scan over the segment warps, and the total.
-    for (int e = tid; e < E; e += blockDim.x) {
-        int run = 0;
-        for (int w = 0; w < sw; ++w) {
-            const int c = cnt[w * E + e];
-            cnt[w * E + e] = run;
-            run += c;
-        }
-        tot[e] = run;
-    }
-    __syncthreads();
-
-    // Exclusive scans over experts (E <= 1024 = one element per thread):
+    // Exclusive scans over experts (one element per thread):
     // offsets (of counts), active positions (of counts > 0) and segment starts
     // (of ceil(counts / kTcTokensPerTile)).
     const int c = (tid < E) ? tot[tid] : 0;
@@ -136,6 +100,53 @@ __device__ __forceinline__ void group_block(const int32_t* __restrict__ idx, int
         ctrl->n_rsegs = warp_sums[2][31];
     }
     __syncthreads();
+}
+
+// The grouping of all n*k routes by one block of kGroupThreads threads, sw of
+// whose warps own route segments.  sm: (sw + 1) * E ints of shared memory.
+__device__ __forceinline__ void group_block(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_end,
+                                            int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                            int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                                            int32_t* __restrict__ active, int32_t* __restrict__ segs,
+                                            Ctrl* __restrict__ ctrl, int32_t* sm, int sw) {
+    int32_t* cnt = sm;                           // [sw][E]
+    int32_t* tot = sm + sw * E;                  // [E]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    for (int i = tid; i < sw * E; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+
+    const int seg = (nk + sw - 1) / sw;
+    if (warp < sw) {
+        const int b = warp * seg, e_ = min(nk, b + seg);
+        for (int r0 = b; r0 < e_; r0 += 32 * kIdxBatch) {
+            int ev[kIdxBatch];   // L2 (__ldcg): the fused kernel's other blocks wrote idx
+#pragma unroll
+            for (int u = 0; u < kIdxBatch; ++u) {
+                const int r = r0 + 32 * u + lane;
+                ev[u] = r < e_ ? __ldcg(idx + r) : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < kIdxBatch; ++u)
+                if (r0 + 32 * u + lane < e_ && ev[u] >= e_begin && ev[u] < e_end)
+                    atomicAdd(&cnt[warp * E + ev[u]], 1);   // not held here: dropped
+        }
+    }
+    __syncthreads();
+
+    // Per expert: exclusive scan over the segment warps, and the total.
+    for (int e = tid; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < sw; ++w) {
+            const int c = cnt[w * E + e];
+            cnt[w * E + e] = run;
+            run += c;
+        }
+        tot[e] = run;
+    }
+    __syncthreads();
+
+    group_scan_experts(tot, E, counts, offsets, active, segs, ctrl);
 
     // Stable scatter: each segment warp walks its routes in order (loaded
     // kIdxBatch rounds of 32 at a time).
@@ -173,6 +184,75 @@ __device__ __forceinline__ void group_block(const int32_t* __restrict__ idx, int
     }
 }
 
+// The grouping of the routes of n tokens with k distinct experts each (the
+// top-k kernel's routes), by one block.  Within one expert the routes then
+// come from distinct tokens, so the stable position of route r = t*k + j of
+// expert e among e's routes is the number of earlier tokens that chose e:
+// bits[e][w] holds bit t & 31 of word w = t >> 5 for each token t that chose
+// e, and pre[e][w] the tokens of e's words before w.  No per-warp counts and
+// no match over a warp's routes; the same outputs as group_block.
+// sm: 2 * E * W + E ints, W = ceil(n / 32); n * k <= kBitsRoutes.
+constexpr int kBitsRoutes = 8 * kGroupThreads;   // routes a thread holds in registers: 8
+constexpr int kBitsWords = 8192;                 // E * W words of bitmap at most (32 KB)
+
+__device__ __forceinline__ void group_block_bits(const int32_t* __restrict__ idx, int n, int k, int E, int e_begin,
+                                                 int e_end, int32_t* __restrict__ counts,
+                                                 int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                                                 int32_t* __restrict__ inv, int32_t* __restrict__ active,
+                                                 int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl, int32_t* sm) {
+    const int W = (n + 31) >> 5, nk = n * k, tid = threadIdx.x, nt = blockDim.x;
+    uint32_t* bits = reinterpret_cast<uint32_t*>(sm);   // [E][W]
+    int32_t* pre = sm + E * W;                           // [E][W]
+    int32_t* tot = pre + E * W;                          // [E]
+    // This thread's routes r = tid + nt * u, loaded together (L2: other blocks
+    // of the kernel wrote idx), then the bitmap.
+    int ev[kBitsRoutes / kGroupThreads];
+#pragma unroll
+    for (int u = 0; u < kBitsRoutes / kGroupThreads; ++u) {
+        const int r = tid + nt * u;
+        ev[u] = r < nk ? __ldcg(idx + r) : -1;
+    }
+    for (int i = tid; i < E * W; i += nt) bits[i] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kBitsRoutes / kGroupThreads; ++u) {
+        const int r = tid + nt * u;
+        if (r < nk && ev[u] >= e_begin && ev[u] < e_end) {   // not held here: dropped
+            const int t = r / k;
+            atomicOr(&bits[ev[u] * W + (t >> 5)], 1u << (t & 31));
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += nt) {
+        int run = 0;
+        for (int w = 0; w < W; ++w) {
+            pre[e * W + w] = run;
+            run += __popc(bits[e * W + w]);
+        }
+        tot[e] = run;
+    }
+    __syncthreads();
+    group_scan_experts(tot, E, counts, offsets, active, segs, ctrl);
+#pragma unroll
+    for (int u = 0; u < kBitsRoutes / kGroupThreads; ++u) {
+        const int r = tid + nt * u;
+        if (r >= nk) break;
+        const int e = ev[u];
+        if (e >= e_begin && e < e_end) {
+            const int t = r / k, w = t >> 5;
+            const int pos = tot[e] + pre[e * W + w] + __popc(bits[e * W + w] & ((1u << (t & 31)) - 1u));
+            perm[pos] = r;
+            inv[r] = pos;
+        } else {
+            inv[r] = -1;
+        }
+    }
+}
+
+inline bool group_bits_fits(int n, int k, int E) {
+    return n * k <= kBitsRoutes && (size_t)E * ((n + 31) / 32) <= (size_t)kBitsWords;
+}
+
 __global__ void __launch_bounds__(kGroupThreads)
 group_kernel(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_end,
              int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -186,7 +266,8 @@ group_kernel(const int32_t* __restrict__ idx, int nk, int E, int e_begin, int e_
 
 // Top-k routing of every token (one CTA per token, the top-k kernel's
 // arithmetic) and then, in the CTA that finishes last, the grouping of all
-// routes: one launch instead of two.  The last CTA is found with a counter in
+// routes (group_block_bits when its bitmap fits, else group_block): one
+// launch instead of two.  The last CTA is found with a counter in
 // the control block (release fence before the increment, acquire fence after
 // it), which that CTA returns to zero.  kMinBlocks = 2 (at most 32 registers
 // a thread) when there are more tokens than SMs, so that up to two SMs' worth
@@ -197,7 +278,8 @@ topk_group_kernel(const float* __restrict__ logits, int ns, int n, int E, int k,
                   const float* __restrict__ bias, int norm, float scale, int32_t* idx_out,
                   float* __restrict__ w_out, int e_begin, int e_end, int32_t* __restrict__ counts,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-                  int32_t* __restrict__ active, int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl, int sw) {
+                  int32_t* __restrict__ active, int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl, int sw,
+                  int bits) {
     extern __shared__ __align__(16) float smf[];
     float* slg = smf;                                                    // [E]
     unsigned long long* skey =
@@ -228,7 +310,10 @@ topk_group_kernel(const float* __restrict__ logits, int ns, int n, int E, int k,
     }
     __syncthreads();
     if (s_last) {
-        group_block(idx_out, n * k, E, e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, gsm, sw);
+        if (bits)
+            group_block_bits(idx_out, n, k, E, e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, gsm);
+        else
+            group_block(idx_out, n * k, E, e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, gsm, sw);
         if (tid == 0) ctrl->routed = 0;
     }
     pdl_trigger();
@@ -250,8 +335,12 @@ cudaError_t launch_topk_group(const float* logits, int ns, int n, int E, int k, 
                               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
                               Ctrl* ctrl, int num_sms, cudaStream_t st) {
     const int sw = seg_warps(E, n * k);
+    // The routes of one top-k call have distinct experts per token: the bitmap
+    // grouping when its bitmap fits.
+    const bool bits = group_bits_fits(n, k, E);
+    const size_t gwords = bits ? (size_t)(2 * ((n + 31) / 32) + 1) * E : (size_t)(sw + 1) * E;
     const size_t smem = (size_t)((E + 3) & ~3) * sizeof(float) + (size_t)(E + 32) * sizeof(unsigned long long) +
-                        sizeof(int32_t) * (size_t)(sw + 1) * E;
+                        sizeof(int32_t) * gwords;
     static std::mutex mu;
     static size_t configured[128][2] = {};
     int dev = 0;
@@ -267,7 +356,7 @@ cudaError_t launch_topk_group(const float* logits, int ns, int n, int E, int k, 
         }
     }
     launch_pdl(kern, n, kGroupThreads, smem, st, logits, ns, n, E, k, routing, bias, norm, scale, idx, w,
-               e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, sw);
+               e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, sw, bits ? 1 : 0);
     return cudaGetLastError();
 }
 

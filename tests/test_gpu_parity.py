@@ -375,6 +375,21 @@ def test_rows_do_not_depend_on_the_batch_grouped(fmt, norm):
     assert torch.equal(many[-40:], full)
 
 
+def test_both_groupings_of_the_top_k_kernel_agree():
+    """The grouped path's top-k kernel sorts the routes by expert with a token
+    bitmap per expert while it fits (E * ceil(n / 32) <= 8192 words and
+    n * k <= 8192), else with per-warp counts.  With 1024 experts, 250 tokens
+    take the bitmap and 300 the counts: the 300-token call matches the oracle,
+    and the rows both calls share are identical, bit for bit."""
+    cfg = small("groupings", num_experts=1024, top_k=8, hidden=128, inter=64, shared_inter=64)
+    lw, x, out, idx, w, layer = _check(cfg, 300)
+    part, idx_p, w_p = layer.forward(x[:250])
+    torch.cuda.synchronize()
+    assert torch.equal(idx_p, idx[:250])
+    assert torch.equal(w_p, w[:250])
+    assert torch.equal(part, out[:250])
+
+
 # ---------------------------------------------------------------- expert parallelism
 
 def _ep_check(cfg, n, ranges, path="auto", rows=None):
