@@ -380,8 +380,12 @@ def test_both_groupings_of_the_top_k_kernel_agree():
     bitmap per expert while it fits (E * ceil(n / 32) <= 8192 words and
     n * k <= 8192), else with per-warp counts.  With 1024 experts, 250 tokens
     take the bitmap and 300 the counts: the 300-token call matches the oracle,
-    and the rows both calls share are identical, bit for bit."""
-    cfg = small("groupings", num_experts=1024, top_k=8, hidden=128, inter=64, shared_inter=64)
+    and the rows both calls share are identical, bit for bit.  (FP8 experts:
+    their f16 intermediate keeps 300 rows of this small layer well inside the
+    tolerance; BF16's bf16 intermediate at K = 64 reaches ~2e-2 RMS at the tail
+    of 38k outputs.)"""
+    cfg = small("groupings", num_experts=1024, top_k=8, hidden=128, inter=64, shared_inter=64,
+                expert_fmt=synth.FMT_FP8_B128)
     lw, x, out, idx, w, layer = _check(cfg, 300)
     part, idx_p, w_p = layer.forward(x[:250])
     torch.cuda.synchronize()
