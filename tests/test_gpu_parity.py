@@ -375,6 +375,33 @@ def test_rows_do_not_depend_on_the_batch_grouped(fmt, norm):
     assert torch.equal(many[-40:], full)
 
 
+def _scale_at_offset(q, off):
+    """q with its block scales moved to a buffer `off` bytes past a 256-byte
+    aligned allocation (the same bytes at another address)."""
+    flat = q.scale.contiguous().view(torch.uint8).flatten()
+    buf = torch.zeros(flat.numel() + 256, dtype=torch.uint8, device=flat.device)
+    buf[off:off + flat.numel()] = flat
+    moved = buf[off:off + flat.numel()].view(q.scale.dtype).view(q.scale.shape)
+    assert moved.data_ptr() % 16 == off % 16
+    return dataclasses.replace(q, scale=moved)
+
+
+@pytest.mark.parametrize("n", [17, 150])
+def test_nvfp4_scales_at_a_4_byte_offset(n):
+    """The API asks only 4-byte alignment of block scales: the same NVFP4
+    scales 4 bytes off a 16-byte boundary give bit-identical outputs (and the
+    aligned call matches the oracle)."""
+    cfg = small("nvfp4_scale_offset", expert_fmt=synth.FMT_NVFP4, hidden=512, top_k=4, num_experts=32)
+    lw, x, out, idx, w, layer = _check(cfg, n)
+    moved = dataclasses.replace(lw, gate=_scale_at_offset(lw.gate, 4), up=_scale_at_offset(lw.up, 4),
+                                sh_gate=_scale_at_offset(lw.sh_gate, 4), sh_up=_scale_at_offset(lw.sh_up, 4))
+    assert moved.gate.scale.data_ptr() % 16 == 4
+    out2, idx2, _ = MoeLayer(moved, n).forward(x)
+    torch.cuda.synchronize()
+    assert torch.equal(idx2, idx)
+    assert torch.equal(out2, out)
+
+
 def test_both_groupings_of_the_top_k_kernel_agree():
     """The grouped path's top-k kernel sorts the routes by expert with a token
     bitmap per expert while it fits (E * ceil(n / 32) <= 8192 words and
