@@ -36,6 +36,14 @@ if ROOT not in sys.path:
 METRIC = "MoE layer µs/call, tokens/s and HBM GB/s (frac of ~8 TB/s) at N=1–256"
 HEADLINE = "decode_n1"
 ALL_WORKLOADS = ("tiny_n1", "decode_n1", "decode_n16", "fp8_n64", "nvfp4_n256")
+# The steps beside the five workloads' path -- the pre-expert RMSNorm with the
+# shared-expert sigmoid gate, and the NVFP4 router -- on a workload's layer:
+# measured in the default run without the end-to-end legs and the oracle
+# (``next_rows``), or alone with --workload NAME.
+VARIANTS = {
+    "decode_n16+norm+gate": ("decode_n16", {"pre_expert_norm": True, "shared_gate": True}),
+    "nvfp4_n256+nvfp4_router": ("nvfp4_n256", {"router_fmt": "nvfp4"}),
+}
 # Kernel sequence of each expert path, by the number of stage markers a call records.
 STAGES_BY_MARKS = {
     2: ["fused"],
@@ -299,7 +307,11 @@ def _oracle_child(args):
 def workload_config(args, name):
     """The workload's layer, with the --tokens / --experts overrides applied."""
     from mixture_experts_decode_router_gb300 import synth
-    cfg = synth.WORKLOADS[name]
+    if name in VARIANTS:
+        base, kw = VARIANTS[name]
+        cfg = synth.WORKLOADS[base].with_(name=name, **kw)
+    else:
+        cfg = synth.WORKLOADS[name]
     if args.tokens > 0:
         cfg = cfg.with_(n_tokens=args.tokens, name=f"{cfg.name}@n{args.tokens}")
     if args.experts > 0:
@@ -379,17 +391,23 @@ def stage_alg_bytes(cfg, n, distinct, touched, nm, has_bias):
     nk = n * k
     w_gu = distinct * 2 * mb(fmt, I, H) + (2 * mb(fmt, S, H) if S else 0)
     w_dn = distinct * mb(fmt, H, I) + (mb(fmt, H, S) if S else 0)
+    # The pre-expert RMSNorm (x in, the norm weight, the normalised rows out)
+    # runs at the start of the gather stage (grouped) or the gate/up stage.
+    norm = (2 * n * H * 2 + H * 2) if cfg.pre_expert_norm else 0
     return {
         "fused": touched,
-        "router": E * H * 2 + n * H * 2 + n * E * 4,
+        # router matrix (BF16 or NVFP4 codes + scales), x, the logits; the
+        # shared-gate row and its logit when the layer has one
+        "router": (mb(cfg.router_fmt, E, H) if cfg.router_fmt != "bf16" else E * H * 2) + n * H * 2 + n * E * 4
+        + ((H * 2 + n * 4) if cfg.shared_gate else 0),
         # top-k (logits in, routes out) + grouping (routes in, counts/offsets/permutation out)
         "topk_group": n * E * 4 + nk * 8 + (4 * E if has_bias else 0)
         + nk * 4 + 4 * (3 * E + 1) + nk * 4,
         # token-major: fp32 activations; grouped: 16-bit activations
         "gate_up": w_gu + n * H * 2 + (4 if nm == 5 else 2) * (nk * I + n * S)
-        + (2 * (nk * H + n * H) if nm in (6, 7) else 0),
+        + (2 * (nk * H + n * H) if nm in (6, 7) else 0) + (norm if nm == 5 else 0),
         "down_blend": w_dn + 4 * (nk * I + n * S) + n * H * 2 + nk * 8,
-        "gather": 2 * 2 * (nk * H + n * H),
+        "gather": 2 * 2 * (nk * H + n * H) + norm,
         "down": w_dn + 2 * (nk * I + n * S) + 4 * (nk * H + (n * H if S else 0)),
         "combine": 4 * (nk * H + (n * H if S else 0)) + n * H * 2 + nk * 4,
         # the down kernel with the combine folded in: weights and activations in,
@@ -398,7 +416,7 @@ def stage_alg_bytes(cfg, n, distinct, touched, nm, has_bias):
     }
 
 
-def measure_workload(args, name, dev, flush, world, local):
+def measure_workload(args, name, dev, flush, world, local, light=False):
     """Times one workload: K moe_forward calls (L2 flushed between them), the
     per-stage split, the end-to-end legs with host buffers, and a device copy
     of the same byte count.  Returns the workload's entry of the JSON line
@@ -490,65 +508,82 @@ def measure_workload(args, name, dev, flush, world, local):
     dom_ms = float(stage_ms[stages_run.index(dom)])
     achieved = alg[dom] / (dom_ms * 1e-3) / 1e9
     stages = {s: {"us": round(float(stage_ms[j]) * 1e3, 3), "alg_bytes": int(alg[s]),
-                  "gbs": round(alg[s] / (stage_ms[j] * 1e-3) / 1e9, 1)}
+                  "gbs": round(alg[s] / (stage_ms[j] * 1e-3) / 1e9, 1),
+                  "frac_of_measured": round(alg[s] / (stage_ms[j] * 1e-3) / 1e9 / peak, 4)}
               for j, s in enumerate(stages_run)}
 
-    # End to end through the public API with host buffers, two ways, each step
-    # taking a fresh input from pinned host memory and leaving the result there:
-    # (a) zero-copy: x and out are the pinned host buffers themselves; the
-    #     kernels read x and write out across the host link (NVLink-C2C);
-    # (b) explicit copies: H2D of x, the call on device buffers, D2H of out.
-    x_h = x.cpu().pin_memory()
-    out_h = torch.empty(n, cfg.hidden, dtype=torch.bfloat16).pin_memory()
-    x_d = torch.empty_like(x)
-    Ke = min(K, 1000)
+    e2e, size_copy, copy_ratio = None, None, None
+    if not light:
+        # End to end through the public API with host buffers, two ways, each step
+        # taking a fresh input from pinned host memory and leaving the result there:
+        # (a) zero-copy: x and out are the pinned host buffers themselves; the
+        #     kernels read x and write out across the host link (NVLink-C2C);
+        # (b) explicit copies: H2D of x, the call on device buffers, D2H of out.
+        x_h = x.cpu().pin_memory()
+        out_h = torch.empty(n, cfg.hidden, dtype=torch.bfloat16).pin_memory()
+        x_d = torch.empty_like(x)
+        Ke = min(K, 1000)
 
-    def timed_e2e(zero_copy):
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+        def timed_e2e(zero_copy):
+            starts = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+            ends = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+            for i in range(Ke):
+                flush.zero_()
+                starts[i].record(stream)
+                if zero_copy:
+                    s = B.moe_forward(layer.c_cfg, layer.c_w, x_h, n, out_h, idx, wts, layer.ws, layer.ws_bytes, sptr)
+                else:
+                    x_d.copy_(x_h, non_blocking=True)
+                    s = B.moe_forward(layer.c_cfg, layer.c_w, x_d, n, out, idx, wts, layer.ws, layer.ws_bytes, sptr)
+                if s != B.MOE_OK:
+                    raise B.MoeError(B.moe_status_string(s))
+                if not zero_copy:
+                    out_h.copy_(out, non_blocking=True)
+                ends[i].record(stream)
+            torch.cuda.synchronize()
+            return max_over_ranks(float(np.sum([a.elapsed_time(b) for a, b in zip(starts, ends)])), dev)
+
+        e2e_ms = timed_e2e(True)
+        if not torch.equal(out_h.view(torch.int16), out.cpu().view(torch.int16)):
+            raise B.MoeError("zero-copy output differs from the device-buffer output")
+        e2e_copy_ms = timed_e2e(False)
+
+        # A device-to-device copy moving the call's touched bytes (half read, half
+        # written: the measured peak's own method), timed the same way: what one
+        # launch of plain streaming reaches at this size on this GPU.
+        half = max(16, touched // 2 // 16 * 16)
+        src = torch.ones(half, dtype=torch.uint8, device=dev)
+        dst = torch.empty_like(src)
+        for _ in range(3):
+            flush.zero_()
+            dst.copy_(src)
+        cs = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+        ce = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
         for i in range(Ke):
             flush.zero_()
-            starts[i].record(stream)
-            if zero_copy:
-                s = B.moe_forward(layer.c_cfg, layer.c_w, x_h, n, out_h, idx, wts, layer.ws, layer.ws_bytes, sptr)
-            else:
-                x_d.copy_(x_h, non_blocking=True)
-                s = B.moe_forward(layer.c_cfg, layer.c_w, x_d, n, out, idx, wts, layer.ws, layer.ws_bytes, sptr)
-            if s != B.MOE_OK:
-                raise B.MoeError(B.moe_status_string(s))
-            if not zero_copy:
-                out_h.copy_(out, non_blocking=True)
-            ends[i].record(stream)
+            cs[i].record(stream)
+            dst.copy_(src)
+            ce[i].record(stream)
         torch.cuda.synchronize()
-        return max_over_ranks(float(np.sum([a.elapsed_time(b) for a, b in zip(starts, ends)])), dev)
-
-    e2e_ms = timed_e2e(True)
-    if not torch.equal(out_h.view(torch.int16), out.cpu().view(torch.int16)):
-        raise B.MoeError("zero-copy output differs from the device-buffer output")
-    e2e_copy_ms = timed_e2e(False)
-
-    # A device-to-device copy moving the call's touched bytes (half read, half
-    # written: the measured peak's own method), timed the same way: what one
-    # launch of plain streaming reaches at this size on this GPU.
-    half = max(16, touched // 2 // 16 * 16)
-    src = torch.ones(half, dtype=torch.uint8, device=dev)
-    dst = torch.empty_like(src)
-    for _ in range(3):
-        flush.zero_()
-        dst.copy_(src)
-    cs = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
-    ce = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
-    for i in range(Ke):
-        flush.zero_()
-        cs[i].record(stream)
-        dst.copy_(src)
-        ce[i].record(stream)
-    torch.cuda.synchronize()
-    copy_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(cs, ce)]))
-    del src, dst
+        copy_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(cs, ce)]))
+        del src, dst
+        e2e = e2e_line(world, n, cfg.hidden, Ke, e2e_ms, e2e_copy_ms)
+        size_copy = {
+            "us": round(copy_ms * 1e3, 3), "bytes": 2 * half,
+            "gbs": round(2 * half / (copy_ms * 1e-3) / 1e9, 1),
+            "frac_of_measured": round(2 * half / (copy_ms * 1e-3) / 1e9 / peak, 4),
+            "what": "torch copy_ of touched/2 bytes on the device (read + write = the call's touched "
+                    "bytes), L2 flushed, event-timed like the call"}
+        copy_ratio = round((dev_ms / K) / copy_ms, 3)
 
     ms_step = dev_ms / K
-    grouped = nm == 7
+    grouped = nm in (6, 7)
+    # This library's kernels per call: one a stage, plus the shared-gate row's
+    # own router launch beside the tensor-core or NVFP4 router, plus the norm,
+    # plus the BF16 expansion of an NVFP4 router for the tensor-core router.
+    per_call = len(stages_run) + (1 if cfg.pre_expert_norm else 0) \
+        + (1 if cfg.shared_gate and (cfg.router_fmt != "bf16" or grouped) else 0) \
+        + (1 if cfg.router_fmt != "bf16" and grouped else 0)
     entry = {
         "us_per_call": round(ms_step * 1e3, 3),
         "us_per_call_p10_p50_p90": [round(float(np.percentile(per, q)) * 1e3, 3) for q in (10, 50, 90)],
@@ -558,20 +593,17 @@ def measure_workload(args, name, dev, flush, world, local):
         "distinct_experts": distinct,
         "hbm_gbs": round(touched / (ms_step * 1e-3) / 1e9, 1),
         "hbm_frac_of_measured": round(touched / (ms_step * 1e-3) / 1e9 / peak, 4),
-        "size_matched_copy": {
-            "us": round(copy_ms * 1e3, 3), "bytes": 2 * half,
-            "gbs": round(2 * half / (copy_ms * 1e-3) / 1e9, 1),
-            "frac_of_measured": round(2 * half / (copy_ms * 1e-3) / 1e9 / peak, 4),
-            "what": "torch copy_ of touched/2 bytes on the device (read + write = the call's touched "
-                    "bytes), L2 flushed, event-timed like the call"},
-        "call_time_over_copy_time": round(ms_step / copy_ms, 3),
+        "size_matched_copy": size_copy,
+        "call_time_over_copy_time": copy_ratio,
         "dtype": compute_dtype(cfg.expert_fmt, grouped),
         "config": {"workload": cfg.name, "n_tokens": n, "hidden": cfg.hidden,
                    "num_experts": cfg.num_experts, "top_k": cfg.top_k, "inter": cfg.inter,
                    "shared_inter": cfg.shared_inter, "routing": cfg.routing,
-                   "expert_fmt": cfg.expert_fmt, "dup_frac": cfg.dup_frac, "path": args.path},
+                   "expert_fmt": cfg.expert_fmt, "dup_frac": cfg.dup_frac, "path": args.path,
+                   "router_fmt": cfg.router_fmt, "pre_expert_norm": cfg.pre_expert_norm,
+                   "shared_gate": cfg.shared_gate},
         "wall_s_timed_loop": round(t1 - t0, 3),
-        "gpu_launches": K * len(stages_run),   # this library's kernels: one per stage
+        "gpu_launches": K * per_call,
         "stages": stages,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
@@ -579,7 +611,7 @@ def measure_workload(args, name, dev, flush, world, local):
                      "tensor_pipe_active_pct": _tensor_pipe(dom, cfg.name),
                      "alg_bytes_per_launch": int(alg[dom]),
                      "avg_launch_us": round(dom_ms * 1e3, 3)},
-        "e2e": e2e_line(world, n, cfg.hidden, Ke, e2e_ms, e2e_copy_ms),
+        "e2e": e2e,
         "clocks": clk,
     }
     del layer, lw, x, out
@@ -605,6 +637,8 @@ def run_ours(args):
     names = workload_names(args)
     head = HEADLINE if HEADLINE in names else names[0]
     entries = {nm: measure_workload(args, nm, dev, flush, world, local) for nm in names}
+    next_rows = ({nm: measure_workload(args, nm, dev, flush, world, local, light=True) for nm in VARIANTS}
+                 if args.workload == "all" else {})
 
     # The oracle on the host cores (rank 0 at N = 1 only), after every GPU
     # measurement so the two never share the host.
@@ -643,6 +677,7 @@ def run_ours(args):
             "size_matched_copy": h["size_matched_copy"],
             "stages": h["stages"],
             "workloads": entries,
+            "next_rows": next_rows,
         }
         print(json.dumps(line))
     if world > 1:

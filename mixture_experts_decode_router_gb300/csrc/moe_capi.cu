@@ -198,11 +198,12 @@ static int effective_path(const moe_config_t* c, int32_t n) {
 // Enqueue router + top-k.  Arguments already validated.  `with_group`: the
 // top-k launch also groups the routes by expert (the fused top-k + grouping
 // kernel), so the expert stage that follows skips its grouping launch.
-// `x_dev`: x is in device memory.  A BF16 router on the grouped path runs on
-// the tensor cores (partial logits per K split, summed in order by the top-k
-// kernel; the shared-gate row keeps the CUDA-core kernel); the token-major
-// path keeps the CUDA-core router, whose arithmetic the single-token kernel
-// repeats, so that a token alone and in a batch route alike.
+// `x_dev`: x is in device memory.  A BF16 or NVFP4 router on the grouped path
+// runs on the tensor cores (partial logits per K split, summed in order by the
+// top-k kernel; an NVFP4 router expanded to BF16 first; the shared-gate row
+// keeps the CUDA-core kernel); the token-major path keeps the CUDA-core
+// routers, whose arithmetic the single-token kernel repeats, so that a token
+// alone and in a batch route alike.
 static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w, const void* x,
                                   int32_t n, int32_t* idx, float* wt, float* logits, void* ws,
                                   const WsLayout& L, bool with_group, bool x_dev, cudaStream_t st, Marks& mk) {
@@ -212,12 +213,24 @@ static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w,
     float* lsum = nullptr;   // where it writes summed logits (moe_route's output)
     int ns = 1;
     cudaError_t e;
-    if (c->router_fmt == MOE_W_BF16 && x_dev && effective_path(c, n) == MOE_PATH_GROUPED &&
-        router_tc_fits(n, c->num_experts, c->hidden)) {
+    if ((c->router_fmt == MOE_W_BF16 || c->router_fmt == MOE_W_NVFP4) && x_dev &&
+        effective_path(c, n) == MOE_PATH_GROUPED && router_tc_fits(n, c->num_experts, c->hidden)) {
+        // An NVFP4 router is first expanded to BF16 (exactly); its scale2
+        // multiplies the partials.
         float* part = at<float>(ws, L.lgp);
-        e = launch_router_tc(static_cast<const uint16_t*>(x), n, c->hidden,
-                             static_cast<const uint16_t*>(w->router_w), c->num_experts, part,
-                             &at<Ctrl>(ws, L.ctrl)->err, st);
+        const uint16_t* wr = static_cast<const uint16_t*>(w->router_w);
+        const float* rsc = nullptr;
+        e = cudaSuccess;
+        if (c->router_fmt == MOE_W_NVFP4) {
+            uint16_t* rq = at<uint16_t>(ws, L.rq);
+            e = launch_router_nvfp4_expand(qdev(w->router_q, c->num_experts, c->hidden, 0), c->num_experts,
+                                           c->hidden, rq, sms, st);
+            wr = rq;
+            rsc = w->router_q.scale2;
+        }
+        if (e == cudaSuccess)
+            e = launch_router_tc(static_cast<const uint16_t*>(x), n, c->hidden, wr, c->num_experts, part,
+                                 &at<Ctrl>(ws, L.ctrl)->err, rsc, st);
         if (e == cudaSuccess && w->shared_gate_w)
             e = launch_router(static_cast<const uint16_t*>(x), n, c->hidden, nullptr, 0,
                               static_cast<const uint16_t*>(w->shared_gate_w), nullptr,

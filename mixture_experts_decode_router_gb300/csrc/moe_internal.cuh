@@ -79,7 +79,7 @@ inline bool router_tc_fits(int64_t n, int64_t E, int H) {
 
 struct WsLayout {
     size_t ctrl, logits, sg_logit, idx, w, counts, offsets, perm, active, act, act_sh,
-        inv, segs, xs, xh, as, ash, y, ysh, xe, xd, lgp, total;
+        inv, segs, xs, xh, as, ash, y, ysh, xe, xd, lgp, rq, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -119,6 +119,7 @@ inline WsLayout ws_layout(const moe_config_t& c, int64_t n) {
     L.xe = take(sizeof(uint16_t) * n * H);                       // pre-expert RMSNorm of x
     L.xd = take(sizeof(uint16_t) * n * H);                       // x staged from pinned host memory
     L.lgp = take(router_tc_partials_bytes(n, E, (int)H));        // tensor-core router partials
+    L.rq = take(c.router_fmt == MOE_W_NVFP4 ? sizeof(uint16_t) * E * H : 0);   // an NVFP4 router as BF16
     L.total = off;
     return L;
 }

@@ -118,9 +118,13 @@ cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, i
                           const uint16_t* gw, float* logits, float* sg_logit, int num_sms,
                           cudaStream_t st);
 // Tensor-core router (moe_router_tc.cu): partial logits [splits][n][E] of the
-// BF16 router (rows E) for device-resident x; the caller checked router_tc_fits.
+// BF16 router (rows E) for device-resident x, each multiplied by *scale when
+// scale is not null; the caller checked router_tc_fits.
 cudaError_t launch_router_tc(const uint16_t* x, int n, int H, const uint16_t* wr, int E, float* part,
-                             int32_t* err, cudaStream_t st);
+                             int32_t* err, const float* scale, cudaStream_t st);
+// The NVFP4 router [E, H] as BF16 (exact: E2M1 code times E4M3 block scale),
+// for the tensor-core router, which multiplies its partials by scale2.
+cudaError_t launch_router_nvfp4_expand(const QMatDev& wq, int E, int H, uint16_t* out, int num_sms, cudaStream_t st);
 // 2-D TMA map over a row-major [rows, cols] matrix of `esize`-byte elements (moe_grouped_tc.cu).
 bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t cols,
               uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle);

@@ -14,6 +14,7 @@
 // The K splits depend on H only, so a token's partials, and the fixed-order
 // sum of them that the top-k kernels form, do not depend on which or how many
 // tokens share the call.
+#include <algorithm>
 #include <mutex>
 
 #include "moe_launch.cuh"
@@ -34,6 +35,7 @@ struct RouterTcParams {
     int tmem_cols;   // accumulator columns allocated (a power of two >= 32, >= nt)
     float* part;     // [splits][n][E]
     int32_t* err;
+    const float* scale;   // a multiplier of every partial (an NVFP4 router's scale2), or null
 };
 
 __global__ void __launch_bounds__(kRThreads, 1)
@@ -94,6 +96,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant
     // for each token the warp's 32 lanes write 32 consecutive experts.
     if (ptx::mbar_wait_warp(&bars[1], 0, s_abort, p.err, 7)) {
         ptx::tc_fence_after();
+        const float sc = p.scale ? __ldg(p.scale) : 1.0f;
         const int e = m0 + 32 * warp + lane;
         const uint32_t tb = tmem + ((uint32_t)(32 * warp) << 16);
         float* dst = p.part + (size_t)s * p.n * p.E;
@@ -103,7 +106,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int t = t0 + j0 + jj;
-                if (t < p.n && e < p.E) dst[(size_t)t * p.E + e] = d[jj];
+                if (t < p.n && e < p.E) dst[(size_t)t * p.E + e] = p.scale ? d[jj] * sc : d[jj];
             }
         }
     }
@@ -116,10 +119,45 @@ router_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant
     }
 }
 
+// The NVFP4 router matrix [E, H] expanded to BF16 for the tensor-core router:
+// each 16-element block's E2M1 codes times its E4M3 scale, a value of at most
+// 6 significant bits and so exact in BF16; scale2 multiplies the partials.
+// One 8-element chunk a thread.
+__global__ void __launch_bounds__(256)
+router_nvfp4_expand_kernel(const QMatDev wq, int E, int H, uint16_t* __restrict__ out) {
+    pdl_wait();
+    const int C = H >> 3;
+    const int64_t total = (int64_t)E * C;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int r = (int)(i / C), c = (int)(i - (int64_t)r * C);
+        WChunk<MOE_W_NVFP4> ch;
+        ch.load(wq, 0, r, c);
+        float v[8];
+        ch.decode(v);
+        const float s = ch.scale(wq, 0, r, c);
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * q] * s));
+            const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * q + 1] * s));
+            o[q] = lo | (hi << 16);
+        }
+        reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    pdl_trigger();
+}
+
 }  // namespace
 
+cudaError_t launch_router_nvfp4_expand(const QMatDev& wq, int E, int H, uint16_t* out, int num_sms, cudaStream_t st) {
+    const int64_t chunks = (int64_t)E * (H / 8);
+    const int blocks = (int)std::min<int64_t>((chunks + 255) / 256, (int64_t)num_sms * 8);
+    launch_pdl(router_nvfp4_expand_kernel, blocks, 256, 0, st, wq, E, H, out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_router_tc(const uint16_t* x, int n, int H, const uint16_t* wr, int E, float* part,
-                             int32_t* err, cudaStream_t st) {
+                             int32_t* err, const float* scale, cudaStream_t st) {
     const RouterTcSplit sp = router_tc_split(H);
     const int nt = router_tc_tile(n);
     CUtensorMap wmap, xmap;
@@ -134,6 +172,7 @@ cudaError_t launch_router_tc(const uint16_t* x, int n, int H, const uint16_t* wr
     p.tmem_cols = nt <= 32 ? 32 : (nt <= 64 ? 64 : 128);
     p.part = part;
     p.err = err;
+    p.scale = scale;
     const size_t smem = router_tc_smem(H, n);
     static std::mutex mu;
     static size_t configured[128] = {};

@@ -359,8 +359,10 @@ def layer_bytes(cfg: LayerConfig) -> dict:
     per_expert = 2 * matrix_bytes(cfg.expert_fmt, I, H) + matrix_bytes(cfg.expert_fmt, H, I)
     shared = (2 * matrix_bytes(cfg.expert_fmt, S, H) + matrix_bytes(cfg.expert_fmt, H, S)
               if S > 0 else 0)
-    extra = (4 * E if cfg.routing == ROUTE_SIGMOID_BIAS else 0) + (2 * H if cfg.shared_gate else 0)
-    return {"router": E * H * 2, "per_expert": per_expert, "shared": shared, "extra": extra,
+    extra = ((4 * E if cfg.routing == ROUTE_SIGMOID_BIAS else 0) + (2 * H if cfg.shared_gate else 0)
+             + (2 * H if cfg.pre_expert_norm else 0))
+    router = E * H * 2 if cfg.router_fmt == FMT_BF16 else matrix_bytes(cfg.router_fmt, E, H)
+    return {"router": router, "per_expert": per_expert, "shared": shared, "extra": extra,
             "hidden": H}
 
 

@@ -590,6 +590,14 @@ def test_nvfp4_router_full_size(name):
     _check(synth.WORKLOADS[name].with_(router_fmt=synth.FMT_NVFP4), threaded=True)
 
 
+@pytest.mark.parametrize("name", ["decode_n1", "decode_n16", "nvfp4_n256"])
+def test_pre_norm_and_shared_gate_full_size(name):
+    """The pre-expert RMSNorm and the shared-expert sigmoid gate on the
+    full-size layers (one token: the single-token kernel, which applies both
+    itself), every row."""
+    _check(synth.WORKLOADS[name].with_(pre_expert_norm=True, shared_gate=True), threaded=True)
+
+
 # ---------------------------------------------------------------- device error word
 
 def test_workspace_check_clean_after_calls():
