@@ -391,9 +391,10 @@ def stage_alg_bytes(cfg, n, distinct, touched, nm, has_bias):
     nk = n * k
     w_gu = distinct * 2 * mb(fmt, I, H) + (2 * mb(fmt, S, H) if S else 0)
     w_dn = distinct * mb(fmt, H, I) + (mb(fmt, H, S) if S else 0)
-    # The pre-expert RMSNorm (x in, the norm weight, the normalised rows out)
-    # runs at the start of the gather stage (grouped) or the gate/up stage.
-    norm = (2 * n * H * 2 + H * 2) if cfg.pre_expert_norm else 0
+    # The pre-expert RMSNorm: on the token-major path its own kernel at the
+    # start of the gate/up stage (x in, the weight, the normalised rows out);
+    # the grouped path's gather applies it as it copies (the weight only).
+    norm = ((2 * n * H * 2 + H * 2) if nm == 5 else H * 2) if cfg.pre_expert_norm else 0
     return {
         "fused": touched,
         # router matrix (BF16 or NVFP4 codes + scales), x, the logits; the
@@ -578,11 +579,13 @@ def measure_workload(args, name, dev, flush, world, local, light=False):
 
     ms_step = dev_ms / K
     grouped = nm in (6, 7)
-    # This library's kernels per call: one a stage, plus the shared-gate row's
-    # own router launch beside the tensor-core or NVFP4 router, plus the norm,
-    # plus the BF16 expansion of an NVFP4 router for the tensor-core router.
-    per_call = len(stages_run) + (1 if cfg.pre_expert_norm else 0) \
-        + (1 if cfg.shared_gate and (cfg.router_fmt != "bf16" or grouped) else 0) \
+    # This library's kernels per call: one a stage, plus the norm (the grouped
+    # path's gather applies it), plus the
+    # shared-gate row's own router launch beside the CUDA-core NVFP4 router (on
+    # the grouped path the top-k kernel forms it), plus the BF16 expansion of
+    # an NVFP4 router for the tensor-core router.
+    per_call = len(stages_run) + (1 if cfg.pre_expert_norm and not grouped else 0) \
+        + (1 if cfg.shared_gate and cfg.router_fmt != "bf16" and not grouped else 0) \
         + (1 if cfg.router_fmt != "bf16" and grouped else 0)
     entry = {
         "us_per_call": round(ms_step * 1e3, 3),

@@ -213,6 +213,9 @@ static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w,
     float* lsum = nullptr;   // where it writes summed logits (moe_route's output)
     int ns = 1;
     cudaError_t e;
+    // The shared-gate row beside the tensor-core router: formed by the top-k +
+    // grouping kernel when it runs and has room, else launched on its own.
+    const uint16_t* gate_in_topk = nullptr;
     if ((c->router_fmt == MOE_W_BF16 || c->router_fmt == MOE_W_NVFP4) && x_dev &&
         effective_path(c, n) == MOE_PATH_GROUPED && router_tc_fits(n, c->num_experts, c->hidden)) {
         // An NVFP4 router is first expanded to BF16 (exactly); its scale2
@@ -231,7 +234,9 @@ static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w,
         if (e == cudaSuccess)
             e = launch_router_tc(static_cast<const uint16_t*>(x), n, c->hidden, wr, c->num_experts, part,
                                  &at<Ctrl>(ws, L.ctrl)->err, rsc, st);
-        if (e == cudaSuccess && w->shared_gate_w)
+        if (w->shared_gate_w && with_group && topk_group_gate_fits(c->num_experts, c->hidden))
+            gate_in_topk = static_cast<const uint16_t*>(w->shared_gate_w);
+        else if (e == cudaSuccess && w->shared_gate_w)
             e = launch_router(static_cast<const uint16_t*>(x), n, c->hidden, nullptr, 0,
                               static_cast<const uint16_t*>(w->shared_gate_w), nullptr,
                               at<float>(ws, L.sg_logit), sms, st);
@@ -258,7 +263,8 @@ static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w,
                               c->routed_scaling_factor, idx, wt, c->expert_begin, c->expert_end,
                               at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm),
                               at<int32_t>(ws, L.inv), at<int32_t>(ws, L.active), at<int32_t>(ws, L.segs),
-                              at<Ctrl>(ws, L.ctrl), sms, st);
+                              at<Ctrl>(ws, L.ctrl), static_cast<const uint16_t*>(x), gate_in_topk,
+                              at<float>(ws, L.sg_logit), c->hidden, sms, st);
     else
         e = launch_topk(lin, ns, lsum, n, c->num_experts, c->top_k, c->routing, w->correction_bias,
                         c->norm_topk_prob, c->routed_scaling_factor, idx, wt, st);
@@ -268,7 +274,7 @@ static moe_status_t enqueue_route(const moe_config_t* c, const moe_weights_t* w,
 
 
 // The grouped tensor-core expert stage (after the grouping kernel).
-// x: the experts' input (the layer input or its pre-expert RMSNorm).
+// x: the layer input; the gather applies the pre-expert RMSNorm, if any.
 static moe_status_t enqueue_grouped(const moe_config_t* c, const moe_weights_t* w, const void* x,
                                     int32_t n, const float* wt, void* out, void* ws, const WsLayout& L,
                                     float* sg_logit, cudaStream_t st, Marks& mk) {
@@ -279,7 +285,8 @@ static moe_status_t enqueue_grouped(const moe_config_t* c, const moe_weights_t* 
     uint16_t* xs = at<uint16_t>(ws, L.xs);
     uint16_t* xh = at<uint16_t>(ws, L.xh);
     cudaError_t e = launch_gather(fmt, static_cast<const uint16_t*>(x), n, H, k, at<int32_t>(ws, L.perm),
-                                  at<int32_t>(ws, L.offsets), E, xs, xh, sms, st);
+                                  at<int32_t>(ws, L.offsets), E, xs, xh,
+                                  static_cast<const uint16_t*>(w->pre_expert_norm_w), c->rms_norm_eps, sms, st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     mk.mark(st);
 
@@ -365,9 +372,10 @@ static moe_status_t enqueue_experts(const moe_config_t* c, const moe_weights_t* 
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     // The experts' input: x, or its pre-expert RMSNorm (the router and the
-    // shared gate keep x).
+    // shared gate keep x); the grouped path's gather applies the norm itself.
+    const int path = effective_path(c, n);
     const void* xin = x;
-    if (w->pre_expert_norm_w) {
+    if (w->pre_expert_norm_w && path != MOE_PATH_GROUPED) {
         uint16_t* xe = at<uint16_t>(ws, L.xe);
         e = launch_rmsnorm(static_cast<const uint16_t*>(x), n, H,
                            static_cast<const uint16_t*>(w->pre_expert_norm_w), c->rms_norm_eps, xe, st);
@@ -382,9 +390,8 @@ static moe_status_t enqueue_experts(const moe_config_t* c, const moe_weights_t* 
         mk.mark(st);
     }
 
-    const int path = effective_path(c, n);
     if (path == MOE_PATH_GROUPED)
-        return enqueue_grouped(c, w, xin, n, wt, out, ws, L, sg_logit, st, mk);
+        return enqueue_grouped(c, w, x, n, wt, out, ws, L, sg_logit, st, mk);
 
     const int eb = c->expert_begin;
     GateUpParams gu{};

@@ -33,11 +33,18 @@ __device__ __forceinline__ uint4 to_tile16(uint4 v) {
 // One warp per destination row (the row's source index read once), its lanes
 // taking 16-byte chunks lane, lane + 32, ...: kU chunks per lane loaded before
 // any is stored, so a row costs one round of load latency, not one per chunk.
-template <bool F16>
+// With a pre-expert RMSNorm weight nw, the rows copied are the normalised ones,
+// with the norm kernel's arithmetic (rms_inv_warp, then rms_apply8): a first
+// pass over the row sums its squares in the same chunk order (lane l's chunks
+// l, l + 32, ... in order, then the butterfly), so the values are that
+// kernel's, bit for bit.  (NORM: whether nw is given -- its own instance, so
+// that the plain copy keeps its small register count.)
+template <bool F16, bool NORM>
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int n, int H, int k,
                                                      const int32_t* __restrict__ perm,
                                                      const int32_t* __restrict__ offsets, int E,
-                                                     uint16_t* __restrict__ xs, uint16_t* __restrict__ xh) {
+                                                     uint16_t* __restrict__ xs, uint16_t* __restrict__ xh,
+                                                     const uint16_t* __restrict__ nw, float eps) {
     constexpr int kU = 8;
     pdl_wait();
     const int n_routes = offsets[E];
@@ -50,12 +57,69 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
         const int t = routed ? perm[r] / k : r - n_routes;
         const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
         uint4* dst = reinterpret_cast<uint4*>(routed ? xs + (size_t)r * H : xh + (size_t)(r - n_routes) * H);
+        if (NORM && C8 <= 32 * kU) {
+            // The whole row in one round: the lane's chunks and their norm
+            // weights loaded together, then the sum of squares, then the stores.
+            uint4 v[kU], wv[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int c = lane + 32 * u;
+                if (c < C8) {
+                    v[u] = __ldg(src + c);
+                    wv[u] = __ldg(reinterpret_cast<const uint4*>(nw) + c);
+                }
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                if (lane + 32 * u < C8) {
+                    float f[8];
+                    bf16x8_to_float(v[u], f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+                }
+            }
+            ss = warp_sum(ss);
+            const float inv = rsqrtf(ss / (float)H + eps);
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int c = lane + 32 * u;
+                if (c < C8) dst[c] = to_tile16<F16>(rms_apply8(v[u], wv[u], inv));
+            }
+            continue;
+        }
+        float inv = 0.f;
+        if (NORM) {   // a longer row: its sum of squares first, then the copy below
+            float ss = 0.f;
+            for (int c0 = lane; c0 < C8; c0 += 32 * kU) {
+                uint4 v[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c < C8) v[u] = __ldg(src + c);
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    if (c0 + 32 * u < C8) {
+                        float f[8];
+                        bf16x8_to_float(v[u], f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+                    }
+                }
+            }
+            ss = warp_sum(ss);
+            inv = rsqrtf(ss / (float)H + eps);
+        }
         for (int c0 = lane; c0 < C8; c0 += 32 * kU) {
             uint4 v[kU];
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 const int c = c0 + 32 * u;
-                if (c < C8) v[u] = __ldg(src + c);
+                if (c < C8) {
+                    v[u] = __ldg(src + c);
+                    if (NORM) v[u] = rms_apply8(v[u], __ldg(reinterpret_cast<const uint4*>(nw) + c), inv);
+                }
             }
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
@@ -98,11 +162,12 @@ cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, int num_sms,
 }
 
 cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const int32_t* perm,
-                          const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, int num_sms,
-                          cudaStream_t st) {
+                          const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, const uint16_t* norm_w,
+                          float eps, int num_sms, cudaStream_t st) {
     const int grid = 2 * num_sms;
-    if (fmt != MOE_W_BF16) launch_pdl(gather_kernel<true>, grid, 256, 0, st, x, n, H, k, perm, offsets, E, xs, xh);
-    else launch_pdl(gather_kernel<false>, grid, 256, 0, st, x, n, H, k, perm, offsets, E, xs, xh);
+    auto kern = fmt != MOE_W_BF16 ? (norm_w ? gather_kernel<true, true> : gather_kernel<true, false>)
+                                  : (norm_w ? gather_kernel<false, true> : gather_kernel<false, false>);
+    launch_pdl(kern, grid, 256, 0, st, x, n, H, k, perm, offsets, E, xs, xh, norm_w, eps);
     return cudaGetLastError();
 }
 

@@ -279,7 +279,8 @@ topk_group_kernel(const float* __restrict__ logits, int ns, int n, int E, int k,
                   float* __restrict__ w_out, int e_begin, int e_end, int32_t* __restrict__ counts,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                   int32_t* __restrict__ active, int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl, int sw,
-                  int bits) {
+                  int bits, const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw,
+                  float* __restrict__ sg_logit, int H, int sgx_off) {
     extern __shared__ __align__(16) float smf[];
     float* slg = smf;                                                    // [E]
     unsigned long long* skey =
@@ -292,8 +293,50 @@ topk_group_kernel(const float* __restrict__ logits, int ns, int n, int E, int k,
     __shared__ int s_last;
     const int t = blockIdx.x, tid = threadIdx.x;
     pdl_wait();
+    // The shared gate's logit of token t, when the layer has one and the router
+    // ran on the tensor cores (which leaves that row to this kernel): the
+    // threads past the key phase's E + 32 entries (at least the last warp)
+    // stage x[t] and the gate row in shared memory while the routing loads its
+    // logits; warp 0 forms the dot product after the routing, with the
+    // CUDA-core router's arithmetic for a row (lane l chains its chunks l,
+    // l + 32, ... in order, then the butterfly), so its bits are that kernel's.
+    const int C = H >> 3;
+    uint4* sgx = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(smf) + sgx_off);   // [x[t] | gw], C each
+    if (gw) {
+        const int s0 = min(E + 32, (int)blockDim.x - 32), nst = (int)blockDim.x - s0;
+        if (tid >= s0) {
+            constexpr int kU = 4;
+            for (int i0 = tid - s0; i0 < 2 * C; i0 += kU * nst) {
+                uint4 v[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int i = i0 + u * nst;
+                    if (i < 2 * C)
+                        v[u] = __ldg(i < C ? reinterpret_cast<const uint4*>(x + (size_t)t * H) + i
+                                           : reinterpret_cast<const uint4*>(gw) + (i - C));
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int i = i0 + u * nst;
+                    if (i < 2 * C) sgx[i] = v[u];
+                }
+            }
+        }
+    }
     route_token_block(logits + (size_t)t * E, ns, (size_t)n * E, nullptr, E, k, routing, bias, norm, scale, slg, skey,
-                      cand_k, gmax, zg, ssel, sselw);
+                      cand_k, gmax, zg, ssel, sselw);   // (its barriers order the staging before the use below)
+    if (gw && tid < 32) {
+        float acc = 0.f;
+        for (int c = tid; c < C; c += 32) {
+            float wv[8], xv[8];
+            bf16x8_to_float(sgx[C + c], wv);
+            bf16x8_to_float(sgx[c], xv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc = fmaf(wv[i], xv[i], acc);
+        }
+        const float v = warp_sum(acc);
+        if (tid == 0) sg_logit[t] = v;
+    }
     if (tid < k) {
         idx_out[(size_t)t * k + tid] = ssel[tid];
         w_out[(size_t)t * k + tid] = sselw[tid];
@@ -330,17 +373,28 @@ cudaError_t launch_group(const int32_t* idx, int nk, int E, int e_begin, int e_e
     return cudaGetLastError();
 }
 
+bool topk_group_gate_fits(int E, int H) {
+    // The stagers (threads past E + 32, at least one warp) hold both rows' chunks
+    // at kU = 4 loads each.
+    const int nst = kGroupThreads - std::min(E + 32, kGroupThreads - 32);
+    return H % 8 == 0 && 2 * (H / 8) <= 4 * nst;
+}
+
 cudaError_t launch_topk_group(const float* logits, int ns, int n, int E, int k, int routing, const float* bias, int norm,
                               float scale, int32_t* idx, float* w, int e_begin, int e_end, int32_t* counts,
                               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
-                              Ctrl* ctrl, int num_sms, cudaStream_t st) {
+                              Ctrl* ctrl, const uint16_t* x, const uint16_t* gw, float* sg_logit, int H, int num_sms,
+                              cudaStream_t st) {
     const int sw = seg_warps(E, n * k);
     // The routes of one top-k call have distinct experts per token: the bitmap
     // grouping when its bitmap fits.
     const bool bits = group_bits_fits(n, k, E);
     const size_t gwords = bits ? (size_t)(2 * ((n + 31) / 32) + 1) * E : (size_t)(sw + 1) * E;
-    const size_t smem = (size_t)((E + 3) & ~3) * sizeof(float) + (size_t)(E + 32) * sizeof(unsigned long long) +
-                        sizeof(int32_t) * gwords;
+    size_t smem = (size_t)((E + 3) & ~3) * sizeof(float) + (size_t)(E + 32) * sizeof(unsigned long long) +
+                  sizeof(int32_t) * gwords;
+    smem = (smem + 15) / 16 * 16;
+    const int sgx_off = (int)smem;
+    if (gw) smem += (size_t)2 * H * sizeof(uint16_t);   // x[t] and the gate row
     static std::mutex mu;
     static size_t configured[128][2] = {};
     int dev = 0;
@@ -356,7 +410,8 @@ cudaError_t launch_topk_group(const float* logits, int ns, int n, int E, int k, 
         }
     }
     launch_pdl(kern, n, kGroupThreads, smem, st, logits, ns, n, E, k, routing, bias, norm, scale, idx, w,
-               e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, sw, bits ? 1 : 0);
+               e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, sw, bits ? 1 : 0, x, gw, sg_logit, H,
+               sgx_off);
     return cudaGetLastError();
 }
 

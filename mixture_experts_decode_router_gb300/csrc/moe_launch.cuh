@@ -77,9 +77,11 @@ bool build_tc_maps(int fmt, bool gate_up, const moe_weights_t* w, int E, int H, 
 cudaError_t launch_grouped_tc(int fmt, bool gate_up, const TcMaps& maps, const TcParams& p, int num_sms,
                               cudaStream_t st);
 cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t st);
+// norm_w (may be null): the pre-expert RMSNorm weight; the rows gathered are
+// then the normalised ones (the norm kernel's values).
 cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const int32_t* perm,
-                          const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, int num_sms,
-                          cudaStream_t st);
+                          const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, const uint16_t* norm_w,
+                          float eps, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const float* y, const float* ysh, const int32_t* inv, int n, int H, int k,
                            int has_shared, int accumulate, uint16_t* out, int num_sms, cudaStream_t st);
 
@@ -137,10 +139,14 @@ cudaError_t launch_topk(const float* logits, int ns, float* lsum, int n, int E, 
 cudaError_t launch_group(const int32_t* idx, int nk, int E, int e_begin, int e_end, int32_t* counts,
                          int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
                          Ctrl* ctrl, cudaStream_t st);
-cudaError_t launch_topk_group(const float* logits, int ns, int n, int E, int k, int routing, const float* bias, int norm,
-                              float scale, int32_t* idx, float* w, int e_begin, int e_end, int32_t* counts,
+cudaError_t launch_topk_group(const float* logits, int ns, int n, int E, int k, int routing, const float* bias,
+                              int norm, float scale, int32_t* idx, float* w, int e_begin, int e_end, int32_t* counts,
                               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
-                              Ctrl* ctrl, int num_sms, cudaStream_t st);
+                              Ctrl* ctrl, const uint16_t* x, const uint16_t* gw, float* sg_logit, int H, int num_sms,
+                              cudaStream_t st);
+// Whether launch_topk_group can form the shared gate's logit (gw != null) for
+// E experts and hidden size H.
+bool topk_group_gate_fits(int E, int H);
 cudaError_t launch_rmsnorm(const uint16_t* x, int n, int H, const uint16_t* w, float eps, uint16_t* xe,
                            cudaStream_t st);
 cudaError_t launch_gate_up_tm(int fmt, const GateUpParams& gu, int num_sms, cudaStream_t st);
