@@ -142,7 +142,10 @@ typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_TOKEN_MAJOR = 1, MOE_PATH_GROUPED = 2
  * NVFP4 matrix [E, H] in the expert layout below with one expert (w: bytes
  * [E, H/2]; scale: E4M3 [E, H/16]; scale2: one fp32), multiplying the BF16
  * activations; router_w is then unused (may be NULL).  One token then runs the
- * token-major kernels (the single-token kernel reads a BF16 router).
+ * token-major kernels (the single-token kernel reads a BF16 router).  On the
+ * expert-grouped path the router is expanded to BF16 in the workspace (each
+ * code times its block scale, exact) for the tensor-core router, which applies
+ * scale2 to its partial logits; the workspace then holds E x H BF16 more.
  *
  * Layer configuration (the config fields hidden_size, num_experts,
  * num_experts_per_tok, moe_intermediate_size, shared_expert_intermediate_size,
