@@ -44,9 +44,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
                                                      const int32_t* __restrict__ perm,
                                                      const int32_t* __restrict__ offsets, int E,
                                                      uint16_t* __restrict__ xs, uint16_t* __restrict__ xh,
-                                                     const uint16_t* __restrict__ nw, float eps) {
+                                                     const uint16_t* __restrict__ nw, float eps, int early) {
     constexpr int kU = 8;
     pdl_wait();
+    if (early) pdl_trigger();
     const int n_routes = offsets[E];
     const int rows = n_routes + n;
     const int C8 = H >> 3;
@@ -135,8 +136,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
 // calls whose down kernel does not run the combine itself.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ ysh,
                                                       const int32_t* __restrict__ inv, int n, int H, int k,
-                                                      int has_shared, int accumulate, uint16_t* __restrict__ out) {
+                                                      int has_shared, int accumulate, uint16_t* __restrict__ out,
+                                                      int early) {
     pdl_wait();
+    if (early) pdl_trigger();
     combine_range<false>(y, ysh, inv, n, H, k, has_shared, accumulate, out,
                          blockIdx.x * (int64_t)blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
     pdl_trigger();
@@ -163,17 +166,18 @@ cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, int num_sms,
 
 cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const int32_t* perm,
                           const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, const uint16_t* norm_w,
-                          float eps, int num_sms, cudaStream_t st) {
+                          float eps, bool early, int num_sms, cudaStream_t st) {
     const int grid = 2 * num_sms;
     auto kern = fmt != MOE_W_BF16 ? (norm_w ? gather_kernel<true, true> : gather_kernel<true, false>)
                                   : (norm_w ? gather_kernel<false, true> : gather_kernel<false, false>);
-    launch_pdl(kern, grid, 256, 0, st, x, n, H, k, perm, offsets, E, xs, xh, norm_w, eps);
+    launch_pdl(kern, grid, 256, 0, st, x, n, H, k, perm, offsets, E, xs, xh, norm_w, eps, early ? 1 : 0);
     return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const float* y, const float* ysh, const int32_t* inv, int n, int H, int k,
-                           int has_shared, int accumulate, uint16_t* out, int num_sms, cudaStream_t st) {
-    launch_pdl(combine_kernel, 2 * num_sms, 256, 0, st, y, ysh, inv, n, H, k, has_shared, accumulate, out);
+                           int has_shared, int accumulate, uint16_t* out, bool early, int num_sms, cudaStream_t st) {
+    launch_pdl(combine_kernel, 2 * num_sms, 256, 0, st, y, ysh, inv, n, H, k, has_shared, accumulate, out,
+               early ? 1 : 0);
     return cudaGetLastError();
 }
 

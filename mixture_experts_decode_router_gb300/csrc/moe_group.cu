@@ -280,7 +280,7 @@ topk_group_kernel(const float* __restrict__ logits, int ns, int n, int E, int k,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                   int32_t* __restrict__ active, int32_t* __restrict__ segs, Ctrl* __restrict__ ctrl, int sw,
                   int bits, const uint16_t* __restrict__ x, const uint16_t* __restrict__ gw,
-                  float* __restrict__ sg_logit, int H, int sgx_off) {
+                  float* __restrict__ sg_logit, int H, int sgx_off, int early) {
     extern __shared__ __align__(16) float smf[];
     float* slg = smf;                                                    // [E]
     unsigned long long* skey =
@@ -293,6 +293,7 @@ topk_group_kernel(const float* __restrict__ logits, int ns, int n, int E, int k,
     __shared__ int s_last;
     const int t = blockIdx.x, tid = threadIdx.x;
     pdl_wait();
+    if (early) pdl_trigger();
     // The shared gate's logit of token t, when the layer has one and the router
     // ran on the tensor cores (which leaves that row to this kernel): the
     // threads past the key phase's E + 32 entries (at least the last warp)
@@ -383,8 +384,8 @@ bool topk_group_gate_fits(int E, int H) {
 cudaError_t launch_topk_group(const float* logits, int ns, int n, int E, int k, int routing, const float* bias, int norm,
                               float scale, int32_t* idx, float* w, int e_begin, int e_end, int32_t* counts,
                               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
-                              Ctrl* ctrl, const uint16_t* x, const uint16_t* gw, float* sg_logit, int H, int num_sms,
-                              cudaStream_t st) {
+                              Ctrl* ctrl, const uint16_t* x, const uint16_t* gw, float* sg_logit, int H, bool early,
+                              int num_sms, cudaStream_t st) {
     const int sw = seg_warps(E, n * k);
     // The routes of one top-k call have distinct experts per token: the bitmap
     // grouping when its bitmap fits.
@@ -411,7 +412,7 @@ cudaError_t launch_topk_group(const float* logits, int ns, int n, int E, int k, 
     }
     launch_pdl(kern, n, kGroupThreads, smem, st, logits, ns, n, E, k, routing, bias, norm, scale, idx, w,
                e_begin, e_end, counts, offsets, perm, inv, active, segs, ctrl, sw, bits ? 1 : 0, x, gw, sg_logit, H,
-               sgx_off);
+               sgx_off, early ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -141,8 +141,11 @@ struct QMatDev {
 // overlap the tail of the kernel before it.  Each kernel calls pdl_wait()
 // before its first global-memory access (it returns once every earlier kernel
 // on the stream has completed and its writes are visible), and pdl_trigger()
-// once its own main work is done -- never earlier, so all CTAs of a grid have
-// started before a dependent grid may take SM resources.
+// once its own main work is done.  A dependent grid launches only after every
+// CTA of this grid has signalled or exited, so every CTA has started by then;
+// the small kernels of a grouped call with at most one token per SM signal
+// right after pdl_wait(), so that the next kernel's launch and prologue
+// overlap them (it still waits for their completion before reading).
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

@@ -81,9 +81,9 @@ cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, int num_sms,
 // then the normalised ones (the norm kernel's values).
 cudaError_t launch_gather(int fmt, const uint16_t* x, int n, int H, int k, const int32_t* perm,
                           const int32_t* offsets, int E, uint16_t* xs, uint16_t* xh, const uint16_t* norm_w,
-                          float eps, int num_sms, cudaStream_t st);
+                          float eps, bool early, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const float* y, const float* ysh, const int32_t* inv, int n, int H, int k,
-                           int has_shared, int accumulate, uint16_t* out, int num_sms, cudaStream_t st);
+                           int has_shared, int accumulate, uint16_t* out, bool early, int num_sms, cudaStream_t st);
 
 // Fused single-token kernel (moe_fused_n1.cu).
 struct FusedParams {
@@ -123,10 +123,11 @@ cudaError_t launch_router(const uint16_t* x, int n, int H, const uint16_t* wr, i
 // BF16 router (rows E) for device-resident x, each multiplied by *scale when
 // scale is not null; the caller checked router_tc_fits.
 cudaError_t launch_router_tc(const uint16_t* x, int n, int H, const uint16_t* wr, int E, float* part,
-                             int32_t* err, const float* scale, cudaStream_t st);
+                             int32_t* err, const float* scale, bool early, cudaStream_t st);
 // The NVFP4 router [E, H] as BF16 (exact: E2M1 code times E4M3 block scale),
 // for the tensor-core router, which multiplies its partials by scale2.
-cudaError_t launch_router_nvfp4_expand(const QMatDev& wq, int E, int H, uint16_t* out, int num_sms, cudaStream_t st);
+cudaError_t launch_router_nvfp4_expand(const QMatDev& wq, int E, int H, uint16_t* out, bool early, int num_sms,
+                                       cudaStream_t st);
 // 2-D TMA map over a row-major [rows, cols] matrix of `esize`-byte elements (moe_grouped_tc.cu).
 bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t cols,
               uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle);
@@ -142,8 +143,8 @@ cudaError_t launch_group(const int32_t* idx, int nk, int E, int e_begin, int e_e
 cudaError_t launch_topk_group(const float* logits, int ns, int n, int E, int k, int routing, const float* bias,
                               int norm, float scale, int32_t* idx, float* w, int e_begin, int e_end, int32_t* counts,
                               int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active, int32_t* segs,
-                              Ctrl* ctrl, const uint16_t* x, const uint16_t* gw, float* sg_logit, int H, int num_sms,
-                              cudaStream_t st);
+                              Ctrl* ctrl, const uint16_t* x, const uint16_t* gw, float* sg_logit, int H, bool early,
+                              int num_sms, cudaStream_t st);
 // Whether launch_topk_group can form the shared gate's logit (gw != null) for
 // E experts and hidden size H.
 bool topk_group_gate_fits(int E, int H);

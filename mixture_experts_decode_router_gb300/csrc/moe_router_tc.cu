@@ -36,6 +36,7 @@ struct RouterTcParams {
     float* part;     // [splits][n][E]
     int32_t* err;
     const float* scale;   // a multiplier of every partial (an NVFP4 router's scale2), or null
+    int early;            // signal the dependent launch right after the wait (see pdl_trigger)
 };
 
 __global__ void __launch_bounds__(kRThreads, 1)
@@ -64,6 +65,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant
     ptx::tc_fence_after();
     const uint32_t tmem = *s_tmem;
     pdl_wait();
+    if (p.early) pdl_trigger();
 
     if (threadIdx.x == 0) {
         ptx::mbar_arrive_expect_tx(&bars[0], nsteps * (kRM + p.nt) * 128);
@@ -124,8 +126,9 @@ router_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant
 // 6 significant bits and so exact in BF16; scale2 multiplies the partials.
 // One 8-element chunk a thread.
 __global__ void __launch_bounds__(256)
-router_nvfp4_expand_kernel(const QMatDev wq, int E, int H, uint16_t* __restrict__ out) {
+router_nvfp4_expand_kernel(const QMatDev wq, int E, int H, uint16_t* __restrict__ out, int early) {
     pdl_wait();
+    if (early) pdl_trigger();
     const int C = H >> 3;
     const int64_t total = (int64_t)E * C;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -149,15 +152,16 @@ router_nvfp4_expand_kernel(const QMatDev wq, int E, int H, uint16_t* __restrict_
 
 }  // namespace
 
-cudaError_t launch_router_nvfp4_expand(const QMatDev& wq, int E, int H, uint16_t* out, int num_sms, cudaStream_t st) {
+cudaError_t launch_router_nvfp4_expand(const QMatDev& wq, int E, int H, uint16_t* out, bool early, int num_sms,
+                                       cudaStream_t st) {
     const int64_t chunks = (int64_t)E * (H / 8);
     const int blocks = (int)std::min<int64_t>((chunks + 255) / 256, (int64_t)num_sms * 8);
-    launch_pdl(router_nvfp4_expand_kernel, blocks, 256, 0, st, wq, E, H, out);
+    launch_pdl(router_nvfp4_expand_kernel, blocks, 256, 0, st, wq, E, H, out, early ? 1 : 0);
     return cudaGetLastError();
 }
 
 cudaError_t launch_router_tc(const uint16_t* x, int n, int H, const uint16_t* wr, int E, float* part,
-                             int32_t* err, const float* scale, cudaStream_t st) {
+                             int32_t* err, const float* scale, bool early, cudaStream_t st) {
     const RouterTcSplit sp = router_tc_split(H);
     const int nt = router_tc_tile(n);
     CUtensorMap wmap, xmap;
@@ -173,6 +177,7 @@ cudaError_t launch_router_tc(const uint16_t* x, int n, int H, const uint16_t* wr
     p.part = part;
     p.err = err;
     p.scale = scale;
+    p.early = early ? 1 : 0;
     const size_t smem = router_tc_smem(H, n);
     static std::mutex mu;
     static size_t configured[128] = {};
